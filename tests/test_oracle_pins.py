@@ -1,0 +1,361 @@
+"""Pins for the CPU oracle: each check ties an oracle function to something
+other than itself -- an independent library's rounding, exhaustive sorting,
+closed forms and special cases, and the invariants the pages state.
+
+Page citations: "Prox: Training-Free FFN Activation Sparsity via Approximate
+Intermediate-Channel Salience in LLMs", Abstract (two stages, shared mask from
+magnitude ranking, exact Stage 2); "PrunePath: Towards Highly Structured
+Sparse Language Models", Sec. 2.1 Eq. (1) (SwiGLU FFN) and Sec. 2.2 Eq. (2)
+(activating every block after a channel permutation is the identity).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from free_swiglu_ffn_prox_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16_bits(a) -> np.ndarray:
+    return synth.bits(torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16))
+
+
+# ------------------------------------------------------------------ formats
+def test_fp16_decode_matches_numpy_for_every_pattern(oracle_mod):
+    pats = np.arange(0, 1 << 16, 97, dtype=np.uint32).astype(np.uint16)
+    pats = np.concatenate([pats, np.array([0, 1, 0x3FF, 0x400, 0x7BFF, 0x7C00, 0x8001, 0xFBFF],
+                                          dtype=np.uint16)])
+    finite = (pats & 0x7C00) != 0x7C00
+    ours = oracle_mod.fp16_to_double(pats[finite])
+    ref = pats[finite].view(np.float16).astype(np.float64)
+    assert np.array_equal(ours, ref)
+
+
+def test_bf16_decode_matches_torch(oracle_mod):
+    pats = np.arange(0, 1 << 16, 61, dtype=np.uint32).astype(np.uint16)
+    pats = pats[(pats & 0x7F80) != 0x7F80]
+    ref = torch.from_numpy(pats.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle_mod.bf16_bits_to_f64(pats), ref)
+    assert np.array_equal(oracle_mod.bf16_to_double(pats[:300]), ref[:300])
+
+
+def test_fp16_rounding_matches_numpy(oracle_mod):
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        rng.standard_normal(2000).astype(np.float32) * np.float32(0.01),
+        rng.standard_normal(500).astype(np.float32) * np.float32(3e-6),   # subnormal range
+        rng.standard_normal(500).astype(np.float32) * np.float32(2e4),
+    ])
+    ours = oracle_mod.round_to_fp16(vals)
+    ref = vals.astype(np.float16).astype(np.float64)
+    assert np.array_equal(ours, ref)
+
+
+def test_fp16_rounding_golden_ieee_cases(oracle_mod):
+    """Hand-derived binary16 round-to-nearest-even cases (IEEE 754)."""
+    rows = []
+    with open(os.path.join(GOLDEN, "fp16_rne_cases.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                a, b = line.split()
+                rows.append((float.fromhex(a), float(b) if b != "inf" else math.inf))
+    for inp, want in rows:
+        got = oracle_mod.round_to_fp16(np.float32(inp))
+        assert got == want, (inp, got, want)
+
+
+def test_bf16_rounding_matches_torch(oracle_mod):
+    rng = np.random.default_rng(2)
+    v = (rng.standard_normal(3000) * 3).astype(np.float32)
+    v[:10] = [0.0, -0.0, 1.0, 1.00390625, 1.01171875, -2.5, 3e-39, 1e38, 255.5, 256.5]
+    ref = synth.bits(torch.from_numpy(v).to(torch.bfloat16))
+    assert np.array_equal(oracle_mod.double_to_bf16(v.astype(np.float64)), ref)
+
+
+def test_silu_closed_forms(oracle_mod):
+    assert oracle_mod.silu(0.0) == 0.0
+    ln3 = math.log(3.0)
+    assert abs(oracle_mod.silu(ln3) - 0.75 * ln3) < 1e-15   # sigma(ln 3) = 3/4
+    assert oracle_mod.silu(40.0) == 40.0                     # sigma(40) rounds to 1
+    for z in (-7.5, -1.0, 0.3, 2.0, 11.0):
+        # z*s(z) - (-z)*s(-z) = z (s(z) + s(-z)) = z
+        assert abs(oracle_mod.silu(z) - oracle_mod.silu(-z) - z) < 1e-13
+
+
+def test_keep_count_is_ceil_and_clamped(oracle_mod):
+    assert oracle_mod.keep_count(14336, 0.3) == 4301
+    assert oracle_mod.keep_count(11008, 0.3) == 3303
+    assert oracle_mod.keep_count(11008, 0.1) == 1101
+    assert oracle_mod.keep_count(28672, 0.3) == 8602
+    assert oracle_mod.keep_count(688, 0.5) == 344
+    assert oracle_mod.keep_count(4096, 0.5) == 2048
+    assert oracle_mod.keep_count(100, 1.0) == 100
+    assert oracle_mod.keep_count(100, 1e-9) == 1
+
+
+# ------------------------------------------------------------------ a0 quantizer
+def test_quantizer_recovers_exact_codes_and_power_of_two_scales(oracle_mod):
+    """W = s * q with q in [-7, 7] (one +-7 per group) and s = 2^-e is exactly
+    representable, so the quantizer must return q and s unchanged."""
+    rng = np.random.default_rng(3)
+    F, d = 24, 384
+    G = d // 128
+    q = rng.integers(-7, 8, size=(F, d))
+    for c in range(F):
+        for g in range(G):
+            q[c, g * 128 + rng.integers(0, 128)] = rng.choice([-7, 7])
+    e = rng.integers(3, 12, size=(F, G))
+    s = np.ldexp(1.0, -e)
+    w = q * np.repeat(s, 128, axis=1)
+    qo, so = oracle_mod.quantize(_bf16_bits(w))
+    assert np.array_equal(qo.astype(np.int64), q)
+    assert np.array_equal(so, s)
+
+
+def test_quantizer_invariants_on_gaussian_weights(oracle_mod):
+    rng = np.random.default_rng(4)
+    F, d = 40, 512
+    w = _bf16_bits(rng.standard_normal((F, d)) * 0.02)
+    wv = oracle_mod.bf16_bits_to_f64(w)
+    q, s = oracle_mod.quantize(w)
+    G = d // 128
+    assert q.min() >= -8 and q.max() <= 7
+    for c in range(F):
+        for g in range(G):
+            blk = wv[c, g * 128:(g + 1) * 128]
+            qq = q[c, g * 128:(g + 1) * 128].astype(np.float64)
+            amax = np.abs(blk).max()
+            sc = s[c, g]
+            # the stored scale is an fp16 value within half an fp16 ulp of amax/7
+            assert sc == np.float16(np.float32(amax) / np.float32(7.0)).astype(np.float64)
+            assert abs(sc - amax / 7) <= abs(amax / 7) * 2.0 ** -11 * 1.0001
+            # reconstruction error at most half a step (plus fp32 rounding)
+            assert np.all(np.abs(blk - sc * qq) <= sc * 0.5 * (1 + 1e-6) + 1e-12)
+            # the largest element lands on +-7
+            j = int(np.argmax(np.abs(blk)))
+            assert abs(qq[j]) == 7 and np.sign(qq[j]) == np.sign(blk[j])
+            assert np.all(np.abs(qq) <= 7)
+
+
+def test_quantizer_zero_group(oracle_mod):
+    w = np.zeros((3, 256))
+    w[1, 200] = 0.5
+    q, s = oracle_mod.quantize(_bf16_bits(w))
+    assert s[0, 0] == 0 and s[0, 1] == 0 and s[1, 0] == 0
+    assert s[1, 1] == float(np.float16(np.float32(0.5) / np.float32(7)))
+    assert q[1, 200] == 7 and np.count_nonzero(q) == 1
+
+
+# ------------------------------------------------------------------ a1 / a3 top-k
+def _brute_topk(keys, k):
+    order = sorted(range(len(keys)), key=lambda j: (-keys[j], j))
+    return np.array(sorted(order[:k]), dtype=np.int32)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_input_topk_matches_exhaustive_sort_with_ties(oracle_mod, seed):
+    rng = np.random.default_rng(10 + seed)
+    d = 128 * (1 + seed % 3)
+    # few distinct magnitudes -> many exact ties; include -0.0 and +0.0
+    pool = np.array([0.0, -0.0, 0.5, -0.5, 1.0, -1.0, 1.5, 3.0, -3.0, 7.25])
+    x = rng.choice(pool, size=d)
+    xb = _bf16_bits(x)
+    mags = [abs(v) for v in oracle_mod.bf16_bits_to_f64(xb)]
+    for kx in (1, d // 2, d - 3, d):
+        got = oracle_mod.input_topk(xb, kx)
+        assert np.array_equal(got, _brute_topk(mags, kx))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_channel_topk_matches_exhaustive_sort_with_ties(oracle_mod, seed):
+    rng = np.random.default_rng(20 + seed)
+    F = [1, 7, 64, 333, 688, 1000][seed]
+    sc = rng.integers(0, 5, size=F).astype(np.float64) * 0.25  # heavy ties
+    for k in sorted({1, max(1, F // 3), F}):
+        got = oracle_mod.channel_topk(sc, k)
+        assert np.array_equal(got, _brute_topk(list(sc), k))
+        assert len(set(got.tolist())) == k
+
+
+# ------------------------------------------------------------------ a2 proxy scores
+def test_proxy_one_hot_input_closed_form(oracle_mod):
+    """x = v e_j: g~_c = s_gate[c][j/128] q_gate[c][j] v, u~ likewise."""
+    rng = np.random.default_rng(5)
+    F, d = 50, 256
+    wg = _bf16_bits(rng.standard_normal((F, d)) * 0.02)
+    wu = _bf16_bits(rng.standard_normal((F, d)) * 0.02)
+    qg, sg = oracle_mod.quantize(wg)
+    qu, su = oracle_mod.quantize(wu)
+    j, v = 133, 3.5
+    x = np.zeros(d)
+    x[j] = v
+    xb = _bf16_bits(x)
+    kept = oracle_mod.input_topk(xb, d // 2)
+    assert j in kept
+    g, u, score = oracle_mod.proxy_scores(qg, sg, qu, su, xb, kept)
+    g_ref = sg[:, j // 128] * qg[:, j] * v
+    u_ref = su[:, j // 128] * qu[:, j] * v
+    assert np.array_equal(g, g_ref) and np.array_equal(u, u_ref)
+    want = np.abs(g_ref / (1 + np.exp(-g_ref)) * u_ref)
+    assert np.allclose(score, want, rtol=1e-14, atol=0)
+
+
+def test_proxy_equals_exact_state_for_quantization_exact_weights(oracle_mod):
+    """With W = s*q exactly and x supported on exactly d/2 entries, the input
+    keep drops only zeros and the proxy state is the exact SwiGLU state, so
+    the score is |h| of Eq. (1) and the mask is the exact top-k of |h|."""
+    rng = np.random.default_rng(6)
+    F, d = 64, 256
+    G = d // 128
+
+    def exact_w():
+        q = rng.integers(-7, 8, size=(F, d))
+        for c in range(F):
+            for g in range(G):
+                q[c, g * 128] = 7
+        return q * np.repeat(np.ldexp(1.0, -rng.integers(4, 8, size=(F, G))), 128, axis=1)
+
+    wg, wu = exact_w(), exact_w()
+    wd = rng.standard_normal((d, F)) * 0.02
+    x = np.zeros(d)
+    support = rng.choice(d, size=d // 2, replace=False)
+    x[support] = rng.choice([-2.0, -1.0, -0.5, 0.25, 1.0, 3.0], size=d // 2)
+    wgb, wub, wdb, xb = _bf16_bits(wg), _bf16_bits(wu), _bf16_bits(wd), _bf16_bits(x)
+    qg, sg = oracle_mod.quantize(wgb)
+    qu, su = oracle_mod.quantize(wub)
+    kept = oracle_mod.input_topk(xb, d // 2)
+    assert np.array_equal(np.sort(support), kept)
+    g, u, score = oracle_mod.proxy_scores(qg, sg, qu, su, xb, kept)
+    xv = oracle_mod.bf16_bits_to_f64(xb)
+    assert np.allclose(g, oracle_mod.bf16_bits_to_f64(wgb) @ xv, rtol=1e-13, atol=1e-13)
+    assert np.allclose(u, oracle_mod.bf16_bits_to_f64(wub) @ xv, rtol=1e-13, atol=1e-13)
+    h, _ = oracle_mod.dense_ffn(wgb, wub, wdb, xb)
+    assert np.allclose(score, np.abs(h), rtol=1e-12, atol=1e-12)
+
+
+def test_proxy_uses_only_the_kept_inputs(oracle_mod):
+    """Scores from x over its kept set equal scores from x~ (x zeroed outside
+    the kept set) with every input kept."""
+    rng = np.random.default_rng(7)
+    F, d = 40, 384
+    wg = _bf16_bits(rng.standard_normal((F, d)) * 0.02)
+    wu = _bf16_bits(rng.standard_normal((F, d)) * 0.02)
+    qg, sg = oracle_mod.quantize(wg)
+    qu, su = oracle_mod.quantize(wu)
+    xb = synth.bits(synth.make_x(d, 4, 20.0, seed=3))
+    kept = oracle_mod.input_topk(xb, d // 2)
+    xt = np.zeros(d, dtype=np.uint16)
+    xt[kept] = xb[kept]
+    a = oracle_mod.proxy_scores(qg, sg, qu, su, xb, kept)
+    b = oracle_mod.proxy_scores(qg, sg, qu, su, xt, np.arange(d, dtype=np.int32))
+    for p, r in zip(a, b):
+        assert np.allclose(p, r, rtol=1e-13, atol=1e-15)
+    # and x~ is not x: dropping the kept set changes the state
+    c = oracle_mod.proxy_scores(qg, sg, qu, su, xb, np.arange(d, dtype=np.int32))
+    assert not np.allclose(a[0], c[0])
+
+
+# ------------------------------------------------------------------ Stage 2 / dense
+def _tiny_layer(seed=0, F=96, d=256):
+    rng = np.random.default_rng(100 + seed)
+    wg = _bf16_bits(rng.standard_normal((F, d)) * 0.05)
+    wu = _bf16_bits(rng.standard_normal((F, d)) * 0.05)
+    wd = _bf16_bits(rng.standard_normal((d, F)) * 0.05)
+    xb = synth.bits(synth.make_x(d, 2, 20.0, seed=seed))
+    return wg, wu, wd, xb
+
+
+def test_keep_fraction_one_equals_dense(oracle_mod):
+    """Every channel selected: Stage 2 is the dense FFN of Eq. (1)."""
+    wg, wu, wd, xb = _tiny_layer(1)
+    r = oracle_mod.prox_ffn(wg, wu, wd, xb, 1.0)
+    h, y = oracle_mod.dense_ffn(wg, wu, wd, xb)
+    assert r["k"] == wg.shape[0]
+    assert np.array_equal(r["idx"], np.arange(wg.shape[0]))
+    assert np.allclose(r["y"], y, rtol=1e-13, atol=1e-13)
+    assert np.allclose(r["h"], h, rtol=1e-13, atol=1e-13)
+
+
+def test_sparse_equals_dense_with_unselected_channels_zeroed(oracle_mod):
+    wg, wu, wd, xb = _tiny_layer(2)
+    r = oracle_mod.prox_ffn(wg, wu, wd, xb, 0.3)
+    h, _ = oracle_mod.dense_ffn(wg, wu, wd, xb)
+    mask = np.zeros(wg.shape[0])
+    mask[r["idx"]] = 1.0
+    y_ref = oracle_mod.bf16_bits_to_f64(wd) @ (h * mask)   # library matmul
+    assert np.allclose(r["y"], y_ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(r["h"], h[r["idx"]], rtol=1e-13, atol=1e-13)
+
+
+def test_channel_permutation_identity(oracle_mod):
+    """Eq. (2): permuting channels in all three matrices leaves the FFN and,
+    with the mask permuted alike, the sparse FFN unchanged."""
+    wg, wu, wd, xb = _tiny_layer(3)
+    F = wg.shape[0]
+    perm = np.random.default_rng(9).permutation(F)
+    _, y = oracle_mod.dense_ffn(wg, wu, wd, xb)
+    _, yp = oracle_mod.dense_ffn(wg[perm], wu[perm], wd[:, perm], xb)
+    assert np.allclose(y, yp, rtol=1e-12, atol=1e-12)
+    r = oracle_mod.prox_ffn(wg, wu, wd, xb, 0.25)
+    rp = oracle_mod.prox_ffn(wg[perm], wu[perm], wd[:, perm], xb, 0.25)
+    inv = np.argsort(perm)
+    assert np.array_equal(np.sort(perm[rp["idx"]]), r["idx"])
+    assert np.allclose(r["y"], rp["y"], rtol=1e-12, atol=1e-12)
+    assert np.array_equal(np.sort(inv[r["idx"]]), rp["idx"])
+
+
+def test_large_gate_reduces_to_matrix_products(oracle_mod):
+    """x = e_0, W_up[:, 0] = 1 and W_gate[:, 0] = a_c: u_c = 1, g_c = a_c.
+    For a_c >= 40, silu(a_c) = a_c in fp64 and y = W_down a; for a_c <= -40
+    silu(a_c) ~ 0 and y ~ 0 (catches a sign flip in silu or in the gate)."""
+    rng = np.random.default_rng(11)
+    F, d = 32, 128
+    a = rng.choice([40.0, 48.0, 64.0, 96.0], size=F)
+    wg = np.zeros((F, d))
+    wg[:, 0] = a
+    wu = np.zeros((F, d))
+    wu[:, 0] = 1.0
+    wd = rng.standard_normal((d, F)) * 0.1
+    x = np.zeros(d)
+    x[0] = 1.0
+    b = [_bf16_bits(m) for m in (wg, wu, wd, x)]
+    _, y = oracle_mod.dense_ffn(*b)
+    assert np.allclose(y, oracle_mod.bf16_bits_to_f64(b[2]) @ a, rtol=1e-14, atol=1e-14)
+    wg[:, 0] = -a
+    _, y2 = oracle_mod.dense_ffn(_bf16_bits(wg), b[1], b[2], b[3])
+    assert np.max(np.abs(y2)) < 1e-12
+
+
+def test_prox_composition_is_the_stage_functions_in_order(oracle_mod):
+    wg, wu, wd, xb = _tiny_layer(4, F=200, d=384)
+    r = oracle_mod.prox_ffn(wg, wu, wd, xb, 0.4)
+    kept = oracle_mod.input_topk(xb, r["kx"])
+    assert np.array_equal(kept, r["kept"])
+    px = oracle_mod.Proxy(wg, wu)
+    _, _, sc = oracle_mod.proxy_scores(px.q_gate, px.s_gate, px.q_up, px.s_up, xb, kept)
+    assert np.array_equal(sc, r["score"])
+    idx = oracle_mod.channel_topk(sc, r["k"])
+    assert np.array_equal(idx, r["idx"])
+    _, y = oracle_mod.sparse_ffn(wg, wu, wd, xb, idx)
+    assert np.array_equal(y, r["y"])
+
+
+def test_residual_rmsnorm_closed_forms(oracle_mod):
+    d = 256
+    x = np.zeros(d, dtype=np.uint16)
+    out = oracle_mod.residual_rmsnorm(x, np.full(d, 3.0))
+    # z = 3 everywhere: 3 / sqrt(9 + 1e-6) rounds to 1.0 in bf16
+    assert np.all(out == 0x3F80)
+    rng = np.random.default_rng(12)
+    xb = _bf16_bits(rng.standard_normal(d))
+    y = rng.standard_normal(d)
+    o1 = oracle_mod.bf16_bits_to_f64(oracle_mod.residual_rmsnorm(xb, y))
+    rms = math.sqrt(np.mean(o1 ** 2))
+    assert abs(rms - 1.0) < 5e-3
+    z = oracle_mod.bf16_bits_to_f64(xb) + y
+    assert np.all(np.sign(o1[np.abs(z) > 1e-3]) == np.sign(z[np.abs(z) > 1e-3]))
