@@ -1,0 +1,250 @@
+// prox_abi.cu -- the extern "C" entry points declared in include/prox.h:
+// argument checks, workspace carving, and the launch sequence of the Prox
+// decode step ("Prox", Abstract):
+//   1. input sparsity           (top-|x|, prox_select.cu)
+//   2. proxy GEMV                (int4 proxy x kept inputs, prox_proxy.cu)
+//   3. channel mask              (top-k of |silu(g~) u~|, prox_select.cu)
+//   4. exact Stage 2             (gate|up gather + silu*mul + down, prox_gather.cu)
+#include <math.h>
+#include <stdlib.h>
+
+#include <new>
+
+#include "prox_internal.cuh"
+
+struct prox_layer {
+    int d_model, d_ff, Fp;
+    int device, num_sms;
+    const uint8_t* codes;
+    const __half2* scales;
+    const __nv_bfloat16* gateup;
+    const __nv_bfloat16* down_t;
+    prox::Workspace ws;
+};
+
+namespace prox {
+
+static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+size_t workspace_bytes(int d, int F) {
+    const int Fp = padded_ff(F);
+    return align256(256) + align256((size_t)d * 4) + align256((size_t)Fp * 8) +
+           align256((size_t)Fp * 4) + align256((size_t)F * 4);
+}
+
+Workspace carve_workspace(void* base, int d, int F) {
+    const int Fp = padded_ff(F);
+    uint8_t* p = static_cast<uint8_t*>(base);
+    Workspace w;
+    w.status = reinterpret_cast<int*>(p);
+    p += align256(256);
+    w.kept = reinterpret_cast<uint32_t*>(p);
+    p += align256((size_t)d * 4);
+    w.acc = reinterpret_cast<float2*>(p);
+    p += align256((size_t)Fp * 8);
+    w.scores = reinterpret_cast<float*>(p);
+    p += align256((size_t)Fp * 4);
+    w.idx = reinterpret_cast<int32_t*>(p);
+    return w;
+}
+
+}  // namespace prox
+
+namespace {
+
+bool shape_ok(int d, int F) {
+    return d >= prox::kGroup && d <= prox::kMaxDModel && d % prox::kGroup == 0 && F >= 1 &&
+           F <= prox::kMaxDff;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool frac_ok(float f) { return isfinite(f) && f > 0.0f && f <= 1.0f; }
+
+prox_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PROX_OK : PROX_ERR_CUDA; }
+
+// The decode step on a checked layer.  kept_out/scores_out/idx_out/h_out
+// are the debug outputs (NULL on the hot path).
+prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, float input_keep,
+                     float* y, int32_t* kept_out, float* scores_out, int32_t* idx_out,
+                     float* h_out, cudaStream_t stream, long long limit_ns, int inject) {
+    const int d = L->d_model, F = L->d_ff;
+    const int kx = prox_keep_count(d, input_keep);
+    const int k = prox_keep_count(F, keep_fraction);
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    cudaError_t e = prox::launch_input_select(xb, d, kx, L->ws, kept_out, y, stream);
+    if (e == cudaSuccess)
+        e = prox::launch_proxy_gemv(L->codes, L->scales, L->ws, d, F, kx, L->num_sms, limit_ns,
+                                    inject == 1, stream);
+    if (e == cudaSuccess) e = prox::launch_channel_select(L->ws, F, k, scores_out, stream);
+    if (e == cudaSuccess)
+        e = prox::launch_gather_ffn(L->gateup, L->down_t, xb, L->ws.idx, k, d, y, h_out,
+                                    L->ws.acc, L->Fp, L->ws.status, L->num_sms, limit_ns,
+                                    inject == 2, stream);
+    if (e == cudaSuccess && idx_out)
+        e = cudaMemcpyAsync(idx_out, L->ws.idx, (size_t)k * sizeof(int32_t),
+                            cudaMemcpyDeviceToDevice, stream);
+    return cuda_status(e);
+}
+
+prox_status check_call(const prox_layer* L, const void* x, const float* y) {
+    if (!L || !x || !y) return PROX_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return PROX_ERR_MISALIGNED;
+    return PROX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int prox_keep_count(int n, float frac) {
+    if (n < 1 || !frac_ok(frac)) return 0;
+    double k = ceil((double)frac * (double)n);
+    if (k < 1.0) k = 1.0;
+    if (k > (double)n) k = (double)n;
+    return (int)k;
+}
+
+const char* prox_status_string(prox_status s) {
+    switch (s) {
+        case PROX_OK: return "ok";
+        case PROX_ERR_INVALID_ARG: return "invalid argument";
+        case PROX_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case PROX_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+        case PROX_ERR_CUDA: return "CUDA runtime error";
+        case PROX_ERR_TIMEOUT: return "bounded device wait ran out";
+        case PROX_ERR_DEVICE_CHECK: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+prox_status prox_query_sizes(int d_model, int d_ff, prox_sizes* out) {
+    if (!out) return PROX_ERR_INVALID_ARG;
+    if (!shape_ok(d_model, d_ff)) return PROX_ERR_UNSUPPORTED_SHAPE;
+    const size_t Fp = (size_t)prox::padded_ff(d_ff);
+    out->proxy_codes = (size_t)d_model * Fp;
+    out->proxy_scales = (size_t)(d_model / prox::kGroup) * Fp * 4;
+    out->gateup = (size_t)d_ff * 2 * d_model * 2;
+    out->down_t = (size_t)d_ff * d_model * 2;
+    out->workspace = prox::workspace_bytes(d_model, d_ff);
+    return PROX_OK;
+}
+
+prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, const void* w_up,
+                         const void* w_down, void* proxy_codes, void* proxy_scales,
+                         void* gateup, void* down_t, void* workspace, prox_stream_t stream,
+                         prox_layer** out) {
+    if (!out) return PROX_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!shape_ok(d_model, d_ff)) return PROX_ERR_UNSUPPORTED_SHAPE;
+    const void* ptrs[] = {w_gate, w_up, w_down, proxy_codes, proxy_scales, gateup, down_t, workspace};
+    for (const void* p : ptrs) {
+        if (!p) return PROX_ERR_INVALID_ARG;
+        if (!aligned16(p)) return PROX_ERR_MISALIGNED;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = prox::proxy_configure();
+    if (e == cudaSuccess) e = prox::gather_configure(d_model);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(workspace, 0, prox::workspace_bytes(d_model, d_ff), s);
+    if (e == cudaSuccess)
+        e = prox::launch_prepare(d_model, d_ff, static_cast<const __nv_bfloat16*>(w_gate),
+                                 static_cast<const __nv_bfloat16*>(w_up),
+                                 static_cast<const __nv_bfloat16*>(w_down),
+                                 static_cast<uint8_t*>(proxy_codes),
+                                 static_cast<__half2*>(proxy_scales),
+                                 static_cast<__nv_bfloat16*>(gateup),
+                                 static_cast<__nv_bfloat16*>(down_t), s);
+    if (e != cudaSuccess) return PROX_ERR_CUDA;
+    prox_layer* L = new (std::nothrow) prox_layer;
+    if (!L) return PROX_ERR_INVALID_ARG;
+    L->d_model = d_model;
+    L->d_ff = d_ff;
+    L->Fp = prox::padded_ff(d_ff);
+    L->device = dev;
+    L->num_sms = sms;
+    L->codes = static_cast<const uint8_t*>(proxy_codes);
+    L->scales = static_cast<const __half2*>(proxy_scales);
+    L->gateup = static_cast<const __nv_bfloat16*>(gateup);
+    L->down_t = static_cast<const __nv_bfloat16*>(down_t);
+    L->ws = prox::carve_workspace(workspace, d_model, d_ff);
+    *out = L;
+    return PROX_OK;
+}
+
+prox_status prox_ffn_ex(const prox_layer* layer, const void* x, float keep_fraction,
+                        float input_keep, float* y, prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    if (!frac_ok(keep_fraction) || !frac_ok(input_keep)) return PROX_ERR_INVALID_ARG;
+    return run_prox(layer, x, keep_fraction, input_keep, y, nullptr, nullptr, nullptr, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0);
+}
+
+prox_status prox_ffn(const prox_layer* layer, const void* x, float keep_fraction, float* y,
+                     prox_stream_t stream) {
+    return prox_ffn_ex(layer, x, keep_fraction, 0.5f, y, stream);
+}
+
+prox_status prox_dense_ffn(const prox_layer* layer, const void* x, float* y,
+                           prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(y, 0, (size_t)layer->d_model * sizeof(float), s);
+    if (e == cudaSuccess)
+        e = prox::launch_gather_ffn(layer->gateup, layer->down_t, static_cast<const uint16_t*>(x),
+                                    nullptr, layer->d_ff, layer->d_model, y, nullptr, nullptr, 0,
+                                    layer->ws.status, layer->num_sms, prox::kWaitLimitNs, 0, s);
+    return cuda_status(e);
+}
+
+prox_status prox_ffn_debug(const prox_layer* layer, const void* x, float keep_fraction,
+                           float input_keep, float* y, int32_t* kept_inputs, float* scores,
+                           int32_t* idx, float* h, prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    if (!frac_ok(keep_fraction) || !frac_ok(input_keep)) return PROX_ERR_INVALID_ARG;
+    const void* outs[] = {kept_inputs, scores, idx, h};
+    for (const void* p : outs)
+        if (p && !aligned16(p)) return PROX_ERR_MISALIGNED;
+    return run_prox(layer, x, keep_fraction, input_keep, y, kept_inputs, scores, idx, h,
+                    reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0);
+}
+
+prox_status prox_residual_rmsnorm(int d_model, const void* x, const float* y, float eps,
+                                  void* x_next, prox_stream_t stream) {
+    if (!x || !y || !x_next) return PROX_ERR_INVALID_ARG;
+    if (d_model < 1 || d_model > prox::kMaxDModel) return PROX_ERR_UNSUPPORTED_SHAPE;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return PROX_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y) || !aligned16(x_next)) return PROX_ERR_MISALIGNED;
+    return cuda_status(prox::launch_residual_rmsnorm(d_model, static_cast<const uint16_t*>(x), y,
+                                                     eps, static_cast<uint16_t*>(x_next),
+                                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+prox_status prox_get_status(const prox_layer* layer, prox_stream_t stream) {
+    if (!layer) return PROX_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, layer->ws.status, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(layer->ws.status, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return PROX_ERR_CUDA;
+    return (prox_status)v;
+}
+
+prox_status prox_layer_info(const prox_layer* layer, int* d_model, int* d_ff) {
+    if (!layer) return PROX_ERR_INVALID_ARG;
+    if (d_model) *d_model = layer->d_model;
+    if (d_ff) *d_ff = layer->d_ff;
+    return PROX_OK;
+}
+
+void prox_destroy(prox_layer* layer) { delete layer; }
+
+}  // extern "C"

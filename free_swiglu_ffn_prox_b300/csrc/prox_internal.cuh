@@ -1,0 +1,162 @@
+// prox_internal.cuh -- shared device helpers and launcher declarations for
+// libprox (sm_103a).  Inline PTX for mbarriers and bulk (TMA) copies, the
+// bounded waits every kernel uses, and the workspace layout.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "prox.h"
+
+namespace prox {
+
+constexpr int kMaxDModel = 16384;
+constexpr int kMaxDff = 32768;
+constexpr int kGroup = 128;       // proxy quantization group along d_model
+constexpr int kChanAlign = 64;    // Fp = d_ff rounded up to this
+constexpr long long kWaitLimitNs = 2000000000LL;  // 2 s per bounded wait
+
+inline int padded_ff(int d_ff) { return (d_ff + kChanAlign - 1) / kChanAlign * kChanAlign; }
+
+// Workspace carve-out (offsets in bytes, each 256-aligned).
+struct Workspace {
+    int* status;      // [0] device status word, [1] input prescale exponent
+    uint32_t* kept;   // [d] packed (j << 16 | fp16 bits of x_j * 2^shift)
+    float2* acc;      // [Fp] proxy (g~, u~) accumulators, zero between calls
+    float* scores;    // [Fp]
+    int32_t* idx;     // [d_ff] selected channels
+};
+
+size_t workspace_bytes(int d_model, int d_ff);
+Workspace carve_workspace(void* base, int d_model, int d_ff);
+
+// ----------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes mbarrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the given phase parity of an mbarrier, giving up after
+// limit_ns or as soon as *abort (when given) becomes non-zero.  Returns
+// true when the phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit_ns, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (abort && *abort) return false;
+            if ((long long)(global_timer_ns() - t0) > limit_ns) return false;
+        }
+    }
+}
+
+// One bulk (TMA, non-tensor) global->shared copy completing on an mbarrier.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for weights that are read once per call.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
+    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(a), "f"(b)
+                 : "memory");
+}
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+// ----------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error.  All run on `stream`.
+cudaError_t launch_prepare(int d, int F, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
+                           const __nv_bfloat16* w_down, uint8_t* codes, __half2* scales,
+                           __nv_bfloat16* gateup, __nv_bfloat16* down_t, cudaStream_t stream);
+
+cudaError_t launch_input_select(const uint16_t* x, int d, int kx, const Workspace& ws,
+                                int32_t* kept_out, float* y_zero, cudaStream_t stream);
+
+struct ProxyGeom {
+    int tiles, slices;
+};
+ProxyGeom proxy_geometry(int F, int kx, int num_sms);
+cudaError_t proxy_configure();
+cudaError_t launch_proxy_gemv(const uint8_t* codes, const __half2* scales, const Workspace& ws,
+                              int d, int F, int kx, int num_sms, long long wait_limit_ns,
+                              int inject_stall, cudaStream_t stream);
+
+cudaError_t launch_channel_select(const Workspace& ws, int F, int k, float* scores_out,
+                                  cudaStream_t stream);
+
+cudaError_t gather_configure(int d);
+cudaError_t launch_gather_ffn(const __nv_bfloat16* gateup, const __nv_bfloat16* down_t,
+                              const uint16_t* x, const int32_t* idx, int k, int d, float* y,
+                              float* h_out, float2* acc_zero, int acc_n, int* status,
+                              int num_sms, long long wait_limit_ns, int inject_stall,
+                              cudaStream_t stream);
+
+cudaError_t launch_residual_rmsnorm(int d, const uint16_t* x, const float* y, float eps,
+                                    uint16_t* x_next, cudaStream_t stream);
+
+}  // namespace prox

@@ -1,0 +1,241 @@
+"""Thin Python binding of libprox (include/prox.h), same entry-point names.
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and streams.  There
+is no fallback: if ``libprox.so`` is missing or cannot be loaded, importing
+the entry points raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libprox.so")
+
+PROX_OK = 0
+PROX_ERR_INVALID_ARG = 1
+PROX_ERR_UNSUPPORTED_SHAPE = 2
+PROX_ERR_MISALIGNED = 3
+PROX_ERR_CUDA = 4
+PROX_ERR_TIMEOUT = 5
+PROX_ERR_DEVICE_CHECK = 6
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ProxError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = int(code)
+        super().__init__(f"{what}: {prox_status_string(code)} (status {code})")
+
+
+class _Sizes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("proxy_codes", "proxy_scales", "gateup", "down_t", "workspace")]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libprox.so not found at {LIB_PATH}; build it with "
+                "`python -m free_swiglu_ffn_prox_b300.build` (no CPU fallback exists)")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        sig = {
+            "prox_query_sizes": (i32, [i32, i32, ctypes.POINTER(_Sizes)]),
+            "prox_prepare": (i32, [i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                   ctypes.POINTER(vp)]),
+            "prox_ffn": (i32, [vp, vp, f32, vp, vp]),
+            "prox_ffn_ex": (i32, [vp, vp, f32, f32, vp, vp]),
+            "prox_dense_ffn": (i32, [vp, vp, vp, vp]),
+            "prox_ffn_debug": (i32, [vp, vp, f32, f32, vp, vp, vp, vp, vp, vp]),
+            "prox_residual_rmsnorm": (i32, [i32, vp, vp, f32, vp, vp]),
+            "prox_get_status": (i32, [vp, vp]),
+            "prox_layer_info": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
+            "prox_keep_count": (i32, [i32, f32]),
+            "prox_destroy": (None, [vp]),
+            "prox_status_string": (ctypes.c_char_p, [i32]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def loaded_library_path() -> str:
+    _load()
+    return LIB_PATH
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p | None:
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(code: int, what: str) -> None:
+    if code != PROX_OK:
+        raise ProxError(code, what)
+
+
+def _need(t: torch.Tensor, dtype, shape, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ---------------------------------------------------------------- entry points
+def prox_status_string(code: int) -> str:
+    return _load().prox_status_string(int(code)).decode()
+
+
+def prox_keep_count(n: int, frac: float) -> int:
+    return int(_load().prox_keep_count(int(n), float(frac)))
+
+
+def prox_query_sizes(d_model: int, d_ff: int) -> dict:
+    s = _Sizes()
+    _check(_load().prox_query_sizes(int(d_model), int(d_ff), ctypes.byref(s)), "prox_query_sizes")
+    return {n: int(getattr(s, n)) for n, _ in _Sizes._fields_}
+
+
+class ProxLayer:
+    """A prepared layer: the device buffers (owned here, as torch tensors)
+    and the library's host handle."""
+
+    def __init__(self, d_model, d_ff, bufs, handle, device):
+        self.d_model, self.d_ff = int(d_model), int(d_ff)
+        self.bufs = bufs
+        self.handle = handle
+        self.device = device
+
+    def close(self):
+        if self.handle is not None and _lib is not None:
+            _lib.prox_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def prox_prepare(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
+                 stream=None) -> ProxLayer:
+    """Builds the proxy and Stage-2 layouts of one layer (see prox.h)."""
+    lib = _load()
+    if w_gate.dim() != 2:
+        raise ValueError("w_gate must be [d_ff, d_model]")
+    d_ff, d_model = w_gate.shape
+    for t, shp, nm in ((w_gate, (d_ff, d_model), "w_gate"), (w_up, (d_ff, d_model), "w_up"),
+                       (w_down, (d_model, d_ff), "w_down")):
+        _need(t, torch.bfloat16, shp, nm)
+    sz = prox_query_sizes(d_model, d_ff)
+    dev = w_gate.device
+    bufs = {n: torch.empty(sz[n], dtype=torch.uint8, device=dev) for n in sz}
+    h = ctypes.c_void_p()
+    with torch.cuda.device(dev):
+        _check(lib.prox_prepare(d_model, d_ff, _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                _ptr(bufs["proxy_codes"]), _ptr(bufs["proxy_scales"]),
+                                _ptr(bufs["gateup"]), _ptr(bufs["down_t"]),
+                                _ptr(bufs["workspace"]), _stream(stream), ctypes.byref(h)),
+               "prox_prepare")
+    return ProxLayer(d_model, d_ff, bufs, h, dev)
+
+
+def _x_y(layer: ProxLayer, x, y):
+    _need(x, torch.bfloat16, (layer.d_model,), "x")
+    if y is None:
+        y = torch.empty(layer.d_model, dtype=torch.float32, device=x.device)
+    _need(y, torch.float32, (layer.d_model,), "y")
+    return y
+
+
+def prox_ffn(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, y=None, stream=None):
+    y = _x_y(layer, x, y)
+    _check(_load().prox_ffn(layer.handle, _ptr(x), float(keep_fraction), _ptr(y), _stream(stream)),
+           "prox_ffn")
+    return y
+
+
+def prox_ffn_ex(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, input_keep: float,
+                y=None, stream=None):
+    y = _x_y(layer, x, y)
+    _check(_load().prox_ffn_ex(layer.handle, _ptr(x), float(keep_fraction), float(input_keep),
+                               _ptr(y), _stream(stream)), "prox_ffn_ex")
+    return y
+
+
+def prox_dense_ffn(layer: ProxLayer, x: torch.Tensor, y=None, stream=None):
+    y = _x_y(layer, x, y)
+    _check(_load().prox_dense_ffn(layer.handle, _ptr(x), _ptr(y), _stream(stream)),
+           "prox_dense_ffn")
+    return y
+
+
+def prox_ffn_debug(layer: ProxLayer, x: torch.Tensor, keep_fraction: float,
+                   input_keep: float = 0.5, stream=None) -> dict:
+    """prox_ffn_ex plus kept inputs, scores, channel list and h (device tensors)."""
+    y = _x_y(layer, x, None)
+    dev = x.device
+    kx = prox_keep_count(layer.d_model, input_keep)
+    k = prox_keep_count(layer.d_ff, keep_fraction)
+    kept = torch.empty(max(kx, 1), dtype=torch.int32, device=dev)
+    scores = torch.empty(layer.d_ff, dtype=torch.float32, device=dev)
+    idx = torch.empty(max(k, 1), dtype=torch.int32, device=dev)
+    h = torch.empty(max(k, 1), dtype=torch.float32, device=dev)
+    _check(_load().prox_ffn_debug(layer.handle, _ptr(x), float(keep_fraction), float(input_keep),
+                                  _ptr(y), _ptr(kept), _ptr(scores), _ptr(idx), _ptr(h),
+                                  _stream(stream)), "prox_ffn_debug")
+    return {"y": y, "kept": kept[:kx], "scores": scores, "idx": idx[:k], "h": h[:k],
+            "kx": kx, "k": k}
+
+
+def prox_residual_rmsnorm(x: torch.Tensor, y: torch.Tensor, eps: float = 1e-6, out=None,
+                          stream=None):
+    d = x.numel()
+    _need(x, torch.bfloat16, (d,), "x")
+    _need(y, torch.float32, (d,), "y")
+    if out is None:
+        out = torch.empty(d, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, (d,), "out")
+    _check(_load().prox_residual_rmsnorm(d, _ptr(x), _ptr(y), float(eps), _ptr(out),
+                                         _stream(stream)), "prox_residual_rmsnorm")
+    return out
+
+
+def prox_get_status(layer: ProxLayer, stream=None) -> int:
+    return int(_load().prox_get_status(layer.handle, _stream(stream)))
+
+
+def prox_layer_info(layer: ProxLayer):
+    a, b = ctypes.c_int(), ctypes.c_int()
+    _check(_load().prox_layer_info(layer.handle, ctypes.byref(a), ctypes.byref(b)), "prox_layer_info")
+    return a.value, b.value
+
+
+def prox_destroy(layer: ProxLayer) -> None:
+    layer.close()

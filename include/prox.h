@@ -1,0 +1,186 @@
+/*
+ * prox.h -- C ABI of libprox: two-stage sparse SwiGLU FFN decode (batch 1)
+ * on NVIDIA B300 (sm_103a).
+ *
+ * The method: "Prox: Training-Free FFN Activation Sparsity via Approximate
+ * Intermediate-Channel Salience in LLMs", Abstract.  Stage 1 builds one
+ * channel mask, shared by all three projections, from a sparsified input and
+ * quantized proxy weights, keeping the channels whose approximate
+ * intermediate-state magnitude ranks highest.  Stage 2 computes the selected
+ * channels exactly.  The FFN itself is the SwiGLU block of "PrunePath:
+ * Towards Highly Structured Sparse Language Models", Sec. 2.1 Eq. (1):
+ *     FFN(x) = W_down ( silu(W_gate x) (.) (W_up x) )
+ * (written there with x as a row vector; this library takes the nn.Linear
+ * layouts below, i.e. the same product transposed).
+ *
+ * Readings the pages leave open, fixed here:
+ *   - proxy: int4, symmetric, one fp16 scale per (channel, 128 input dims),
+ *     s = fp16_rne(fl32(amax / 7)), q = clamp(rne(fl32(w / s)), -8, 7);
+ *   - input sparsity: keep the ceil(input_keep * d) entries of largest |x|
+ *     (ties -> lower index); default input_keep = 0.5;
+ *   - ranking signal: score_c = |silu(g~_c) * u~_c| from the proxy state;
+ *   - keep count: k = ceil(keep_fraction * d_ff) clamped to [1, d_ff]; the k
+ *     highest scores win, ties -> lower channel;
+ *   - Stage 2 uses the full (unsparsified) x; h and y are fp32.
+ *
+ * Conventions for every call:
+ *   - Device memory is allocated and owned by the caller.  The library never
+ *     allocates device memory and keeps no pointer to the source weights
+ *     after prox_prepare returns.
+ *   - Every call is ordered on the given CUDA stream (a cudaStream_t; NULL
+ *     means the legacy default stream) and returns without synchronising,
+ *     except prox_get_status.  prox_ffn needs no host read-back, so a
+ *     sequence of calls can be captured in a CUDA graph.
+ *   - Arguments are checked before any work is queued; a failed check
+ *     returns an error code and queues nothing.  Launch failures return
+ *     PROX_ERR_CUDA.  Faults found on the device (a bounded wait that ran
+ *     out) are recorded in the layer's status word, read by
+ *     prox_get_status.  No call traps, aborts or throws.
+ *   - All device pointers must be 16-byte aligned.
+ *   - Calls that share one prox_layer use its workspace and must be ordered
+ *     with respect to each other (one stream, or events); calls on
+ *     different layers are independent.
+ *   - Shapes: d_model a multiple of 128 in [128, 16384]; d_ff in [1, 32768].
+ *   - Inputs must be finite (no NaN or Inf in x or the weights).
+ */
+#ifndef PROX_H
+#define PROX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of the ABI are exported even when the library is built with
+ * hidden default visibility. */
+#if defined(__GNUC__)
+#define PROX_API __attribute__((visibility("default")))
+#else
+#define PROX_API
+#endif
+
+typedef struct CUstream_st* prox_stream_t; /* identical to cudaStream_t */
+
+typedef enum prox_status {
+    PROX_OK = 0,
+    PROX_ERR_INVALID_ARG = 1,       /* null pointer, bad fraction, bad handle */
+    PROX_ERR_UNSUPPORTED_SHAPE = 2, /* d_model / d_ff outside the limits above */
+    PROX_ERR_MISALIGNED = 3,        /* a device pointer is not 16-byte aligned */
+    PROX_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+    PROX_ERR_TIMEOUT = 5,           /* a bounded on-device wait ran out */
+    PROX_ERR_DEVICE_CHECK = 6       /* an on-device consistency check failed */
+} prox_status;
+
+/* Byte sizes of the caller-allocated device buffers for one layer. */
+typedef struct prox_sizes {
+    size_t proxy_codes;  /* int4 proxy codes, layout below */
+    size_t proxy_scales; /* fp16 proxy scales, layout below */
+    size_t gateup;       /* bf16 gate|up rows, [d_ff][2][d_model] */
+    size_t down_t;       /* bf16 W_down transposed, [d_ff][d_model] */
+    size_t workspace;    /* per-layer scratch used by prox_ffn */
+} prox_sizes;
+
+/* Opaque host-side handle: shapes plus the device pointers given to
+ * prox_prepare.  Allocated by prox_prepare, released by prox_destroy. */
+typedef struct prox_layer prox_layer;
+
+/*
+ * Device layouts written by prox_prepare (F = d_ff, d = d_model,
+ * Fp = F rounded up to a multiple of 64, G = d / 128):
+ *   proxy_codes  uint8 [d][Fp]: byte (j, c) = (q_gate[c][j] + 8)
+ *                | (q_up[c][j] + 8) << 4, i.e. two offset-binary nibbles;
+ *                input-dim-major so that one kept input j is one contiguous
+ *                row; padding channels hold 0x88 (code 0).
+ *   proxy_scales fp16  [G][Fp][2]: (s_gate[c][g], s_up[c][g]); padding 0.
+ *   gateup       bf16  [F][2][d]: row c = (W_gate[c][:], W_up[c][:]).
+ *   down_t       bf16  [F][d]:    row c = W_down[:][c].
+ */
+
+/* Sizes of the buffers above for a layer shape.  Host only; queues nothing.
+ * Returns PROX_ERR_UNSUPPORTED_SHAPE for shapes outside the limits. */
+PROX_API prox_status prox_query_sizes(int d_model, int d_ff, prox_sizes* out);
+
+/*
+ * One-off per-layer preparation ("Prox", Abstract: quantized proxy weights
+ * for Stage 1; Stage-2 layouts for the selected rows and columns).
+ *   w_gate, w_up : bf16 [d_ff][d_model] (nn.Linear weight layout), device
+ *   w_down       : bf16 [d_model][d_ff], device
+ *   proxy_codes, proxy_scales, gateup, down_t, workspace : device buffers of
+ *                  at least the sizes prox_query_sizes reports; written here
+ *                  (workspace is zeroed) and referenced by the handle.
+ * On success *out receives a new handle.  The source weights may be freed
+ * once the stream has passed this call.  Not timed; not for graph capture
+ * (it sets kernel attributes).
+ */
+PROX_API prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, const void* w_up,
+                         const void* w_down, void* proxy_codes, void* proxy_scales,
+                         void* gateup, void* down_t, void* workspace, prox_stream_t stream,
+                         prox_layer** out);
+
+/*
+ * The Prox decode step ("Prox", Abstract; Eq. (1) of the PrunePath page for
+ * Stage 2), input keep fixed at 0.5:
+ *   x             bf16 [d_model], device
+ *   keep_fraction FFN keep fraction rho in (0, 1]; k = ceil(rho * d_ff)
+ *   y             fp32 [d_model], device, overwritten with
+ *                 y = sum_{c in mask} W_down[:, c] * silu(W_gate[c] . x) * (W_up[c] . x)
+ */
+PROX_API prox_status prox_ffn(const prox_layer* layer, const void* x, float keep_fraction, float* y,
+                     prox_stream_t stream);
+
+/* As prox_ffn with an explicit input keep fraction in (0, 1]:
+ * k_x = ceil(input_keep * d_model) inputs feed the proxy. */
+PROX_API prox_status prox_ffn_ex(const prox_layer* layer, const void* x, float keep_fraction,
+                        float input_keep, float* y, prox_stream_t stream);
+
+/* Dense SwiGLU FFN, Eq. (1) of the PrunePath page over all d_ff channels,
+ * streaming the same gateup / down_t buffers (the in-library dense
+ * baseline).  x bf16 [d_model], y fp32 [d_model], both device. */
+PROX_API prox_status prox_dense_ffn(const prox_layer* layer, const void* x, float* y,
+                           prox_stream_t stream);
+
+/*
+ * prox_ffn_ex plus the intermediate results, for parity checks (not timed).
+ * Each extra output may be NULL; all are device buffers:
+ *   kept_inputs int32 [k_x]  kept input indices, ascending
+ *   scores      fp32  [d_ff] proxy ranking signal |silu(g~) u~| per channel
+ *   idx         int32 [k]    selected channels, ascending
+ *   h           fp32  [k]    Stage-2 intermediate state h_c, in idx order
+ */
+PROX_API prox_status prox_ffn_debug(const prox_layer* layer, const void* x, float keep_fraction,
+                           float input_keep, float* y, int32_t* kept_inputs, float* scores,
+                           int32_t* idx, float* h, prox_stream_t stream);
+
+/*
+ * Glue between stacked layers (no page defines it; plain reading of a
+ * residual stream): z = x + y, x_next = bf16_rne(z / sqrt(mean(z^2) + eps)),
+ * no learned gain.  x, x_next bf16 [d_model]; y fp32 [d_model]; device.
+ * x_next may not alias y.
+ */
+PROX_API prox_status prox_residual_rmsnorm(int d_model, const void* x, const float* y, float eps,
+                                  void* x_next, prox_stream_t stream);
+
+/* Synchronises the stream, returns the status recorded on the device by
+ * earlier calls on this layer (PROX_OK if none) and clears it. */
+PROX_API prox_status prox_get_status(const prox_layer* layer, prox_stream_t stream);
+
+/* Shapes of a prepared layer.  Host only. */
+PROX_API prox_status prox_layer_info(const prox_layer* layer, int* d_model, int* d_ff);
+
+/* k = ceil(frac * n) in fp64, clamped to [1, n]; 0 for n < 1 or a fraction
+ * outside (0, 1].  Host only. */
+PROX_API int prox_keep_count(int n, float frac);
+
+/* Releases the host handle only; the device buffers stay the caller's. */
+PROX_API void prox_destroy(prox_layer* layer);
+
+/* Static description of a status code. */
+PROX_API const char* prox_status_string(prox_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PROX_H */

@@ -1,0 +1,202 @@
+"""GPU vs oracle parity through the C ABI (marked gpu).
+
+Bars: proxy codes/scales and the kept-input set bit-exact; the channel mask
+exact outside the tie band (channels whose oracle score lies within 1e-4
+relative of the oracle's k-th score may differ); y within max-abs 2e-2 and
+relative-L2 1e-2 of the oracle's sparse FFN evaluated on the GPU's mask.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from free_swiglu_ffn_prox_b300 import synth
+from parity_util import (ATOL_Y, RTOL_L2_Y, decode_proxy, host_bits, tie_band_mask_check,
+                         y_errors)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def prox():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from free_swiglu_ffn_prox_b300 import build, prox as p
+
+    build.build()
+    return p
+
+
+def _layer(prox, d, F, sigma=0.02, seed=0, device="cpu"):
+    wg, wu, wd = synth.make_weights(d, F, sigma, seed, device=device)
+    L = prox.prox_prepare(wg.cuda(), wu.cuda(), wd.cuda())
+    torch.cuda.synchronize()
+    return L, (host_bits(wg), host_bits(wu), host_bits(wd))
+
+
+def _x(d, n_out, seed):
+    return synth.make_x(d, n_out, 20.0, seed)
+
+
+def _check_step(prox, L, w, x, rho, kappa=0.5, px=None):
+    wg, wu, wd = w
+    xb = host_bits(x)
+    r = prox.prox_ffn_debug(L, x.cuda(), rho, kappa)
+    torch.cuda.synchronize()
+    assert prox.prox_get_status(L) == 0
+    kx, k = oracle.keep_count(L.d_model, kappa), oracle.keep_count(L.d_ff, rho)
+    assert (r["kx"], r["k"]) == (kx, k)
+    # input sparsity: bit-exact
+    kept_or = oracle.input_topk(xb, kx)
+    assert np.array_equal(r["kept"].cpu().numpy(), kept_or)
+    # proxy scores and the mask
+    if px is None:
+        px = oracle.Proxy(wg, wu)
+    g, u, sc = oracle.proxy_scores(px.q_gate, px.s_gate, px.q_up, px.s_up, xb, kept_or)
+    sc_gpu = r["scores"].cpu().numpy().astype(np.float64)
+    # fp32 proxy vs fp64 oracle, measured on the ranking scale: the k-th score
+    # (or the median score, when k is so large that the k-th is near zero)
+    kth = np.sort(sc)[::-1][k - 1]
+    scale = max(kth, float(np.median(sc)), 1e-30)
+    rel = np.abs(sc_gpu - sc) / np.maximum(np.abs(sc), scale)
+    assert rel.max() < 1e-5, rel.max()
+    idx = r["idx"].cpu().numpy()
+    bad, in_band = tie_band_mask_check(idx, sc, k)
+    assert bad == 0, f"{bad} channels outside the tie band disagree ({in_band} in band)"
+    # Stage 2 on the GPU's mask
+    h_or, y_or = oracle.sparse_ffn(wg, wu, wd, xb, idx)
+    mx, rl = y_errors(r["y"].cpu().numpy(), y_or)
+    assert mx <= ATOL_Y and rl <= RTOL_L2_Y, (mx, rl)
+    assert mx <= 1e-3 * max(1.0, np.abs(y_or).max())  # fp32 path: far inside the bar
+    hh = r["h"].cpu().numpy().astype(np.float64)
+    assert np.allclose(hh, h_or, rtol=1e-4, atol=1e-4 * np.abs(h_or).max())
+    return r
+
+
+@pytest.mark.parametrize("d,F", [(256, 688), (128, 64), (384, 1000), (1024, 77), (512, 3000)])
+def test_prepare_layouts_bit_exact(prox, d, F):
+    L, (wg, wu, wd) = _layer(prox, d, F, seed=d + F)
+    qg, qu, sg, su, pad_codes, pad_scales = decode_proxy(L)
+    og, osg = oracle.quantize(wg)
+    ou, osu = oracle.quantize(wu)
+    assert np.array_equal(qg, og) and np.array_equal(qu, ou)
+    assert np.array_equal(sg, osg) and np.array_equal(su, osu)
+    assert np.all(pad_codes == 0x88) and np.all(pad_scales == 0)
+    gu = L.bufs["gateup"].cpu().view(torch.int16).numpy().view(np.uint16).reshape(F, 2, d)
+    assert np.array_equal(gu[:, 0, :], wg) and np.array_equal(gu[:, 1, :], wu)
+    dt = L.bufs["down_t"].cpu().view(torch.int16).numpy().view(np.uint16).reshape(F, d)
+    assert np.array_equal(dt, wd.T)
+
+
+@pytest.mark.parametrize("d,F,rho", [(256, 688, 0.5), (256, 688, 0.1), (128, 64, 0.3),
+                                     (384, 1000, 0.3), (1024, 77, 0.5), (512, 3000, 0.05),
+                                     (2048, 5000, 0.3)])
+def test_prox_ffn_matches_oracle(prox, d, F, rho):
+    L, w = _layer(prox, d, F, seed=7 * d + F)
+    for s in range(3):
+        _check_step(prox, L, w, _x(d, max(1, d // 100), seed=100 + s), rho)
+
+
+def test_keep_fraction_extremes(prox):
+    d, F = 256, 688
+    L, w = _layer(prox, d, F, seed=3)
+    x = _x(d, 4, seed=9)
+    r1 = _check_step(prox, L, w, x, 1.0)
+    assert r1["k"] == F
+    y_dense = prox.prox_dense_ffn(L, x.cuda())
+    torch.cuda.synchronize()
+    assert torch.allclose(r1["y"], y_dense, rtol=1e-5, atol=1e-5)
+    _check_step(prox, L, w, x, 1e-6)  # k = 1
+    _check_step(prox, L, w, x, 0.5, kappa=1.0)   # every input kept
+    _check_step(prox, L, w, x, 0.5, kappa=1e-6)  # a single input kept
+
+
+def test_dense_matches_oracle(prox):
+    for d, F in ((256, 688), (1024, 2000)):
+        L, (wg, wu, wd) = _layer(prox, d, F, seed=11)
+        x = _x(d, 4, seed=12)
+        y = prox.prox_dense_ffn(L, x.cuda())
+        torch.cuda.synchronize()
+        _, y_or = oracle.dense_ffn(wg, wu, wd, host_bits(x))
+        mx, rl = y_errors(y.cpu().numpy(), y_or)
+        assert mx <= ATOL_Y and rl <= RTOL_L2_Y
+
+
+def test_degenerate_inputs(prox):
+    d, F = 256, 300
+    L, w = _layer(prox, d, F, seed=5)
+    # x = 0: every score is 0, ties -> the first k channels, y = 0
+    x0 = torch.zeros(d, dtype=torch.bfloat16)
+    r = prox.prox_ffn_debug(L, x0.cuda(), 0.3)
+    torch.cuda.synchronize()
+    k = oracle.keep_count(F, 0.3)
+    assert np.array_equal(r["idx"].cpu().numpy(), np.arange(k))
+    assert np.array_equal(r["kept"].cpu().numpy(), np.arange(d // 2))
+    assert torch.count_nonzero(r["y"]) == 0
+    # one-hot and heavily tied inputs
+    xo = torch.zeros(d, dtype=torch.bfloat16)
+    xo[77] = -3.5
+    _check_step(prox, L, w, xo, 0.3)
+    xt = torch.tensor(np.random.default_rng(1).choice([0.0, -1.0, 1.0, 2.0], size=d),
+                      dtype=torch.float32).to(torch.bfloat16)
+    _check_step(prox, L, w, xt, 0.3)
+
+
+def test_channel_permutation_identity_on_gpu(prox):
+    """Eq. (2) of the PrunePath page: permuting channels of all three weights
+    permutes the mask and leaves y unchanged (up to fp32 rounding)."""
+    d, F = 512, 1024
+    wg, wu, wd = synth.make_weights(d, F, 0.02, 21)
+    perm = torch.randperm(F, generator=torch.Generator().manual_seed(2))
+    L1 = prox.prox_prepare(wg.cuda(), wu.cuda(), wd.cuda())
+    L2 = prox.prox_prepare(wg[perm].contiguous().cuda(), wu[perm].contiguous().cuda(),
+                           wd[:, perm].contiguous().cuda())
+    x = _x(d, 5, 22).cuda()
+    r1 = prox.prox_ffn_debug(L1, x, 0.3)
+    r2 = prox.prox_ffn_debug(L2, x, 0.3)
+    torch.cuda.synchronize()
+    s1 = r1["scores"].cpu()
+    s2 = r2["scores"].cpu()
+    assert torch.allclose(s1[perm], s2, rtol=1e-5, atol=1e-6)
+    assert torch.allclose(r1["y"], r2["y"], rtol=1e-4, atol=1e-4)
+
+
+def test_errors_are_reported_not_raised_on_device(prox):
+    L, _ = _layer(prox, 256, 688, seed=1)
+    x = torch.zeros(256, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(prox.ProxError) as e:
+        prox.prox_ffn(L, x, 0.0)
+    assert e.value.code == prox.PROX_ERR_INVALID_ARG
+    with pytest.raises(prox.ProxError) as e:
+        prox.prox_ffn(L, x, 1.5)
+    assert e.value.code == prox.PROX_ERR_INVALID_ARG
+    buf = torch.zeros(300, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(prox.ProxError) as e:
+        prox.prox_ffn(L, buf[1:257], 0.3)
+    assert e.value.code == prox.PROX_ERR_MISALIGNED
+    assert prox.prox_get_status(L) == 0
+
+
+# ------------------------------------------------------------- full-size layers
+FULL = [synth.LLAMA2_7B, synth.LLAMA3_8B, synth.LLAMA3_70B]
+
+
+@pytest.mark.parametrize("shape", FULL, ids=lambda s: s.name)
+def test_full_size_layers(prox, shape):
+    """The Llama-shaped layers at every keep fraction: kept inputs exact,
+    mask exact outside the tie band against the oracle's full proxy, y within
+    the bar against the oracle's Stage 2 on the GPU's mask."""
+    wg, wu, wd = synth.layer(shape, seed=0, device="cuda")
+    L = prox.prox_prepare(wg, wu, wd)
+    torch.cuda.synchronize()
+    w = (host_bits(wg), host_bits(wu), host_bits(wd))
+    del wg, wu, wd
+    qg, qu, sg, su, _, _ = decode_proxy(L)
+    px = oracle.Proxy.__new__(oracle.Proxy)
+    px.q_gate, px.s_gate = oracle.quantize(w[0])
+    px.q_up, px.s_up = oracle.quantize(w[1])
+    assert np.array_equal(qg, px.q_gate) and np.array_equal(qu, px.q_up)
+    assert np.array_equal(sg, px.s_gate) and np.array_equal(su, px.s_up)
+    x = synth.hidden(shape, seed=1)
+    for rho in shape.keep_fractions:
+        _check_step(prox, L, w, x, rho, px=px)
