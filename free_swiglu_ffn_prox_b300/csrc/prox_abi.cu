@@ -29,7 +29,8 @@ static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 size_t workspace_bytes(int d, int F) {
     const int Fp = padded_ff(F);
     return align256(256) + align256((size_t)d * 4) + align256((size_t)Fp * 8) +
-           align256((size_t)Fp * 4) + align256((size_t)F * 4);
+           align256((size_t)Fp * 4) + align256((size_t)F * 4) + align256((size_t)d * 2) +
+           align256((size_t)d * 4);
 }
 
 Workspace carve_workspace(void* base, int d, int F) {
@@ -45,6 +46,10 @@ Workspace carve_workspace(void* base, int d, int F) {
     w.scores = reinterpret_cast<float*>(p);
     p += align256((size_t)Fp * 4);
     w.idx = reinterpret_cast<int32_t*>(p);
+    p += align256((size_t)F * 4);
+    w.x_stage = reinterpret_cast<uint16_t*>(p);
+    p += align256((size_t)d * 2);
+    w.y_stage = reinterpret_cast<float*>(p);
     return w;
 }
 
@@ -65,22 +70,44 @@ prox_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PROX_OK : PRO
 
 // The decode step on a checked layer.  kept_out/scores_out/idx_out/h_out
 // are the debug outputs (NULL on the hot path).
+// Records `ev` on the stream; inside a stream capture it becomes an event
+// node of the graph, so traced calls can be captured too.
+cudaError_t record(cudaEvent_t ev, cudaStream_t stream) {
+    if (!ev) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return e;
+    return cs == cudaStreamCaptureStatusActive
+               ? cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal)
+               : cudaEventRecord(ev, stream);
+}
+
+// The decode step on a checked layer.  kept_out/scores_out/idx_out/h_out
+// are the debug outputs (NULL on the hot path); ev (NULL or
+// PROX_TRACE_EVENTS events) brackets each kernel.
 prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, float input_keep,
                      float* y, int32_t* kept_out, float* scores_out, int32_t* idx_out,
-                     float* h_out, cudaStream_t stream, long long limit_ns, int inject) {
+                     float* h_out, cudaStream_t stream, long long limit_ns, int inject,
+                     cudaEvent_t const* ev = nullptr) {
     const int d = L->d_model, F = L->d_ff;
     const int kx = prox_keep_count(d, input_keep);
     const int k = prox_keep_count(F, keep_fraction);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    cudaError_t e = prox::launch_input_select(xb, d, kx, L->ws, kept_out, y, stream);
+    auto mark = [&](int i) { return ev ? record(ev[i], stream) : cudaSuccess; };
+    cudaError_t e = mark(0);
+    if (e == cudaSuccess) e = prox::launch_input_select(xb, d, kx, L->ws, kept_out, y, stream);
+    if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess)
         e = prox::launch_proxy_gemv(L->codes, L->scales, L->ws, d, F, kx, L->num_sms, limit_ns,
                                     inject == 1, stream);
+    if (e == cudaSuccess) e = mark(2);
     if (e == cudaSuccess) e = prox::launch_channel_select(L->ws, F, k, scores_out, stream);
+    if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess)
         e = prox::launch_gather_ffn(L->gateup, L->down_t, xb, L->ws.idx, k, d, y, h_out,
                                     L->ws.acc, L->Fp, L->ws.status, L->num_sms, limit_ns,
                                     inject == 2, stream);
+    if (e == cudaSuccess) e = mark(4);
     if (e == cudaSuccess && idx_out)
         e = cudaMemcpyAsync(idx_out, L->ws.idx, (size_t)k * sizeof(int32_t),
                             cudaMemcpyDeviceToDevice, stream);
@@ -187,6 +214,36 @@ prox_status prox_ffn_ex(const prox_layer* layer, const void* x, float keep_fract
 prox_status prox_ffn(const prox_layer* layer, const void* x, float keep_fraction, float* y,
                      prox_stream_t stream) {
     return prox_ffn_ex(layer, x, keep_fraction, 0.5f, y, stream);
+}
+
+prox_status prox_ffn_host(const prox_layer* layer, const void* x_host, float keep_fraction,
+                          float* y_host, prox_stream_t stream) {
+    if (!layer || !x_host || !y_host) return PROX_ERR_INVALID_ARG;
+    if (!frac_ok(keep_fraction)) return PROX_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int d = layer->d_model;
+    cudaError_t e = cudaMemcpyAsync(layer->ws.x_stage, x_host, (size_t)d * 2,
+                                    cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return PROX_ERR_CUDA;
+    prox_status st = run_prox(layer, layer->ws.x_stage, keep_fraction, 0.5f, layer->ws.y_stage,
+                              nullptr, nullptr, nullptr, nullptr, s, prox::kWaitLimitNs, 0);
+    if (st != PROX_OK) return st;
+    e = cudaMemcpyAsync(y_host, layer->ws.y_stage, (size_t)d * 4, cudaMemcpyDeviceToHost, s);
+    return cuda_status(e);
+}
+
+prox_status prox_ffn_traced(const prox_layer* layer, const void* x, float keep_fraction,
+                            float input_keep, float* y, void* const* events, int n_events,
+                            prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    if (!frac_ok(keep_fraction) || !frac_ok(input_keep)) return PROX_ERR_INVALID_ARG;
+    if (!events || n_events != PROX_TRACE_EVENTS) return PROX_ERR_INVALID_ARG;
+    for (int i = 0; i < n_events; ++i)
+        if (!events[i]) return PROX_ERR_INVALID_ARG;
+    return run_prox(layer, x, keep_fraction, input_keep, y, nullptr, nullptr, nullptr, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0,
+                    reinterpret_cast<cudaEvent_t const*>(events));
 }
 
 prox_status prox_dense_ffn(const prox_layer* layer, const void* x, float* y,

@@ -27,6 +27,8 @@ struct Workspace {
     float2* acc;      // [Fp] proxy (g~, u~) accumulators, zero between calls
     float* scores;    // [Fp]
     int32_t* idx;     // [d_ff] selected channels
+    uint16_t* x_stage;  // [d] bf16 input staged from host memory (prox_ffn_host)
+    float* y_stage;     // [d] fp32 output staged for host memory (prox_ffn_host)
 };
 
 size_t workspace_bytes(int d_model, int d_ff);

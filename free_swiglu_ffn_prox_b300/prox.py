@@ -23,6 +23,7 @@ PROX_ERR_MISALIGNED = 3
 PROX_ERR_CUDA = 4
 PROX_ERR_TIMEOUT = 5
 PROX_ERR_DEVICE_CHECK = 6
+PROX_TRACE_EVENTS = 5
 
 _lock = threading.Lock()
 _lib = None
@@ -56,6 +57,8 @@ def _load():
                                    ctypes.POINTER(vp)]),
             "prox_ffn": (i32, [vp, vp, f32, vp, vp]),
             "prox_ffn_ex": (i32, [vp, vp, f32, f32, vp, vp]),
+            "prox_ffn_host": (i32, [vp, vp, f32, vp, vp]),
+            "prox_ffn_traced": (i32, [vp, vp, f32, f32, vp, ctypes.POINTER(vp), i32, vp]),
             "prox_dense_ffn": (i32, [vp, vp, vp, vp]),
             "prox_ffn_debug": (i32, [vp, vp, f32, f32, vp, vp, vp, vp, vp, vp]),
             "prox_residual_rmsnorm": (i32, [i32, vp, vp, f32, vp, vp]),
@@ -186,6 +189,42 @@ def prox_ffn_ex(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, input_k
     y = _x_y(layer, x, y)
     _check(_load().prox_ffn_ex(layer.handle, _ptr(x), float(keep_fraction), float(input_keep),
                                _ptr(y), _stream(stream)), "prox_ffn_ex")
+    return y
+
+
+def prox_ffn_host(layer: ProxLayer, x_host: torch.Tensor, keep_fraction: float, y_host=None,
+                  stream=None):
+    """prox_ffn on host tensors: the library copies x in and y out on the
+    stream.  Pinned tensors give asynchronous copies; y_host is valid once
+    the stream has passed the call."""
+    if not isinstance(x_host, torch.Tensor) or x_host.is_cuda:
+        raise ValueError("x_host must be a host tensor")
+    if x_host.dtype != torch.bfloat16 or tuple(x_host.shape) != (layer.d_model,) \
+            or not x_host.is_contiguous():
+        raise ValueError(f"x_host must be a contiguous bf16 tensor of shape ({layer.d_model},)")
+    if y_host is None:
+        y_host = torch.empty(layer.d_model, dtype=torch.float32, pin_memory=x_host.is_pinned())
+    if y_host.is_cuda or y_host.dtype != torch.float32 or tuple(y_host.shape) != (layer.d_model,) \
+            or not y_host.is_contiguous():
+        raise ValueError(f"y_host must be a contiguous fp32 host tensor of shape ({layer.d_model},)")
+    with torch.cuda.device(layer.device):
+        _check(_load().prox_ffn_host(layer.handle, _ptr(x_host), float(keep_fraction),
+                                     _ptr(y_host), _stream(stream)), "prox_ffn_host")
+    return y_host
+
+
+def prox_ffn_traced(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, events,
+                    input_keep: float = 0.5, y=None, stream=None):
+    """prox_ffn_ex recording ``events`` (PROX_TRACE_EVENTS timing-enabled
+    torch.cuda.Event objects, each already recorded once so that it exists)
+    around its kernels; events[i].elapsed_time(events[i + 1]) is kernel i+1."""
+    y = _x_y(layer, x, y)
+    if len(events) != PROX_TRACE_EVENTS:
+        raise ValueError(f"need {PROX_TRACE_EVENTS} events")
+    handles = (ctypes.c_void_p * PROX_TRACE_EVENTS)(*[int(e.cuda_event) for e in events])
+    _check(_load().prox_ffn_traced(layer.handle, _ptr(x), float(keep_fraction), float(input_keep),
+                                   _ptr(y), handles, PROX_TRACE_EVENTS, _stream(stream)),
+           "prox_ffn_traced")
     return y
 
 

@@ -135,6 +135,36 @@ PROX_API prox_status prox_ffn(const prox_layer* layer, const void* x, float keep
 PROX_API prox_status prox_ffn_ex(const prox_layer* layer, const void* x, float keep_fraction,
                         float input_keep, float* y, prox_stream_t stream);
 
+/*
+ * prox_ffn with host buffers, for callers whose token lives in host memory:
+ * copies x_host (bf16 [d_model]) to a staging slot of the layer's
+ * workspace, runs the decode step there (input keep 0.5) and copies y (fp32
+ * [d_model]) back to y_host.  All three steps are queued on the stream; the
+ * call does not synchronise, so y_host is valid once the stream has passed
+ * the call.  Pass page-locked host memory (cudaHostAlloc / pinned tensors)
+ * for asynchronous copies; pageable memory still works but the runtime then
+ * copies synchronously.  No alignment rule applies to the host pointers.
+ */
+PROX_API prox_status prox_ffn_host(const prox_layer* layer, const void* x_host, float keep_fraction,
+                          float* y_host, prox_stream_t stream);
+
+/* Number of CUDA events prox_ffn_traced records. */
+#define PROX_TRACE_EVENTS 5
+
+/*
+ * prox_ffn_ex that also records `events` (n_events == PROX_TRACE_EVENTS
+ * cudaEvent_t handles, created by the caller with timing enabled) around its
+ * kernels: events[0] before the input selection, events[1] after it,
+ * events[2] after the proxy GEMV, events[3] after the channel select and
+ * events[4] after Stage 2, so cudaEventElapsedTime(events[i], events[i+1])
+ * is the duration of kernel i+1 on the stream.  Inside a stream capture the
+ * records become event nodes of the graph (cudaEventRecordExternal).  For
+ * per-kernel timing only; it launches the same kernels as prox_ffn_ex.
+ */
+PROX_API prox_status prox_ffn_traced(const prox_layer* layer, const void* x, float keep_fraction,
+                            float input_keep, float* y, void* const* events, int n_events,
+                            prox_stream_t stream);
+
 /* Dense SwiGLU FFN, Eq. (1) of the PrunePath page over all d_ff channels,
  * streaming the same gateup / down_t buffers (the in-library dense
  * baseline).  x bf16 [d_model], y fp32 [d_model], both device. */

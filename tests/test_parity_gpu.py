@@ -177,6 +177,47 @@ def test_errors_are_reported_not_raised_on_device(prox):
     assert prox.prox_get_status(L) == 0
 
 
+def test_host_buffer_and_traced_entry_points(prox):
+    """prox_ffn_host (host x/y, copies queued by the library) and
+    prox_ffn_traced (events between the kernels) compute what prox_ffn does."""
+    d, F = 1024, 3000
+    L, (wg, wu, wd) = _layer(prox, d, F, seed=31)
+    x = _x(d, 10, 32)
+    y_dev = prox.prox_ffn(L, x.cuda(), 0.3)
+    xh = x.clone().pin_memory()
+    yh = torch.full((d,), float("nan")).pin_memory()
+    prox.prox_ffn_host(L, xh, 0.3, y_host=yh)
+    torch.cuda.synchronize()
+    assert torch.allclose(yh, y_dev.cpu(), rtol=1e-5, atol=1e-5)
+    y_pageable = prox.prox_ffn_host(L, x.clone(), 0.3)  # pageable memory works too
+    torch.cuda.synchronize()
+    assert torch.allclose(y_pageable, y_dev.cpu(), rtol=1e-5, atol=1e-5)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(prox.PROX_TRACE_EVENTS)]
+    for e in evs:
+        e.record()
+    y_tr = prox.prox_ffn_traced(L, x.cuda(), 0.3, evs)
+    torch.cuda.synchronize()
+    assert torch.allclose(y_tr, y_dev, rtol=1e-5, atol=1e-5)
+    dt = [evs[i].elapsed_time(evs[i + 1]) for i in range(prox.PROX_TRACE_EVENTS - 1)]
+    assert all(t >= 0.0 for t in dt) and sum(dt) > 0.0
+    with pytest.raises(prox.ProxError):
+        prox.prox_ffn_host(L, xh, 1.5, y_host=yh)
+    # the same traced step captured in a CUDA graph (event nodes)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    y_g = torch.empty(d, device="cuda")
+    xg = x.cuda()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            prox.prox_ffn_traced(L, xg, 0.3, evs, y=y_g)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.allclose(y_g, y_dev, rtol=1e-5, atol=1e-5)
+    dt = [evs[i].elapsed_time(evs[i + 1]) for i in range(prox.PROX_TRACE_EVENTS - 1)]
+    assert all(t >= 0.0 for t in dt)
+    assert prox.prox_get_status(L) == 0
+
+
 # ------------------------------------------------------------- full-size layers
 FULL = [synth.LLAMA2_7B, synth.LLAMA3_8B, synth.LLAMA3_70B]
 
