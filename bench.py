@@ -51,13 +51,10 @@ if ROOT not in sys.path:
 METRIC = "sparse SwiGLU FFN decode tokens/s/layer & HBM GB/s (% roofline) at 70% sparsity"
 UNIT = "tokens/s/layer"
 SPEC_HBM_GBS = 8000.0      # B300 HBM3e nominal, for the "% of spec" figure
-KERNELS_PER_STEP = 4       # input select, proxy GEMV, channel select, Stage 2
-KERNEL_NAMES = ("k_input_select", "k_proxy_gemv", "k_channel_select", "k_gather_ffn")
+KERNELS_PER_STEP = 1       # the decode step is one persistent kernel
+KERNEL_NAMES = ("k_prox_fused",)
 SOURCE_OF = {              # kernel -> source file whose hash guards ncu traffic numbers
-    "k_input_select": "prox_select.cu",
-    "k_proxy_gemv": "prox_proxy.cu",
-    "k_channel_select": "prox_select.cu",
-    "k_gather_ffn": "prox_gather.cu",
+    "k_prox_fused": "prox_fused.cu",
 }
 N_X = 16                   # distinct hidden states cycled through
 CHUNK = 64                 # steps per captured graph
@@ -72,13 +69,10 @@ def algorithmic_bytes(d: int, F: int, k: int, kx: int) -> dict:
     2*k*d bf16, selected W_down^T rows k*d bf16, x bf16, y fp32, the kept list
     and the channel list int32, the proxy accumulators fp32 (g~, u~)."""
     G = d // 128
+    step = F * kx + 4 * F * G + 6 * k * d + 2 * d + 4 * d + 4 * k
     return {
-        "k_input_select": 2 * d + 4 * kx + 4 * d,
-        "k_proxy_gemv": F * kx + 4 * F * G + 4 * kx + 8 * F,
-        "k_channel_select": 8 * F + 4 * k,
-        "k_gather_ffn": 6 * k * d + 2 * d + 4 * k + 4 * d,
-        # whole step, the per-token total of the method (no housekeeping)
-        "step": F * kx + 4 * F * G + 6 * k * d + 2 * d + 4 * d + 4 * k,
+        "k_prox_fused": step,  # the whole step runs in one kernel
+        "step": step,
         "dense": 6 * F * d + 2 * d + 4 * d,
     }
 
@@ -520,8 +514,9 @@ def run_gpu(args):
     y_dev = prox.prox_ffn(L, x, rho).cpu()
     y_dev2 = prox.prox_ffn(L, x, rho).cpu()
     torch.cuda.synchronize()
-    ok = torch.allclose(yh[(K - 1) % N_X], y_dev, rtol=1e-5, atol=1e-5)
     e2e_diff = float((yh[(K - 1) % N_X] - y_dev).abs().max())
+    # fp32 atomics in the output reduction: agreement to a few ulps of max|y|
+    ok = e2e_diff <= 1e-5 * float(y_dev.abs().max())
     rep_diff = float((y_dev2 - y_dev).abs().max())
     e2e = {"value": round(ws * K / e2e_s, 1), "unit": UNIT,
            "h2d_bytes_per_step": 2 * d, "d2h_bytes_per_step": 4 * d,

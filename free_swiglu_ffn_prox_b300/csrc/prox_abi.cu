@@ -1,10 +1,7 @@
 // prox_abi.cu -- the extern "C" entry points declared in include/prox.h:
-// argument checks, workspace carving, and the launch sequence of the Prox
-// decode step ("Prox", Abstract):
-//   1. input sparsity           (top-|x|, prox_select.cu)
-//   2. proxy GEMV                (int4 proxy x kept inputs, prox_proxy.cu)
-//   3. channel mask              (top-k of |silu(g~) u~|, prox_select.cu)
-//   4. exact Stage 2             (gate|up gather + silu*mul + down, prox_gather.cu)
+// argument checks, workspace carving, and the launch of the Prox decode step
+// ("Prox", Abstract), which runs as one persistent kernel (prox_fused.cu):
+// input sparsity, proxy GEMV, channel mask and exact Stage 2.
 #include <math.h>
 #include <stdlib.h>
 
@@ -14,7 +11,7 @@
 
 struct prox_layer {
     int d_model, d_ff, Fp;
-    int device, num_sms;
+    int device, num_sms, num_blocks;
     const uint8_t* codes;
     const __half2* scales;
     const __nv_bfloat16* gateup;
@@ -28,9 +25,9 @@ static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t workspace_bytes(int d, int F) {
     const int Fp = padded_ff(F);
-    return align256(256) + align256((size_t)d * 4) + align256((size_t)Fp * 8) +
-           align256((size_t)Fp * 4) + align256((size_t)F * 4) + align256((size_t)d * 2) +
-           align256((size_t)d * 4);
+    return align256(256) + align256((size_t)kHistWords * 4) +
+           align256((size_t)kMaxSlices * Fp * 8) + align256((size_t)Fp * 4) +
+           align256((size_t)d * 2) + align256((size_t)d * 4);
 }
 
 Workspace carve_workspace(void* base, int d, int F) {
@@ -38,15 +35,14 @@ Workspace carve_workspace(void* base, int d, int F) {
     uint8_t* p = static_cast<uint8_t*>(base);
     Workspace w;
     w.status = reinterpret_cast<int*>(p);
+    w.bar = reinterpret_cast<unsigned*>(p + 128);
     p += align256(256);
-    w.kept = reinterpret_cast<uint32_t*>(p);
-    p += align256((size_t)d * 4);
-    w.acc = reinterpret_cast<float2*>(p);
-    p += align256((size_t)Fp * 8);
+    w.hist = reinterpret_cast<uint32_t*>(p);
+    p += align256((size_t)kHistWords * 4);
+    w.part = reinterpret_cast<float2*>(p);
+    p += align256((size_t)kMaxSlices * Fp * 8);
     w.scores = reinterpret_cast<float*>(p);
     p += align256((size_t)Fp * 4);
-    w.idx = reinterpret_cast<int32_t*>(p);
-    p += align256((size_t)F * 4);
     w.x_stage = reinterpret_cast<uint16_t*>(p);
     p += align256((size_t)d * 2);
     w.y_stage = reinterpret_cast<float*>(p);
@@ -59,7 +55,7 @@ namespace {
 
 bool shape_ok(int d, int F) {
     return d >= prox::kGroup && d <= prox::kMaxDModel && d % prox::kGroup == 0 && F >= 1 &&
-           F <= prox::kMaxDff;
+           F <= prox::kMaxDff && prox::fused_fits(d, F);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -68,8 +64,6 @@ bool frac_ok(float f) { return isfinite(f) && f > 0.0f && f <= 1.0f; }
 
 prox_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PROX_OK : PROX_ERR_CUDA; }
 
-// The decode step on a checked layer.  kept_out/scores_out/idx_out/h_out
-// are the debug outputs (NULL on the hot path).
 // Records `ev` on the stream; inside a stream capture it becomes an event
 // node of the graph, so traced calls can be captured too.
 cudaError_t record(cudaEvent_t ev, cudaStream_t stream) {
@@ -84,33 +78,34 @@ cudaError_t record(cudaEvent_t ev, cudaStream_t stream) {
 
 // The decode step on a checked layer.  kept_out/scores_out/idx_out/h_out
 // are the debug outputs (NULL on the hot path); ev (NULL or
-// PROX_TRACE_EVENTS events) brackets each kernel.
+// PROX_TRACE_EVENTS events) brackets the kernel.
 prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, float input_keep,
                      float* y, int32_t* kept_out, float* scores_out, int32_t* idx_out,
                      float* h_out, cudaStream_t stream, long long limit_ns, int inject,
-                     cudaEvent_t const* ev = nullptr) {
-    const int d = L->d_model, F = L->d_ff;
-    const int kx = prox_keep_count(d, input_keep);
-    const int k = prox_keep_count(F, keep_fraction);
-    const uint16_t* xb = static_cast<const uint16_t*>(x);
-    auto mark = [&](int i) { return ev ? record(ev[i], stream) : cudaSuccess; };
-    cudaError_t e = mark(0);
-    if (e == cudaSuccess) e = prox::launch_input_select(xb, d, kx, L->ws, kept_out, y, stream);
-    if (e == cudaSuccess) e = mark(1);
-    if (e == cudaSuccess)
-        e = prox::launch_proxy_gemv(L->codes, L->scales, L->ws, d, F, kx, L->num_sms, limit_ns,
-                                    inject == 1, stream);
-    if (e == cudaSuccess) e = mark(2);
-    if (e == cudaSuccess) e = prox::launch_channel_select(L->ws, F, k, scores_out, stream);
-    if (e == cudaSuccess) e = mark(3);
-    if (e == cudaSuccess)
-        e = prox::launch_gather_ffn(L->gateup, L->down_t, xb, L->ws.idx, k, d, y, h_out,
-                                    L->ws.acc, L->Fp, L->ws.status, L->num_sms, limit_ns,
-                                    inject == 2, stream);
-    if (e == cudaSuccess) e = mark(4);
-    if (e == cudaSuccess && idx_out)
-        e = cudaMemcpyAsync(idx_out, L->ws.idx, (size_t)k * sizeof(int32_t),
-                            cudaMemcpyDeviceToDevice, stream);
+                     cudaEvent_t const* ev = nullptr, uint64_t* ts = nullptr) {
+    prox::FusedLaunch f;
+    f.codes = L->codes;
+    f.scales = L->scales;
+    f.gateup = L->gateup;
+    f.down_t = L->down_t;
+    f.d = L->d_model;
+    f.F = L->d_ff;
+    f.x = static_cast<const uint16_t*>(x);
+    f.y = y;
+    f.kx = prox_keep_count(L->d_model, input_keep);
+    f.k = prox_keep_count(L->d_ff, keep_fraction);
+    f.ws = &L->ws;
+    f.kept_out = kept_out;
+    f.scores_out = scores_out;
+    f.idx_out = idx_out;
+    f.h_out = h_out;
+    f.num_blocks = L->num_blocks;
+    f.limit_ns = limit_ns;
+    f.inject = inject;
+    f.ts = ts;
+    cudaError_t e = ev ? record(ev[0], stream) : cudaSuccess;
+    if (e == cudaSuccess) e = prox::launch_fused(f, stream);
+    if (e == cudaSuccess && ev) e = record(ev[1], stream);
     return cuda_status(e);
 }
 
@@ -173,8 +168,7 @@ prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, const void* 
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = prox::proxy_configure();
-    if (e == cudaSuccess) e = prox::gather_configure(d_model);
+    if (e == cudaSuccess) e = prox::fused_configure();
     if (e == cudaSuccess)
         e = cudaMemsetAsync(workspace, 0, prox::workspace_bytes(d_model, d_ff), s);
     if (e == cudaSuccess)
@@ -186,6 +180,9 @@ prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, const void* 
                                  static_cast<__nv_bfloat16*>(gateup),
                                  static_cast<__nv_bfloat16*>(down_t), s);
     if (e != cudaSuccess) return PROX_ERR_CUDA;
+    // one persistent CTA per SM; every CTA must hold its share of the
+    // channel list in shared memory
+    if ((d_ff + sms - 1) / sms > prox::fused_max_chan()) return PROX_ERR_UNSUPPORTED_SHAPE;
     prox_layer* L = new (std::nothrow) prox_layer;
     if (!L) return PROX_ERR_INVALID_ARG;
     L->d_model = d_model;
@@ -193,6 +190,7 @@ prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, const void* 
     L->Fp = prox::padded_ff(d_ff);
     L->device = dev;
     L->num_sms = sms;
+    L->num_blocks = sms;
     L->codes = static_cast<const uint8_t*>(proxy_codes);
     L->scales = static_cast<const __half2*>(proxy_scales);
     L->gateup = static_cast<const __nv_bfloat16*>(gateup);
@@ -253,9 +251,9 @@ prox_status prox_dense_ffn(const prox_layer* layer, const void* x, float* y,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(y, 0, (size_t)layer->d_model * sizeof(float), s);
     if (e == cudaSuccess)
-        e = prox::launch_gather_ffn(layer->gateup, layer->down_t, static_cast<const uint16_t*>(x),
-                                    nullptr, layer->d_ff, layer->d_model, y, nullptr, nullptr, 0,
-                                    layer->ws.status, layer->num_sms, prox::kWaitLimitNs, 0, s);
+        e = prox::launch_dense(layer->gateup, layer->down_t, static_cast<const uint16_t*>(x),
+                               layer->d_model, layer->d_ff, y, layer->ws.status,
+                               layer->num_blocks, prox::kWaitLimitNs, nullptr, s);
     return cuda_status(e);
 }
 
@@ -289,10 +287,47 @@ prox_status prox_get_status(const prox_layer* layer, prox_stream_t stream) {
     int v = 0;
     cudaError_t e = cudaMemcpyAsync(&v, layer->ws.status, sizeof(int), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(layer->ws.status, 0, sizeof(int), s);
+    // clear the status word and, after a fault, the grid barrier word (a
+    // barrier that ran out leaves it part-way)
+    if (e == cudaSuccess) e = cudaMemsetAsync(layer->ws.status, 0, v != 0 ? 256 : sizeof(int), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return PROX_ERR_CUDA;
     return (prox_status)v;
+}
+
+int prox_layer_blocks(const prox_layer* layer) { return layer ? layer->num_blocks : 0; }
+
+prox_status prox_ffn_phase_times(const prox_layer* layer, const void* x, float keep_fraction,
+                                 float* y, uint64_t* stamps, int dense, prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    if (!stamps || (!dense && !frac_ok(keep_fraction))) return PROX_ERR_INVALID_ARG;
+    if (!aligned16(stamps)) return PROX_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(stamps, 0,
+                                    (size_t)layer->num_blocks * PROX_PHASE_STAMPS * sizeof(uint64_t), s);
+    if (e != cudaSuccess) return PROX_ERR_CUDA;
+    if (dense) {
+        e = cudaMemsetAsync(y, 0, (size_t)layer->d_model * sizeof(float), s);
+        if (e == cudaSuccess)
+            e = prox::launch_dense(layer->gateup, layer->down_t, static_cast<const uint16_t*>(x),
+                                   layer->d_model, layer->d_ff, y, layer->ws.status,
+                                   layer->num_blocks, prox::kWaitLimitNs, stamps, s);
+        return cuda_status(e);
+    }
+    return run_prox(layer, x, keep_fraction, 0.5f, y, nullptr, nullptr, nullptr, nullptr, s,
+                    prox::kWaitLimitNs, 0, nullptr, stamps);
+}
+
+prox_status prox_test_barrier_timeout(const prox_layer* layer, const void* x, float* y,
+                                      prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = run_prox(layer, x, 0.5f, 0.5f, y, nullptr, nullptr, nullptr, nullptr, s,
+                  20 * 1000 * 1000LL /* 20 ms */, 1);
+    if (st != PROX_OK) return st;
+    return prox_get_status(layer, stream);
 }
 
 prox_status prox_layer_info(const prox_layer* layer, int* d_model, int* d_ff) {

@@ -20,13 +20,16 @@ constexpr long long kWaitLimitNs = 2000000000LL;  // 2 s per bounded wait
 
 inline int padded_ff(int d_ff) { return (d_ff + kChanAlign - 1) / kChanAlign * kChanAlign; }
 
+constexpr int kMaxSlices = 16;   // proxy row slices (partial sums per channel)
+constexpr int kHistWords = 2048; // global score histogram (11-bit digit)
+
 // Workspace carve-out (offsets in bytes, each 256-aligned).
 struct Workspace {
-    int* status;      // [0] device status word, [1] input prescale exponent
-    uint32_t* kept;   // [d] packed (j << 16 | fp16 bits of x_j * 2^shift)
-    float2* acc;      // [Fp] proxy (g~, u~) accumulators, zero between calls
-    float* scores;    // [Fp]
-    int32_t* idx;     // [d_ff] selected channels
+    int* status;        // [0] device status word (0 = ok)
+    unsigned* bar;      // grid barrier word of the fused kernel
+    uint32_t* hist;     // [kHistWords] score histogram, zeroed by each call
+    float2* part;       // [kMaxSlices][Fp] per-slice proxy partials (g~, u~)
+    float* scores;      // [Fp] proxy ranking signal |silu(g~) u~|
     uint16_t* x_stage;  // [d] bf16 input staged from host memory (prox_ffn_host)
     float* y_stage;     // [d] fp32 output staged for host memory (prox_ffn_host)
 };
@@ -82,13 +85,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // true when the phase completed.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   long long limit_ns, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
+    // the clock is read only once the phase is clearly late (every 64 polls)
+    uint64_t t0 = 0;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (abort && *abort) return false;
-            if ((long long)(global_timer_ns() - t0) > limit_ns) return false;
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) t0 = now;
+            else if ((long long)(now - t0) > limit_ns) return false;
         }
     }
 }
@@ -136,27 +141,42 @@ cudaError_t launch_prepare(int d, int F, const __nv_bfloat16* w_gate, const __nv
                            const __nv_bfloat16* w_down, uint8_t* codes, __half2* scales,
                            __nv_bfloat16* gateup, __nv_bfloat16* down_t, cudaStream_t stream);
 
-cudaError_t launch_input_select(const uint16_t* x, int d, int kx, const Workspace& ws,
-                                int32_t* kept_out, float* y_zero, cudaStream_t stream);
-
+// Proxy work split: `tiles` channel tiles of `tile_w` channels (a multiple
+// of 16) times `slices` slices of the kept inputs, tiles * slices <= blocks.
 struct ProxyGeom {
-    int tiles, slices;
+    int tiles, slices, tile_w;
 };
-ProxyGeom proxy_geometry(int F, int kx, int num_sms);
-cudaError_t proxy_configure();
-cudaError_t launch_proxy_gemv(const uint8_t* codes, const __half2* scales, const Workspace& ws,
-                              int d, int F, int kx, int num_sms, long long wait_limit_ns,
-                              int inject_stall, cudaStream_t stream);
+ProxyGeom proxy_geometry(int F, int kx, int num_blocks);
 
-cudaError_t launch_channel_select(const Workspace& ws, int F, int k, float* scores_out,
-                                  cudaStream_t stream);
+struct FusedLaunch {
+    const uint8_t* codes;
+    const __half2* scales;
+    const __nv_bfloat16* gateup;
+    const __nv_bfloat16* down_t;
+    int d, F;
+    const uint16_t* x;
+    float* y;
+    int kx, k;
+    const Workspace* ws;
+    int32_t* kept_out;   // debug outputs, may be null
+    float* scores_out;
+    int32_t* idx_out;
+    float* h_out;
+    int num_blocks;
+    long long limit_ns;
+    int inject;          // test hook: 1 = one CTA withholds the first grid barrier
+    uint64_t* ts;        // phase stamps [num_blocks][PROX_PHASE_STAMPS] or null
+};
 
-cudaError_t gather_configure(int d);
-cudaError_t launch_gather_ffn(const __nv_bfloat16* gateup, const __nv_bfloat16* down_t,
-                              const uint16_t* x, const int32_t* idx, int k, int d, float* y,
-                              float* h_out, float2* acc_zero, int acc_n, int* status,
-                              int num_sms, long long wait_limit_ns, int inject_stall,
-                              cudaStream_t stream);
+cudaError_t fused_configure();
+bool fused_fits(int d, int F);
+int fused_threads();
+int fused_max_chan();
+size_t fused_smem_bytes();
+cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream);
+cudaError_t launch_dense(const __nv_bfloat16* gateup, const __nv_bfloat16* down_t,
+                         const uint16_t* x, int d, int F, float* y, int* status, int num_blocks,
+                         long long limit_ns, uint64_t* ts, cudaStream_t stream);
 
 cudaError_t launch_residual_rmsnorm(int d, const uint16_t* x, const float* y, float eps,
                                     uint16_t* x_next, cudaStream_t stream);

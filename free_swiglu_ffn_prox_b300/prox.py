@@ -23,7 +23,10 @@ PROX_ERR_MISALIGNED = 3
 PROX_ERR_CUDA = 4
 PROX_ERR_TIMEOUT = 5
 PROX_ERR_DEVICE_CHECK = 6
-PROX_TRACE_EVENTS = 5
+PROX_TRACE_EVENTS = 2
+PROX_PHASE_STAMPS = 10
+PHASES = ("start", "input_select", "proxy", "barrier1", "scores", "barrier2", "stage2_begin",
+          "first_row", "stage2_dots", "end")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +66,9 @@ def _load():
             "prox_ffn_debug": (i32, [vp, vp, f32, f32, vp, vp, vp, vp, vp, vp]),
             "prox_residual_rmsnorm": (i32, [i32, vp, vp, f32, vp, vp]),
             "prox_get_status": (i32, [vp, vp]),
+            "prox_test_barrier_timeout": (i32, [vp, vp, vp, vp]),
+            "prox_layer_blocks": (i32, [vp]),
+            "prox_ffn_phase_times": (i32, [vp, vp, f32, vp, vp, i32, vp]),
             "prox_layer_info": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "prox_keep_count": (i32, [i32, f32]),
             "prox_destroy": (None, [vp]),
@@ -217,7 +223,7 @@ def prox_ffn_traced(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, eve
                     input_keep: float = 0.5, y=None, stream=None):
     """prox_ffn_ex recording ``events`` (PROX_TRACE_EVENTS timing-enabled
     torch.cuda.Event objects, each already recorded once so that it exists)
-    around its kernels; events[i].elapsed_time(events[i + 1]) is kernel i+1."""
+    around its kernel; events[0].elapsed_time(events[1]) is the step."""
     y = _x_y(layer, x, y)
     if len(events) != PROX_TRACE_EVENTS:
         raise ValueError(f"need {PROX_TRACE_EVENTS} events")
@@ -268,6 +274,30 @@ def prox_residual_rmsnorm(x: torch.Tensor, y: torch.Tensor, eps: float = 1e-6, o
 
 def prox_get_status(layer: ProxLayer, stream=None) -> int:
     return int(_load().prox_get_status(layer.handle, _stream(stream)))
+
+
+def prox_layer_blocks(layer: ProxLayer) -> int:
+    return int(_load().prox_layer_blocks(layer.handle))
+
+
+def prox_ffn_phase_times(layer: ProxLayer, x: torch.Tensor, keep_fraction: float = 0.3,
+                         dense: bool = False, stream=None):
+    """One step with per-CTA %globaltimer stamps at the phase boundaries;
+    returns (y, stamps int64 [blocks][PROX_PHASE_STAMPS] on the device)."""
+    y = _x_y(layer, x, None)
+    nb = prox_layer_blocks(layer)
+    ts = torch.zeros(nb, PROX_PHASE_STAMPS, dtype=torch.int64, device=x.device)
+    _check(_load().prox_ffn_phase_times(layer.handle, _ptr(x), float(keep_fraction), _ptr(y),
+                                        _ptr(ts), int(bool(dense)), _stream(stream)),
+           "prox_ffn_phase_times")
+    return y, ts
+
+
+def prox_test_barrier_timeout(layer: ProxLayer, x: torch.Tensor, stream=None) -> int:
+    """Failure-detection test hook: a step whose first grid barrier can not
+    complete; returns the status the bounded waits recorded."""
+    y = _x_y(layer, x, None)
+    return int(_load().prox_test_barrier_timeout(layer.handle, _ptr(x), _ptr(y), _stream(stream)))
 
 
 def prox_layer_info(layer: ProxLayer):

@@ -40,7 +40,8 @@
  *   - Calls that share one prox_layer use its workspace and must be ordered
  *     with respect to each other (one stream, or events); calls on
  *     different layers are independent.
- *   - Shapes: d_model a multiple of 128 in [128, 16384]; d_ff in [1, 32768].
+ *   - Shapes: d_model a multiple of 128 in [128, 16384]; d_ff in [1, 32768]
+ *     (prox_prepare also needs ceil(d_ff / #SMs) <= 512).
  *   - Inputs must be finite (no NaN or Inf in x or the weights).
  */
 #ifndef PROX_H
@@ -149,21 +150,43 @@ PROX_API prox_status prox_ffn_host(const prox_layer* layer, const void* x_host, 
                           float* y_host, prox_stream_t stream);
 
 /* Number of CUDA events prox_ffn_traced records. */
-#define PROX_TRACE_EVENTS 5
+#define PROX_TRACE_EVENTS 2
 
 /*
  * prox_ffn_ex that also records `events` (n_events == PROX_TRACE_EVENTS
  * cudaEvent_t handles, created by the caller with timing enabled) around its
- * kernels: events[0] before the input selection, events[1] after it,
- * events[2] after the proxy GEMV, events[3] after the channel select and
- * events[4] after Stage 2, so cudaEventElapsedTime(events[i], events[i+1])
- * is the duration of kernel i+1 on the stream.  Inside a stream capture the
- * records become event nodes of the graph (cudaEventRecordExternal).  For
- * per-kernel timing only; it launches the same kernels as prox_ffn_ex.
+ * kernel: the decode step is one persistent kernel, so
+ * cudaEventElapsedTime(events[0], events[1]) is its duration on the stream.
+ * Inside a stream capture the records become event nodes of the graph
+ * (cudaEventRecordExternal).  For timing only; it launches the same kernel
+ * as prox_ffn_ex.
  */
 PROX_API prox_status prox_ffn_traced(const prox_layer* layer, const void* x, float keep_fraction,
                             float input_keep, float* y, void* const* events, int n_events,
                             prox_stream_t stream);
+
+/* Number of phase timestamps per CTA written by prox_ffn_phase_times. */
+#define PROX_PHASE_STAMPS 10
+
+/* Number of CTAs (one per SM) the layer's kernels launch.  Host only. */
+PROX_API int prox_layer_blocks(const prox_layer* layer);
+
+/*
+ * Tracing: one decode step (dense == 0, input keep 0.5) or one dense step
+ * (dense != 0, keep_fraction ignored) that also stores, per CTA b, the
+ * device clock (%globaltimer, ns) at its phase boundaries into
+ * stamps[b * PROX_PHASE_STAMPS + i] (uint64, device, prox_layer_blocks()
+ * rows, zeroed first; a phase the kernel does not have stays 0):
+ *   0 start; 1 input selection done; 2 proxy partials written;
+ *   3 past the first grid barrier; 4 scores and histogram done;
+ *   5 past the second grid barrier; 6 Stage 2 begins (channel list ready);
+ *   7 first gate|up row landed; 8 Stage 2 dot products done; 9 end.
+ * The dense step stamps 0 and 6..9 only.  Same results as prox_ffn /
+ * prox_dense_ffn.
+ */
+PROX_API prox_status prox_ffn_phase_times(const prox_layer* layer, const void* x,
+                                 float keep_fraction, float* y, uint64_t* stamps, int dense,
+                                 prox_stream_t stream);
 
 /* Dense SwiGLU FFN, Eq. (1) of the PrunePath page over all d_ff channels,
  * streaming the same gateup / down_t buffers (the in-library dense
@@ -193,8 +216,21 @@ PROX_API prox_status prox_residual_rmsnorm(int d_model, const void* x, const flo
                                   void* x_next, prox_stream_t stream);
 
 /* Synchronises the stream, returns the status recorded on the device by
- * earlier calls on this layer (PROX_OK if none) and clears it. */
+ * earlier calls on this layer (PROX_OK if none) and clears it.  After a
+ * fault it also resets the layer's grid-barrier word, so later calls on the
+ * layer run normally again. */
 PROX_API prox_status prox_get_status(const prox_layer* layer, prox_stream_t stream);
+
+/*
+ * Failure-detection test hook (not for production use): runs one decode
+ * step in which one CTA withholds its arrival at the first grid barrier and
+ * every bounded wait gives up after 20 ms, then synchronises and returns
+ * the layer's status, which is PROX_ERR_TIMEOUT when the bounded waits work
+ * (the status and barrier words are reset as by prox_get_status).  y is
+ * left undefined.  x bf16 [d_model], y fp32 [d_model], both device.
+ */
+PROX_API prox_status prox_test_barrier_timeout(const prox_layer* layer, const void* x, float* y,
+                                      prox_stream_t stream);
 
 /* Shapes of a prepared layer.  Host only. */
 PROX_API prox_status prox_layer_info(const prox_layer* layer, int* d_model, int* d_ff);

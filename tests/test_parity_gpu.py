@@ -11,8 +11,8 @@ import torch
 
 import oracle
 from free_swiglu_ffn_prox_b300 import synth
-from parity_util import (ATOL_Y, RTOL_L2_Y, decode_proxy, host_bits, tie_band_mask_check,
-                         y_errors)
+from parity_util import (ATOL_Y, RTOL_L2_Y, TIE_BAND, decode_proxy, host_bits,
+                         tie_band_mask_check, y_errors)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,11 +55,16 @@ def _check_step(prox, L, w, x, rho, kappa=0.5, px=None):
     g, u, sc = oracle.proxy_scores(px.q_gate, px.s_gate, px.q_up, px.s_up, xb, kept_or)
     sc_gpu = r["scores"].cpu().numpy().astype(np.float64)
     # fp32 proxy vs fp64 oracle, measured on the ranking scale: the k-th score
-    # (or the median score, when k is so large that the k-th is near zero)
+    # (or the median score, when k is so large that the k-th is near zero).
+    # The bound is half the tie band: with every score within band/2 of the
+    # oracle's, no two channels whose oracle scores lie outside the band around
+    # the k-th can change order, so the band covers all fp32 rounding.  (An fp32
+    # sum of k_x products that cancel to ~1/sqrt(k_x) of their magnitude sum
+    # carries ~sqrt(k_x) * 2^-24 relative error: about 1e-5 at k_x = 4096.)
     kth = np.sort(sc)[::-1][k - 1]
     scale = max(kth, float(np.median(sc)), 1e-30)
     rel = np.abs(sc_gpu - sc) / np.maximum(np.abs(sc), scale)
-    assert rel.max() < 1e-5, rel.max()
+    assert rel.max() < TIE_BAND / 2, rel.max()
     idx = r["idx"].cpu().numpy()
     bad, in_band = tie_band_mask_check(idx, sc, k)
     assert bad == 0, f"{bad} channels outside the tie band disagree ({in_band} in band)"
@@ -216,6 +221,37 @@ def test_host_buffer_and_traced_entry_points(prox):
     dt = [evs[i].elapsed_time(evs[i + 1]) for i in range(prox.PROX_TRACE_EVENTS - 1)]
     assert all(t >= 0.0 for t in dt)
     assert prox.prox_get_status(L) == 0
+
+
+def test_bounded_barrier_wait_reports_timeout_and_recovers(prox):
+    """Failure detection without a GPU fault: one CTA withholds its arrival
+    at a grid barrier, the others give up after 20 ms and record
+    PROX_ERR_TIMEOUT; the status read resets the barrier and the next step on
+    the same layer is correct again."""
+    d, F = 512, 1500
+    L, w = _layer(prox, d, F, seed=41)
+    x = _x(d, 5, 42)
+    _check_step(prox, L, w, x, 0.3)
+    assert prox.prox_test_barrier_timeout(L, x.cuda()) == prox.PROX_ERR_TIMEOUT
+    assert prox.prox_get_status(L) == 0
+    _check_step(prox, L, w, x, 0.3)
+    _check_step(prox, L, w, _x(d, 5, 43), 0.1)
+
+
+def test_masks_are_deterministic(prox):
+    """The proxy partials are summed in a fixed order, so repeated steps give
+    the same scores and the same channel list bit for bit."""
+    d, F = 4096, 14336
+    wg, wu, wd = synth.make_weights(d, F, 0.02, 5, device="cuda")
+    L = prox.prox_prepare(wg, wu, wd)
+    x = _x(d, 41, 6).cuda()
+    r1 = prox.prox_ffn_debug(L, x, 0.3)
+    r2 = prox.prox_ffn_debug(L, x, 0.3)
+    torch.cuda.synchronize()
+    assert torch.equal(r1["scores"], r2["scores"])
+    assert torch.equal(r1["idx"], r2["idx"])
+    assert torch.equal(r1["kept"], r2["kept"])
+    assert torch.allclose(r1["y"], r2["y"], rtol=0, atol=1e-5 * float(r1["y"].abs().max()))
 
 
 # ------------------------------------------------------------- full-size layers
