@@ -324,6 +324,43 @@ def graphs_for(fn_step, K: int, stream):
     return seq
 
 
+def run_phases(args):
+    """Per-phase timeline of the fused decode kernel (prox_ffn_phase_times):
+    for several steps, the median over CTAs of each phase boundary, in us
+    after the earliest CTA start; also the dense kernel.  One JSON line."""
+    import numpy as np
+    import torch
+
+    from free_swiglu_ffn_prox_b300 import prox, synth
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    shape = synth.LLAMA3_8B
+    wl = Workload(prox, synth, shape, 4, dev)
+    for i in range(32):
+        L, x, y = wl.slot(i)
+        prox.prox_ffn(L, x, args.keep_fraction, y=y)
+    torch.cuda.synchronize()
+    out = {"workload": f"{shape.name} keep_fraction {args.keep_fraction}", "unit": "us",
+           "phases": list(prox.PHASES), "steps": {}}
+    for mode in ("prox", "dense"):
+        rows = []
+        for i in range(8):
+            L, x, _ = wl.slot(i)
+            _, ts = prox.prox_ffn_phase_times(L, x, args.keep_fraction, dense=(mode == "dense"))
+            torch.cuda.synchronize()
+            t = ts.cpu().numpy().astype(np.int64)
+            t0 = t[:, 0].min()
+            rows.append([float(np.median(t[:, j] - t0)) / 1e3 if (t[:, j] != 0).all() else None
+                         for j in range(prox.PROX_PHASE_STAMPS)])
+        med = []
+        for j in range(prox.PROX_PHASE_STAMPS):
+            v = [r[j] for r in rows if r[j] is not None]
+            med.append(round(float(np.median(v)), 2) if v else None)
+        out["steps"][mode] = dict(zip(prox.PHASES, med))
+    print(json.dumps(out), flush=True)
+
+
 def run_gpu(args):
     import torch
 
@@ -645,11 +682,15 @@ def main():
     ap.add_argument("--reference-budget", type=float, default=90.0,
                     help="time cap of the --impl reference timed region, seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--phases", action="store_true",
+                    help="print the per-phase timeline of the decode kernel instead")
     args = ap.parse_args()
     if args.steps < 1:
         raise SystemExit("--steps must be >= 1")
     if args.impl == "reference":
         run_reference(args)
+    elif args.phases:
+        run_phases(args)
     else:
         run_gpu(args)
 

@@ -44,7 +44,8 @@ constexpr int kGuProducerWarp = 16;
 constexpr int kDProducerWarp = 17;
 constexpr int kMaxStages = 16;
 constexpr int kMaxChan = 512;            // Stage-2 channels per CTA
-constexpr int kUnroll = 8;               // proxy rows in flight per thread
+constexpr int kRing = 8;                 // proxy rows in flight per thread (cp.async ring)
+static_assert((kRing & (kRing - 1)) == 0, "ring depth must be a power of two");
 constexpr int kHistBins = 2048;
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kPhaseStamps = 10;
@@ -61,12 +62,14 @@ struct Ctl {
     float h[kMaxChan];
     uint32_t warp_tot[kNT / 32 + 1];
     uint32_t sel[4];
-    float fmax_part[kNT / 32];
+    uint64_t ld_bar[2];  // bulk loads of the proxy scales (P1) and the scores (P3)
+    unsigned epoch;
     int abort;
     int chan[kMaxChan];
 };
 
 constexpr size_t ctl_bytes() { return (sizeof(Ctl) + 127) / 128 * 128; }
+__host__ __device__ constexpr size_t area_budget_dev() { return kSmemLimit - ctl_bytes(); }
 
 struct FusedParams {
     // layer
@@ -84,6 +87,7 @@ struct FusedParams {
     // workspace
     int* status;
     unsigned* bar;
+    unsigned* epoch;     // number of completed calls on this workspace
     uint32_t* hist;      // [kHistBins]
     float2* part;        // [slices][Fp]
     float* scores;       // [Fp]
@@ -100,42 +104,41 @@ struct FusedParams {
 };
 
 // ----------------------------------------------------------------- helpers
-__device__ __forceinline__ unsigned atom_add_release_gpu(unsigned* p, unsigned v) {
-    unsigned old;
-    asm volatile("atom.add.release.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
-// Grid-wide barrier for co-resident CTAs without a reset between uses: CTA 0
-// adds 2^31 - (n - 1), every other CTA adds 1, so each completed barrier
-// flips bit 31 and leaves the low bits unchanged.  Returns false (and
-// records PROX_ERR_TIMEOUT) if the flip does not come within limit_ns.
-__device__ bool grid_barrier(unsigned* bar, int* status, long long limit_ns, Ctl& ctl,
-                             bool skip_arrive) {
+__device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide barrier for co-resident CTAs.  The barrier word counts arrivals
+// and is never reset between calls: in call number `epoch` (read by every
+// CTA at its start) barrier i (1 or 2) completes when the word reaches
+// n * (2 epoch + i).  Arrivals are fire-and-forget release reductions; CTA
+// thread 0 polls with acquire loads.  Returns false (and records
+// PROX_ERR_TIMEOUT) if the count does not arrive within limit_ns.
+__device__ bool grid_barrier(unsigned* bar, unsigned target, int* status, long long limit_ns,
+                             Ctl& ctl, bool skip_arrive) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        bool ok = true;
-        if (!skip_arrive) {
-            __threadfence();
-            const unsigned inc = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1) : 1u;
-            const unsigned old = atom_add_release_gpu(bar, inc);
-            const uint64_t t0 = global_timer_ns();
-            for (uint32_t it = 0;; ++it) {
-                if (((ld_acquire_gpu(bar) ^ old) & 0x80000000u) != 0) break;
-                if ((it & 15u) == 15u && (long long)(global_timer_ns() - t0) > limit_ns) {
-                    ok = false;
-                    break;
+        bool ok = !skip_arrive;
+        if (ok) {
+            red_add_release_gpu(bar, 1u);
+            uint64_t t0 = 0;
+            for (uint32_t it = 1;; ++it) {
+                if ((int)(ld_acquire_gpu(bar) - target) >= 0) break;
+                if ((it & 15u) == 0) {
+                    const uint64_t now = global_timer_ns();
+                    if (t0 == 0) t0 = now;
+                    else if ((long long)(now - t0) > limit_ns) {
+                        ok = false;
+                        break;
+                    }
                 }
             }
-            __threadfence();
-        } else {
-            ok = false;
         }
         if (!ok) {
             record_status(status, PROX_ERR_TIMEOUT);
@@ -146,8 +149,64 @@ __device__ bool grid_barrier(unsigned* bar, int* status, long long limit_ns, Ctl
     return ctl.abort == 0;
 }
 
-// Exclusive scan of one value per thread over the block; also the total.
-__device__ __forceinline__ uint32_t block_scan(uint32_t v, Ctl& ctl, uint32_t& total) {
+// Given a histogram h[nbins] of digits (nbins a multiple of 128, at most
+// 2048) and krem >= 1 with sum(h) >= krem, warp 0 finds the digit b with
+// sum(h[b+1..]) < krem <= sum(h[b..]) and stores (b, krem - sum(h[b+1..]))
+// in sel[0..1].  Level 1: lane l sums the nbins/32 bins just below
+// nbins - l nbins/32 (independent vector loads) and a warp scan finds the
+// lane holding the k-th; level 2 spreads that lane's bins over the warp
+// (at most two per lane) and scans again.  No data-dependent loop.  Called
+// by warp 0 only; the caller synchronises.
+template <int NBINS>
+__device__ __forceinline__ void select_bin_warp(const uint32_t* h, uint32_t krem, uint32_t* sel) {
+    constexpr int PER = NBINS / 32, NQ = PER / 4, PER2 = PER > 32 ? 2 : 1;
+    static_assert(NBINS % 128 == 0 && NBINS <= 2048, "bins");
+    const int lane = threadIdx.x & 31;
+    const int lo = NBINS - (lane + 1) * PER;
+    const uint4* hv = reinterpret_cast<const uint4*>(h + lo);
+    uint4 w[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) w[q] = hv[q];  // all loads in flight at once
+    uint32_t sum = 0;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) sum += (w[q].x + w[q].y) + (w[q].z + w[q].w);
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, incl - sum < krem && incl >= krem);
+    const int L = hit ? __ffs(hit) - 1 : 0;  // hit != 0 whenever sum(h) >= krem
+    const uint32_t above_l = __shfl_sync(0xffffffffu, incl - sum, L);
+    const int top = NBINS - L * PER - 1;  // lane L's highest bin
+    // level 2: lane l takes bins top - PER2 l and (PER2 = 2) top - 2 l - 1
+    const int b0 = top - lane * PER2;
+    uint32_t v0 = 0, v1 = 0;
+    if (lane * PER2 < PER) v0 = h[b0];
+    if (PER2 == 2 && lane * 2 + 1 < PER) v1 = h[b0 - 1];
+    const uint32_t s2 = v0 + v1;
+    uint32_t incl2 = s2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl2, o);
+        if (lane >= o) incl2 += t;
+    }
+    const uint32_t above2 = above_l + incl2 - s2;
+    if (above2 < krem && above2 + s2 >= krem) {
+        if (above2 + v0 >= krem) {
+            sel[0] = (uint32_t)b0;
+            sel[1] = krem - above2;
+        } else {
+            sel[0] = (uint32_t)(b0 - 1);
+            sel[1] = krem - above2 - v0;
+        }
+    }
+}
+
+// Exclusive scan of one value per thread over the block (warp shuffles, one
+// barrier); also returns the block total.  Uses ctl.warp_tot.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Ctl& ctl, uint32_t& total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     uint32_t s = v;
 #pragma unroll
@@ -157,96 +216,103 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, Ctl& ctl, uint32_t& t
     }
     if (lane == 31) ctl.warp_tot[wid] = s;
     __syncthreads();
-    if (wid == 0) {
-        const uint32_t w = lane < kNT / 32 ? ctl.warp_tot[lane] : 0u;
-        uint32_t ws = w;
+    uint32_t wp = 0, tt = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, ws, o);
-            if (lane >= o) ws += t;
-        }
-        if (lane < kNT / 32) ctl.warp_tot[lane] = ws - w;
-        if (lane == kNT / 32 - 1) ctl.warp_tot[kNT / 32] = ws;
+    for (int w = 0; w < kNT / 32; ++w) {
+        const uint32_t x = ctl.warp_tot[w];
+        wp += w < wid ? x : 0u;
+        tt += x;
+    }
+    total = tt;
+    return wp + s - v;
+}
+
+// Exact top-k over n keys in shared memory (thread t owns the contiguous
+// keys [t kpt, (t+1) kpt), kpt <= 64), ties to the lower index, in three
+// radix digits: d1 = key >> s1 from a histogram h1 already built, then the
+// next digits over the thread's own candidates only (the keys in the
+// selected d1 bin, tracked in a bit mask), so only the first pass touches
+// every key.  Produces T (the k-th key) and r (ties at T to keep) in
+// ctl.sel[0..1], and for this thread: the number of selected keys before
+// its range (in ascending index order) and a candidate mask.
+struct TopkPlan {
+    int s1, n1;        // digit-1 shift and histogram size (h1)
+    int s2, n2;        // digit-2 shift and bins (h2), digit 3 = key & (n3 - 1)
+    int n3;
+};
+
+template <typename KeyFn>
+__device__ __forceinline__ void topk_digits(const TopkPlan& pl, int n, int kpt, uint32_t k,
+                                            KeyFn key, uint32_t* h1, uint32_t* h2, uint32_t* h3,
+                                            Ctl& ctl, uint32_t& T, uint32_t& r, uint32_t& pos0,
+                                            uint32_t& ties_before, uint32_t& nsel) {
+    const int wid = threadIdx.x >> 5;
+    const int i0 = threadIdx.x * kpt;
+    // digit 1 from h1
+    if (wid == 0) {
+        if (pl.n1 == 2048) select_bin_warp<2048>(h1, k, ctl.sel);
+        else select_bin_warp<256>(h1, k, ctl.sel);
     }
     __syncthreads();
-    const uint32_t excl = ctl.warp_tot[wid] + s - v;
-    total = ctl.warp_tot[kNT / 32];
-    __syncthreads();
-    return excl;
-}
-
-// h[bin] += 1 for the active lanes, one atomic per distinct bin in the warp.
-// Every lane of the warp must call it.
-__device__ __forceinline__ void hist_add_smem(uint32_t* h, uint32_t bin, bool active) {
-    const unsigned m = __ballot_sync(0xffffffffu, active);
-    if (active) {
-        const unsigned peers = __match_any_sync(m, bin);
-        if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
-    }
-}
-
-__device__ __forceinline__ void hist_add_global(uint32_t* h, uint32_t bin, bool active) {
-    const unsigned m = __ballot_sync(0xffffffffu, active);
-    if (active) {
-        const unsigned peers = __match_any_sync(m, bin);
-        if ((threadIdx.x & 31) == __ffs(peers) - 1)
-            asm volatile("red.global.add.u32 [%0], %1;" ::"l"(h + bin), "r"((uint32_t)__popc(peers))
-                         : "memory");
-    }
-}
-
-// Given a histogram h[nbins] of digits and krem >= 1 with sum(h) >= krem,
-// finds the digit b with sum(h[b+1..]) < krem <= sum(h[b..]) and returns
-// (b, krem - sum(h[b+1..])) in ctl.sel[0..1] for every thread.
-__device__ void select_bin(const uint32_t* h, int nbins, uint32_t krem, Ctl& ctl) {
-    const int per = (nbins + kNT - 1) / kNT;
-    // thread t owns the bins [nbins - (t+1) per, nbins - t per) (from the top)
-    const int hi = nbins - threadIdx.x * per;
-    const int lo = max(hi - per, 0);
-    uint32_t sum = 0;
-    for (int b = lo; b < hi; ++b) sum += h[b];
-    uint32_t total;
-    const uint32_t above = block_scan(hi > 0 ? sum : 0u, ctl, total);  // count in bins >= hi
-    if (hi > 0 && above < krem && above + sum >= krem) {
-        uint32_t acc = above;
-        for (int b = hi - 1; b >= lo; --b) {
-            if (acc + h[b] >= krem) {
-                ctl.sel[0] = (uint32_t)b;
-                ctl.sel[1] = krem - acc;
-                break;
-            }
-            acc += h[b];
+    const uint32_t b1 = ctl.sel[0], k1 = ctl.sel[1];
+    uint32_t gt1 = 0;
+    uint64_t cmask = 0;
+    for (int e = 0; e < kpt; ++e) {
+        const int i = i0 + e;
+        if (i < n) {
+            const uint32_t d1 = key(i) >> pl.s1;
+            gt1 += d1 > b1;
+            cmask |= (uint64_t)(d1 == b1) << e;
         }
     }
+    for (uint64_t m = cmask; m; m &= m - 1)
+        atomicAdd(&h2[(key(i0 + __ffsll((long long)m) - 1) >> pl.s2) & (pl.n2 - 1)], 1u);
     __syncthreads();
-}
-
-// Emits, in ascending index order, the indices i < n whose key(i) > T plus
-// the first r (lowest) with key(i) == T.  emit(pos, i) is called for each.
-template <typename KeyFn, typename Emit>
-__device__ void compact_topk(int n, uint32_t T, uint32_t r, KeyFn key, Emit emit, Ctl& ctl) {
-    const int per = (n + kNT - 1) / kNT;
-    const int i0 = min(n, (int)threadIdx.x * per), i1 = min(n, i0 + per);
-    uint32_t gt = 0, eq = 0;
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t kk = key(i);
+    if (wid == 0) {
+        if (pl.n2 == 2048) select_bin_warp<2048>(h2, k1, ctl.sel);
+        else select_bin_warp<128>(h2, k1, ctl.sel);
+    }
+    __syncthreads();
+    const uint32_t b12 = (b1 << (pl.s1 - pl.s2)) | ctl.sel[0], k2 = ctl.sel[1];
+    if (pl.n3 > 1) {
+        for (uint64_t m = cmask; m; m &= m - 1) {
+            const uint32_t kk = key(i0 + __ffsll((long long)m) - 1);
+            if ((kk >> pl.s2) == b12) atomicAdd(&h3[kk & (pl.n3 - 1)], 1u);
+        }
+        __syncthreads();
+        if (wid == 0) select_bin_warp<512>(h3, k2, ctl.sel);
+        __syncthreads();
+        T = (b12 << pl.s2) | ctl.sel[0];
+        r = ctl.sel[1];
+    } else {
+        T = b12;
+        r = k2;
+    }
+    // per-thread counts from the sure keys and the thread's own candidates
+    uint32_t gt = gt1, eq = 0;
+    for (uint64_t m = cmask; m; m &= m - 1) {
+        const uint32_t kk = key(i0 + __ffsll((long long)m) - 1);
         gt += kk > T;
         eq += kk == T;
     }
-    uint32_t tg, te;
-    const uint32_t pg = block_scan(gt, ctl, tg);
-    const uint32_t pe = block_scan(eq, ctl, te);
-    uint32_t pos = pg + min(pe, r);
-    uint32_t tie = pe;
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t kk = key(i);
-        bool keep = kk > T;
-        if (kk == T) {
-            keep = tie < r;
-            ++tie;
-        }
-        if (keep) emit(pos++, i);
-    }
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(gt | (eq << 16), ctl, tot);
+    ties_before = ex >> 16;
+    pos0 = (ex & 0xffffu) + min(ties_before, r);  // selected keys before this range
+    nsel = gt + (ties_before < r ? min(eq, r - ties_before) : 0u);
+}
+
+// fp16 bits of x * 2^shift for a bf16 x (exact whenever the result is a
+// normal fp16; the same rounding as ldexpf followed by __float2half_rn).
+__device__ __forceinline__ uint16_t scaled_fp16(uint16_t xb, int shift) {
+    const uint32_t f = (uint32_t)xb << 16;
+    const int e = (int)((f >> 23) & 0xffu);
+    float v;
+    if (e != 0 && e + shift > 0 && e + shift < 255)
+        v = __uint_as_float(f + ((uint32_t)shift << 23));  // exact power-of-two scaling
+    else
+        v = ldexpf(__uint_as_float(f), shift);
+    return __half_as_ushort(__float2half_rn(v));
 }
 
 // --------------------------------------------------------------- proxy math
@@ -296,12 +362,21 @@ __device__ __forceinline__ void proxy_mac_word(uint32_t w, uint16_t xh, float* a
     fma_f32_f16x2(au[1], au[3], u13, xh);
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p, uint64_t pol) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p), "l"(pol));
-    return v;
+// 16-byte global -> shared copy that bypasses L1 (cp.async), L2 policy hint.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
+                 "l"(src), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Waits until at most N of this thread's cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------- stage 2
@@ -373,9 +448,7 @@ __device__ void stage2(const Stage2Args& a, Ctl& ctl, uint8_t* area, int n) {
         }
         fence_mbar_init();
     }
-    for (int i = threadIdx.x; i < nchunk; i += kNT)
-        reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
-    __syncthreads();
+    __syncthreads();  // the producers start before the consumers fetch x
 
     if (warp == kGuProducerWarp || warp == kDProducerWarp) {
         if (lane == 0) {
@@ -405,6 +478,9 @@ __device__ void stage2(const Stage2Args& a, Ctl& ctl, uint8_t* area, int n) {
             }
         }
     } else {
+        for (int i = threadIdx.x; i < nchunk; i += kConsumers)
+            reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+        named_barrier_sync(1, kConsumers);
         // ------------------------------------------------ pass A: h per channel
         // Warp w < n_gu owns gate|up slot w and takes channels w, w + n_gu, ...
         // Each slot's uses are consumed in order by one warp, so a parity wait
@@ -505,66 +581,85 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nb = gridDim.x, b = blockIdx.x;
     const int d = p.d, F = p.F, Fp = p.Fp;
-    if (tid == 0) ctl.abort = 0;
     stamp(p.ts, 0);
+    if (tid == 0) {
+        ctl.abort = 0;
+        ctl.epoch = *reinterpret_cast<volatile unsigned*>(p.epoch);
+        mbar_init(&ctl.ld_bar[0], 1);
+        mbar_init(&ctl.ld_bar[1], 1);
+        fence_mbar_init();
+    }
 
     // ------------------------------------------------ P0: input sparsity
-    uint16_t* xs = reinterpret_cast<uint16_t*>(area);                       // [d]
-    uint32_t* kept = reinterpret_cast<uint32_t*>(area + (size_t)2 * d);      // [d]
-    uint32_t* hsm = kept + d;                                                // [kHistBins]
+    // area: x bf16 [d] | kept u32 [d] | histograms u32 [1024] | P1 tables
+    // Warp w takes the x entries [w Lx, (w+1) Lx), lane-consecutive.
+    uint16_t* xs = reinterpret_cast<uint16_t*>(area);
+    uint32_t* kept = reinterpret_cast<uint32_t*>(area + (size_t)2 * d);
+    uint32_t* hA = kept + d;
     for (int i = tid; i < d / 8; i += kNT)
         reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
+    for (int i = tid; i < 384; i += kNT) hA[i] = 0u;
     if (b == 0) {
         for (int i = tid; i < d; i += kNT) p.y[i] = 0.0f;
         for (int i = tid; i < kHistBins; i += kNT) p.hist[i] = 0u;
     }
-    for (int i = tid; i < 256; i += kNT) hsm[i] = 0u;
     __syncthreads();
-    int shift;
+    // exact top-k_x of |x| (15-bit keys): digit 1 = exponent (bits 14..7),
+    // digit 2 = the 7 mantissa bits; thread t owns [t kpx, (t+1) kpx)
+    const int kpx = (d + kNT - 1) / kNT;
+    const int xi0 = tid * kpx;
+    auto xkey = [&](int i) { return (uint32_t)(xs[i] & 0x7fffu); };
     {
         uint32_t mk = 0;
-        for (int i = tid; i < d; i += kNT) mk = max(mk, (uint32_t)(xs[i] & 0x7fffu));
+        for (int e = 0; e < kpx; ++e) {
+            const int i = xi0 + e;
+            if (i < d) {
+                const uint32_t kk = xkey(i);
+                mk = max(mk, kk);
+                atomicAdd(&hA[kk >> 7], 1u);
+            }
+        }
         mk = __reduce_max_sync(0xffffffffu, mk);
         if (lane == 0) ctl.warp_tot[wid] = mk;
-        __syncthreads();
-        mk = 0;
+    }
+    __syncthreads();
+    if (tid == 0) {  // power-of-two prescale: max|x| * 2^shift in [2^14, 2^15)
+        uint32_t mk = 0;
         for (int w = 0; w < kNT / 32; ++w) mk = max(mk, ctl.warp_tot[w]);
-        shift = 0;
+        int sh = 0;
         if (mk != 0) {
             int ex;
             frexpf(__uint_as_float(mk << 16), &ex);  // max|x| in [2^(ex-1), 2^ex)
-            shift = 15 - ex;
+            sh = 15 - ex;
         }
-        __syncthreads();
+        ctl.sel[2] = (uint32_t)sh;
     }
-    // digit 1: |x| bits 14..7
-    const int xrounds = (d + kNT - 1) / kNT;
-    for (int e = 0; e < xrounds; ++e) {
-        const int i = tid + e * kNT;
-        const uint32_t kk = i < d ? (xs[i] & 0x7fffu) : 0u;
-        hist_add_smem(hsm, kk >> 7, i < d);
+    uint32_t xT, xr, xpos, xties, xn;
+    {
+        const TopkPlan plx{7, 256, 0, 128, 1};
+        topk_digits(plx, d, kpx, (uint32_t)p.kx, xkey, hA, hA + 256, nullptr, ctl, xT, xr, xpos,
+                    xties, xn);
     }
-    __syncthreads();
-    select_bin(hsm, 256, (uint32_t)p.kx, ctl);
-    const uint32_t xb1 = ctl.sel[0], xk1 = ctl.sel[1];
-    for (int i = tid; i < 128; i += kNT) hsm[i] = 0u;
-    __syncthreads();
-    for (int e = 0; e < xrounds; ++e) {
-        const int i = tid + e * kNT;
-        const uint32_t kk = i < d ? (xs[i] & 0x7fffu) : 0u;
-        hist_add_smem(hsm, kk & 127u, i < d && (kk >> 7) == xb1);
+    const int shift = (int)ctl.sel[2];
+    if (xn) {
+        uint32_t pos = xpos, tie = xties;
+        for (int e = 0; e < kpx; ++e) {
+            const int j = xi0 + e;
+            if (j < d) {
+                const uint32_t kk = xkey(j);
+                bool keep = kk > xT;
+                if (kk == xT) {
+                    keep = tie < xr;
+                    ++tie;
+                }
+                if (keep) {
+                    kept[pos] = ((uint32_t)j << 16) | scaled_fp16(xs[j], shift);
+                    if (b == 0 && p.kept_out) p.kept_out[pos] = j;
+                    ++pos;
+                }
+            }
+        }
     }
-    __syncthreads();
-    select_bin(hsm, 128, xk1, ctl);
-    const uint32_t xT = (xb1 << 7) | ctl.sel[0], xr = ctl.sel[1];
-    compact_topk(
-        d, xT, xr, [&](int i) { return (uint32_t)(xs[i] & 0x7fffu); },
-        [&](uint32_t pos, int j) {
-            const float xv = ldexpf(__uint_as_float((uint32_t)xs[j] << 16), shift);
-            kept[pos] = ((uint32_t)j << 16) | __half_as_ushort(__float2half_rn(xv));
-            if (b == 0 && p.kept_out) p.kept_out[pos] = j;
-        },
-        ctl);
     __syncthreads();
     stamp(p.ts, 1);
 
@@ -580,23 +675,58 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         const bool active = rl < R && cu * 16 < width;
         const int r0 = (int)((long long)slice * p.kx / p.slices);
         const int r1 = (int)((long long)(slice + 1) * p.kx / p.slices);
+        // row-lane rl takes the contiguous kept rows [q_beg, q_end)
+        const int m = (r1 - r0 + R - 1) / R;
+        const int q_beg = min(r1, r0 + rl * m), q_end = min(r1, q_beg + m);
         // running totals, [R][16][tpr] float2: channel cu * 16 + t of row-lane
         // rl at (rl * 16 + t) * tpr + cu, so a warp's lanes (consecutive cu)
         // touch consecutive 8-byte words
-        float2* tot = reinterpret_cast<float2*>(hsm + kHistBins);
+        float2* tot = reinterpret_cast<float2*>(hA + 1024);
+        // per-thread ring of proxy row segments in flight, [kRing][kNT]
+        uint4* ring = reinterpret_cast<uint4*>(tot + (size_t)R * 16 * tpr);
+        uint8_t* after_ring = reinterpret_cast<uint8_t*>(ring + (size_t)kRing * kNT);
+        const size_t room = area_budget_dev() - (size_t)(after_ring - area);
+        // the slice's fp16 scale pairs, [g - g_lo][W], loaded by bulk copies
+        int g_lo = 0, ng = 0;
+        if (r1 > r0) {
+            g_lo = (int)(kept[r0] >> 23);
+            ng = (int)(kept[r1 - 1] >> 23) - g_lo + 1;
+        }
+        uint32_t* ssc = reinterpret_cast<uint32_t*>(after_ring);
+        const bool smem_scales = ng > 0 && (size_t)ng * W * 4 <= room;
+        if (tid == 0 && smem_scales) {
+            const uint64_t pol = policy_evict_first();
+            mbar_arrive_expect_tx(&ctl.ld_bar[0], (uint32_t)(ng * width * 4));
+            for (int g = 0; g < ng; ++g)
+                bulk_g2s(ssc + (size_t)g * W, p.scales + (size_t)(g_lo + g) * Fp + c0,
+                         (uint32_t)(width * 4), &ctl.ld_bar[0], pol);
+        }
         if (active)
             for (int t = 0; t < 16; ++t) tot[((size_t)rl * 16 + t) * tpr + cu] = make_float2(0.0f, 0.0f);
         float ag[16], au[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) ag[t] = au[t] = 0.0f;
         int cur_g = -1;
+        bool scales_in = false;
         auto flush = [&]() {
             if (cur_g < 0) return;
-            const uint4* src = reinterpret_cast<const uint4*>(p.scales + (size_t)cur_g * Fp + c0 + cu * 16);
+            const uint4* src;
+            if (smem_scales) {
+                if (!scales_in) {
+                    if (!mbar_wait_bounded(&ctl.ld_bar[0], 0, p.limit_ns, &ctl.abort)) {
+                        ctl.abort = 1;
+                        record_status(p.status, PROX_ERR_TIMEOUT);
+                    }
+                    scales_in = true;
+                }
+                src = reinterpret_cast<const uint4*>(ssc + (size_t)(cur_g - g_lo) * W + cu * 16);
+            } else {
+                src = reinterpret_cast<const uint4*>(p.scales + (size_t)cur_g * Fp + c0 + cu * 16);
+            }
             float2* dst = tot + (size_t)rl * 16 * tpr + cu;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-                const uint4 s4 = __ldg(src + v);
+                const uint4 s4 = src[v];
                 const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -611,56 +741,77 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                 }
             }
         };
-        if (active) {
+        if (active && q_beg < q_end) {
+            // kRing rows in flight per thread through a cp.async ring in
+            // shared memory (slot s of thread t at ring[s * kNT + t]); each
+            // thread reads only its own slots, so no block synchronisation.
+            // With tpr a multiple of 16 the row, and kept[q], is uniform
+            // across each half-warp.  One row per iteration keeps the loop
+            // body (and its instruction footprint) small.
             const uint64_t pol = policy_evict_first();
             const uint8_t* colbase = p.codes + c0 + cu * 16;
-            for (int q0 = r0 + rl; q0 < r1; q0 += R * kUnroll) {
-                uint4 w[kUnroll];
-                uint32_t kp[kUnroll];
+            uint4* my = ring + tid;
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int q = q0 + u * R;
-                    kp[u] = 0;
-                    w[u] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-                    if (q < r1) {
-                        kp[u] = kept[q];
-                        w[u] = ldg_stream(colbase + (size_t)(kp[u] >> 16) * Fp, pol);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int q = q0 + u * R;
-                    if (q < r1) {
-                        const int g = (int)(kp[u] >> 23);  // j / 128
-                        if (g != cur_g) {
-                            flush();
-                            cur_g = g;
-                        }
-                        const uint16_t xh = (uint16_t)(kp[u] & 0xffffu);
-                        proxy_mac_word(w[u].x, xh, &ag[0], &au[0]);
-                        proxy_mac_word(w[u].y, xh, &ag[4], &au[4]);
-                        proxy_mac_word(w[u].z, xh, &ag[8], &au[8]);
-                        proxy_mac_word(w[u].w, xh, &ag[12], &au[12]);
-                    }
-                }
+            for (int u = 0; u < kRing; ++u) {
+                const int q = q_beg + u;
+                if (q < q_end)
+                    cp_async_16(my + (size_t)u * kNT, colbase + (size_t)(kept[q] >> 16) * Fp, pol);
+                cp_async_commit();
             }
+            int s = 0;
+#pragma unroll 1
+            for (int q = q_beg; q < q_end; ++q) {
+                cp_async_wait_group<kRing - 1>();  // row q has landed
+                const uint4 w = my[(size_t)s * kNT];
+                const uint32_t kp = kept[q];
+                const int qn = q + kRing;
+                if (qn < q_end)
+                    cp_async_16(my + (size_t)s * kNT, colbase + (size_t)(kept[qn] >> 16) * Fp, pol);
+                cp_async_commit();
+                s = (s + 1) & (kRing - 1);
+                const int g = (int)(kp >> 23);  // j / 128
+                if (g != cur_g) {
+                    flush();
+                    cur_g = g;
+                }
+                const uint16_t xh = (uint16_t)(kp & 0xffffu);
+                proxy_mac_word(w.x, xh, &ag[0], &au[0]);
+                proxy_mac_word(w.y, xh, &ag[4], &au[4]);
+                proxy_mac_word(w.z, xh, &ag[8], &au[8]);
+                proxy_mac_word(w.w, xh, &ag[12], &au[12]);
+            }
+            cp_async_wait_group<0>();
             flush();
         }
+        // the scale copy must have landed before this shared memory is reused
+        if (smem_scales && !scales_in)
+            if (!mbar_wait_bounded(&ctl.ld_bar[0], 0, p.limit_ns, &ctl.abort)) {
+                ctl.abort = 1;
+                record_status(p.status, PROX_ERR_TIMEOUT);
+            }
         __syncthreads();
         float2* out = p.part + (size_t)slice * Fp + c0;
-        for (int cl = tid; cl < width; cl += kNT) {
-            float g = 0.0f, u = 0.0f;
-            const int cu_ = cl >> 4, t_ = cl & 15;
-            for (int r = 0; r < R; ++r) {
-                const float2 v = tot[((size_t)r * 16 + t_) * tpr + cu_];
-                g += v.x;
-                u += v.y;
+        // thread e sums channel (e % tpr) * 16 + e / tpr over the row-lanes:
+        // consecutive threads read consecutive 8-byte words
+        for (int e = tid; e < 16 * tpr; e += kNT) {
+            const int cu_ = e % tpr, t_ = e / tpr;
+            const int cl = cu_ * 16 + t_;
+            if (cl < width) {
+                float g = 0.0f, u = 0.0f;
+                for (int r = 0; r < R; ++r) {
+                    const float2 v = tot[((size_t)r * 16 + t_) * tpr + cu_];
+                    g += v.x;
+                    u += v.y;
+                }
+                out[cl] = make_float2(ldexpf(g, -shift), ldexpf(u, -shift));
             }
-            out[cl] = make_float2(ldexpf(g, -shift), ldexpf(u, -shift));
         }
     }
     stamp(p.ts, 2);
-    if (!grid_barrier(p.bar, p.status, p.limit_ns, ctl, p.inject == 1 && b == nb - 1)) return;
+    const unsigned ep = ctl.epoch;
+    if (!grid_barrier(p.bar, (unsigned)nb * (2u * ep + 1u), p.status, p.limit_ns, ctl,
+                      p.inject == 1 && b == nb - 1))
+        return;
     stamp(p.ts, 3);
 
     // ------------------------------------------------ P2: scores + histogram
@@ -671,67 +822,114 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
             const bool act = c < cb1;
             uint32_t key = 0;
             if (act) {
+                float2 v[kMaxSlices];
+#pragma unroll
+                for (int sl = 0; sl < kMaxSlices; ++sl)
+                    if (sl < p.slices) v[sl] = __ldcg(p.part + (size_t)sl * Fp + c);
                 float g = 0.0f, u = 0.0f;
-                for (int s = 0; s < p.slices; ++s) {
-                    const float2 v = __ldcg(p.part + (size_t)s * Fp + c);
-                    g += v.x;
-                    u += v.y;
-                }
+#pragma unroll
+                for (int sl = 0; sl < kMaxSlices; ++sl)
+                    if (sl < p.slices) {
+                        g += v[sl].x;
+                        u += v[sl].y;
+                    }
                 // |silu(g~) * u~|, silu(z) = z / (1 + e^-z)
                 const float sc = fabsf(g / (1.0f + expf(-g)) * u);
                 p.scores[c] = sc;
                 if (p.scores_out) p.scores_out[c] = sc;
                 key = __float_as_uint(sc);
             }
-            hist_add_global(p.hist, key >> 20, act);
+            // one reduction per distinct bin in the warp
+            const unsigned am = __ballot_sync(0xffffffffu, act);
+            if (act) {
+                const unsigned peers = __match_any_sync(am, key >> 20);
+                if (lane == __ffs(peers) - 1)
+                    asm volatile("red.global.add.u32 [%0], %1;" ::"l"(p.hist + (key >> 20)),
+                                 "r"((uint32_t)__popc(peers))
+                                 : "memory");
+            }
         }
     }
     stamp(p.ts, 4);
-    if (!grid_barrier(p.bar, p.status, p.limit_ns, ctl, false)) return;
+    if (!grid_barrier(p.bar, (unsigned)nb * (2u * ep + 2u), p.status, p.limit_ns, ctl, false))
+        return;
+    if (b == 0 && tid == 0) *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;
     stamp(p.ts, 5);
 
     // ------------------------------------------------ P3: exact top-k, this CTA's share
     int n_mine;
     {
-        uint32_t* h = reinterpret_cast<uint32_t*>(area);                        // [kHistBins]
-        float* sc = reinterpret_cast<float*>(area + kHistBins * sizeof(uint32_t)); // [F]
-        for (int i = tid; i < kHistBins; i += kNT) h[i] = __ldcg(p.hist + i);
-        for (int i = tid; i < F; i += kNT) sc[i] = __ldcg(p.scores + i);
-        __syncthreads();
-        select_bin(h, kHistBins, (uint32_t)p.k, ctl);
-        const uint32_t b1 = ctl.sel[0], k1 = ctl.sel[1];
-        for (int i = tid; i < kHistBins; i += kNT) h[i] = 0u;
-        __syncthreads();
-        const int frounds = (F + kNT - 1) / kNT;
-        for (int e = 0; e < frounds; ++e) {
-            const int i = tid + e * kNT;
-            const uint32_t kk = i < F ? __float_as_uint(sc[i]) : 0u;
-            hist_add_smem(h, (kk >> 9) & 2047u, i < F && (kk >> 20) == b1);
+        // area: global histogram copy [2048] | digit-2 histogram [2048] |
+        // digit-3 histogram [512] | scores [Fp]
+        uint32_t* h1 = reinterpret_cast<uint32_t*>(area);
+        uint32_t* h2 = h1 + kHistBins;
+        uint32_t* h3 = h2 + kHistBins;
+        float* sc = reinterpret_cast<float*>(h3 + 512);
+        if (tid == 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const uint64_t pol = policy_evict_first();
+            mbar_arrive_expect_tx(&ctl.ld_bar[1], (uint32_t)(kHistBins * 4 + Fp * 4));
+            bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.ld_bar[1], pol);
+            bulk_g2s(sc, p.scores, (uint32_t)(Fp * 4), &ctl.ld_bar[1], pol);
+        }
+        for (int i = tid; i < kHistBins + 512; i += kNT) h2[i] = 0u;
+        if (!mbar_wait_bounded(&ctl.ld_bar[1], 0, p.limit_ns, &ctl.abort) && lane == 0) {
+            ctl.abort = 1;
+            record_status(p.status, PROX_ERR_TIMEOUT);
         }
         __syncthreads();
-        select_bin(h, kHistBins, k1, ctl);
-        const uint32_t b12 = (b1 << 11) | ctl.sel[0], k2 = ctl.sel[1];
-        for (int i = tid; i < 512; i += kNT) h[i] = 0u;
-        __syncthreads();
-        for (int e = 0; e < frounds; ++e) {
-            const int i = tid + e * kNT;
-            const uint32_t kk = i < F ? __float_as_uint(sc[i]) : 0u;
-            hist_add_smem(h, kk & 511u, i < F && (kk >> 9) == b12);
+        if (ctl.abort) {
+            // let the copy land (bounded) before the shared memory is released
+            if (tid == 0) mbar_wait_bounded(&ctl.ld_bar[1], 0, p.limit_ns, nullptr);
+            return;
         }
-        __syncthreads();
-        select_bin(h, 512, k2, ctl);
-        const uint32_t T = (b12 << 9) | ctl.sel[0], r = ctl.sel[1];
+        // exact top-k of the score bit patterns: digits of 11, 11 and 9 bits;
+        // thread t owns the channels [t kpf, (t+1) kpf)
+        const int kpf = (F + kNT - 1) / kNT;  // <= 57
+        const int ci0 = tid * kpf;
+        auto skey = [&](int i) { return __float_as_uint(sc[i]); };
+        uint32_t T, r, cpos, cties, cn;
+        {
+            const TopkPlan pls{20, 2048, 9, 2048, 512};
+            topk_digits(pls, F, kpf, (uint32_t)p.k, skey, h1, h2, h3, ctl, T, r, cpos, cties, cn);
+        }
         const int p0 = (int)((long long)p.k * b / nb), p1 = (int)((long long)p.k * (b + 1) / nb);
         n_mine = p1 - p0;
-        compact_topk(
-            F, T, r, [&](int i) { return __float_as_uint(sc[i]); },
-            [&](uint32_t pos, int c) {
-                if ((int)pos >= p0 && (int)pos < p1) {
-                    ctl.chan[pos - p0] = c;
-                    if (p.idx_out) p.idx_out[pos] = c;
+        // only the threads whose positions [cpos, cpos + cn) meet [p0, p1) emit
+        if (cn && (int)(cpos + cn) > p0 && (int)cpos < p1) {
+            uint32_t pos = cpos, tie = cties;
+            for (int e = 0; e < kpf; ++e) {
+                const int c = ci0 + e;
+                if (c < F) {
+                    const uint32_t kk = skey(c);
+                    bool keep = kk > T;
+                    if (kk == T) {
+                        keep = tie < r;
+                        ++tie;
+                    }
+                    if (keep) {
+                        if ((int)pos >= p0 && (int)pos < p1) ctl.chan[pos - p0] = c;
+                        ++pos;
+                    }
                 }
-            },
-            ctl);
+            }
+        }
+        // the debug channel list: every selected channel, by its owner thread
+        if (p.idx_out && b == 0 && cn) {
+            uint32_t pos = cpos, tie = cties;
+            for (int e = 0; e < kpf; ++e) {
+                const int c = ci0 + e;
+                if (c < F) {
+                    const uint32_t kk = skey(c);
+                    bool keep = kk > T;
+                    if (kk == T) {
+                        keep = tie < r;
+                        ++tie;
+                    }
+                    if (keep) p.idx_out[pos++] = c;
+                }
+            }
+        }
         __syncthreads();
     }
 
@@ -808,21 +1006,24 @@ cudaError_t set_smem(K kern) {
 }  // namespace
 
 ProxyGeom proxy_geometry(int F, int kx, int num_blocks) {
+    // Tiles of W = 256, 512 or 1024 channels (a half-warp, a warp or two
+    // warps per proxy row), T tiles x S slices <= blocks; minimise the
+    // bytes of the busiest CTA, then prefer fewer slices (less partial
+    // traffic).
     const int Fp = padded_ff(F);
-    const int units = Fp / 16;
-    ProxyGeom best{1, 1, units * 16};
+    ProxyGeom best{1, 1, 1024};
     long long best_cost = -1;
-    for (int T = 1; T <= num_blocks && T <= units; ++T) {
+    for (int W : {256, 512, 1024}) {
+        const int T = (Fp + W - 1) / W;
+        if (T > num_blocks) continue;
         int S = num_blocks / T;
         if (S > kMaxSlices) S = kMaxSlices;
         if (S > kx) S = kx;
         if (S < 1) S = 1;
-        const int wu = (units + T - 1) / T;
-        if (wu * 16 > 16 * kNT) continue;  // a row segment needs at most one thread per 16 bytes
-        const long long cost = (long long)wu * 16 * ((kx + S - 1) / S);
+        const long long cost = (long long)min(W, Fp) * ((kx + S - 1) / S);
         if (best_cost < 0 || cost < best_cost || (cost == best_cost && S < best.slices)) {
             best_cost = cost;
-            best = {T, S, wu * 16};
+            best = {T, S, W};
         }
     }
     return best;
@@ -847,8 +1048,8 @@ int fused_max_chan() { return kMaxChan; }
 bool fused_fits(int d, int F) {
     // P0: x (2 d) + kept list (4 d) + histogram; P1 adds the [R][W] partial
     // table (at most 8 * 16 * kNT bytes); P3: histogram + F scores; P4: rings.
-    const size_t p01 = (size_t)6 * d + kHistBins * 4 + (size_t)8 * 16 * kNT;
-    const size_t p3 = (size_t)kHistBins * 4 + (size_t)4 * F;
+    const size_t p01 = (size_t)6 * d + 4096 + (size_t)8 * 16 * kNT + (size_t)16 * kRing * kNT;
+    const size_t p3 = (size_t)(2 * kHistBins + 512) * 4 + (size_t)4 * padded_ff(F);
     const Ring r = ring_for(d);
     return p01 <= area_budget() && p3 <= area_budget() && ring_bytes(d, r) <= area_budget() &&
            r.n_gu >= 1 && r.n_d >= 1;
@@ -873,6 +1074,7 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     p.tile_w = geo.tile_w;
     p.status = L.ws->status;
     p.bar = L.ws->bar;
+    p.epoch = L.ws->bar + 1;
     p.hist = L.ws->hist;
     p.part = L.ws->part;
     p.scores = L.ws->scores;
