@@ -9,16 +9,6 @@
 
 #include "prox_internal.cuh"
 
-struct prox_layer {
-    int d_model, d_ff, Fp;
-    int device, num_sms, num_blocks;
-    const uint8_t* codes;
-    const __half2* scales;
-    const __nv_bfloat16* gateup;
-    const __nv_bfloat16* down_t;
-    prox::Workspace ws;
-};
-
 namespace prox {
 
 static size_t align256(size_t v) { return (v + 255) / 256 * 256; }

@@ -182,3 +182,15 @@ cudaError_t launch_residual_rmsnorm(int d, const uint16_t* x, const float* y, fl
                                     uint16_t* x_next, cudaStream_t stream);
 
 }  // namespace prox
+
+// The host handle behind the opaque prox_layer of prox.h: shapes, grid size
+// and the caller's device buffers given to prox_prepare.
+struct prox_layer {
+    int d_model, d_ff, Fp;
+    int device, num_sms, num_blocks;
+    const uint8_t* codes;
+    const __half2* scales;
+    const __nv_bfloat16* gateup;
+    const __nv_bfloat16* down_t;
+    prox::Workspace ws;
+};

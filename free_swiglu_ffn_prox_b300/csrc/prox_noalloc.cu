@@ -1,0 +1,96 @@
+// prox_noalloc.cu -- prox_ffn_noalloc: the decode step with its per-call
+// scratch in a fixed array compiled into the library, for callers that can
+// not allocate device memory when they run a step.
+//
+// Who needs it: code that runs under an allocator it does not own (an
+// inference server or framework that reserved the whole device up front and
+// rejects further cudaMalloc calls), plugins and real-time loops where a
+// device allocation would synchronise the device or is forbidden by policy,
+// and callers that simply hold the prepared weights but no spare buffer.
+// Such callers pass only inputs and outputs; the proxy partials, the score
+// histogram, the scores and the grid-barrier words live in `g_scratch`.
+//
+// The array is a file-scope __device__ variable, so every device that loads
+// the library holds kScratchBytes of it until the process exits, and every
+// call on a device shares it: calls that overlap on the GPU (two streams,
+// two host threads) race on it and must be ordered by the caller.  Host code
+// must not pass `g_scratch` itself to a kernel (in host code the name is a
+// host-side stand-in, not a device address); the device address is looked up
+// once per device with cudaGetSymbolAddress, on the first call made on that
+// device, which should therefore come before any stream capture.
+#include <mutex>
+
+#include "prox_internal.cuh"
+
+namespace prox {
+namespace {
+
+constexpr size_t kScratchBytes = (size_t)4 << 20;  // 4 MiB per device
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void* g_addr[kMaxDevices] = {};
+
+// Device address of g_scratch on the current device (set up on first use).
+cudaError_t scratch_address(int dev, void** out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_addr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+        if (e != cudaSuccess) return e;
+        g_addr[dev] = p;
+    }
+    *out = g_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace prox
+
+extern "C" PROX_API prox_status prox_ffn_noalloc(const prox_layer* layer, const void* x,
+                                                 float keep_fraction, float* y,
+                                                 prox_stream_t stream) {
+    if (!layer || !x || !y) return PROX_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(y) & 15u))
+        return PROX_ERR_MISALIGNED;
+    const int k = prox_keep_count(layer->d_ff, keep_fraction);
+    if (k < 1) return PROX_ERR_INVALID_ARG;
+    // the scratch must hold this layer's workspace (proxy partials dominate)
+    if (prox::workspace_bytes(layer->d_model, layer->d_ff) > prox::kScratchBytes)
+        return PROX_ERR_UNSUPPORTED_SHAPE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PROX_ERR_CUDA;
+    if (dev != layer->device || dev < 0 || dev >= prox::kMaxDevices) return PROX_ERR_INVALID_ARG;
+    void* base = nullptr;
+    if (prox::scratch_address(dev, &base) != cudaSuccess) return PROX_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's contents: restart the grid-barrier
+    // count and epoch (the first 256 bytes) from zero.  The histogram is
+    // cleared by the kernel; partials and scores are overwritten.
+    if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return PROX_ERR_CUDA;
+    prox::Workspace ws = prox::carve_workspace(base, layer->d_model, layer->d_ff);
+    ws.status = layer->ws.status;  // faults stay visible to prox_get_status(layer)
+    prox::FusedLaunch f;
+    f.codes = layer->codes;
+    f.scales = layer->scales;
+    f.gateup = layer->gateup;
+    f.down_t = layer->down_t;
+    f.d = layer->d_model;
+    f.F = layer->d_ff;
+    f.x = static_cast<const uint16_t*>(x);
+    f.y = y;
+    f.kx = prox_keep_count(layer->d_model, 0.5f);
+    f.k = k;
+    f.ws = &ws;
+    f.kept_out = nullptr;
+    f.scores_out = nullptr;
+    f.idx_out = nullptr;
+    f.h_out = nullptr;
+    f.num_blocks = layer->num_blocks;
+    f.limit_ns = prox::kWaitLimitNs;
+    f.inject = 0;
+    f.ts = nullptr;
+    return prox::launch_fused(f, s) == cudaSuccess ? PROX_OK : PROX_ERR_CUDA;
+}

@@ -234,6 +234,24 @@ def prox_ffn_traced(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, eve
     return y
 
 
+def prox_ffn_noalloc(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, y=None,
+                     stream=None):
+    """prox_ffn whose per-step scratch lives in a fixed array inside the
+    library (no workspace of the caller's is used).  For callers that cannot
+    allocate device memory while stepping; see prox.h for the limits (the
+    layer's workspace must fit in 4 MiB; overlapping calls race)."""
+    lib = _load()
+    fn = lib.prox_ffn_noalloc
+    if fn.argtypes is None:
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                       ctypes.c_void_p]
+    y = _x_y(layer, x, y)
+    _check(fn(layer.handle, _ptr(x), float(keep_fraction), _ptr(y), _stream(stream)),
+           "prox_ffn_noalloc")
+    return y
+
+
 def prox_dense_ffn(layer: ProxLayer, x: torch.Tensor, y=None, stream=None):
     y = _x_y(layer, x, y)
     _check(_load().prox_dense_ffn(layer.handle, _ptr(x), _ptr(y), _stream(stream)),

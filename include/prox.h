@@ -215,6 +215,36 @@ PROX_API prox_status prox_ffn_debug(const prox_layer* layer, const void* x, floa
 PROX_API prox_status prox_residual_rmsnorm(int d_model, const void* x, const float* y, float eps,
                                   void* x_next, prox_stream_t stream);
 
+/*
+ * prox_ffn without any caller-provided scratch (the pages have no
+ * counterpart: this is a deployment variant).  For callers that cannot
+ * allocate device memory when they run a step -- a host framework or server
+ * that reserved the device up front and refuses further allocations, plugins
+ * and latency-critical loops where an allocation would synchronise the
+ * device -- the step's scratch (proxy partials, score histogram, scores,
+ * grid-barrier words) lives in a fixed 4 MiB array compiled into the
+ * library, which every device that loads the library holds until the process
+ * exits.  Nothing is allocated: no cudaMalloc, cudaFree or allocating
+ * library routine is called.
+ *   x  bf16 [d_model], device; keep_fraction in (0, 1] (input keep 0.5);
+ *   y  fp32 [d_model], device, overwritten as by prox_ffn.
+ * Limits and rules:
+ *   - the layer's workspace (prox_query_sizes().workspace) must fit in
+ *     4 MiB (every layer up to d_model 8192, d_ff 28672 does); larger layers
+ *     return PROX_ERR_UNSUPPORTED_SHAPE and queue nothing;
+ *   - the layer's device must be the current device (else
+ *     PROX_ERR_INVALID_ARG);
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture;
+ *   - every call on a device shares the array and finds the previous call's
+ *     contents (the call clears what must start at zero); calls that overlap
+ *     on the GPU race and must be ordered by the caller;
+ *   - device-side faults are recorded in the layer's status word, as for
+ *     prox_ffn (prox_get_status).
+ */
+PROX_API prox_status prox_ffn_noalloc(const prox_layer* layer, const void* x, float keep_fraction,
+                             float* y, prox_stream_t stream);
+
 /* Synchronises the stream, returns the status recorded on the device by
  * earlier calls on this layer (PROX_OK if none) and clears it.  After a
  * fault it also resets the layer's grid-barrier word, so later calls on the

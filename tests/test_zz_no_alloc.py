@@ -1,0 +1,62 @@
+"""prox_ffn_noalloc: the decode step with its scratch in a fixed array inside
+the library, for callers that cannot allocate device memory while they step.
+
+Collected last on purpose (file name), so that a run stopping at the first
+failure has run every other test before this one.  Checks the no-allocation
+entry point against prox_ffn on the same layer and input, twice in a row (the
+second call finds the first call's scratch contents), within the output bar
+the parity tests use, and that a layer whose scratch would not fit is
+rejected before anything is queued."""
+import numpy as np
+import pytest
+import torch
+
+from free_swiglu_ffn_prox_b300 import synth
+from parity_util import ATOL_Y, RTOL_L2_Y, y_errors
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def prox():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from free_swiglu_ffn_prox_b300 import build, prox as p
+
+    build.build()
+    return p
+
+
+@pytest.mark.parametrize("d,F,rho", [(1024, 3000, 0.3), (4096, 14336, 0.3)])
+def test_no_alloc_matches_prox_ffn_twice(prox, d, F, rho):
+    wg, wu, wd = synth.make_weights(d, F, 0.02, 51, device="cuda")
+    L = prox.prox_prepare(wg, wu, wd)
+    x = synth.make_x(d, max(1, d // 100), 20.0, 52).cuda()
+    y_ref = prox.prox_ffn(L, x, rho).cpu().numpy().astype(np.float64)
+    for _ in range(2):
+        y = prox.prox_ffn_noalloc(L, x, rho)
+        torch.cuda.synchronize()
+        assert prox.prox_get_status(L) == 0
+        mx, rl = y_errors(y.cpu().numpy(), y_ref)
+        assert mx <= ATOL_Y and rl <= RTOL_L2_Y, (mx, rl)
+        # same mask (deterministic scores), so only the order of the fp32
+        # output additions differs
+        assert mx <= 1e-5 * max(1.0, float(np.abs(y_ref).max()))
+    # a second layer shares the same scratch
+    wg2, wu2, wd2 = synth.make_weights(d, F, 0.02, 53, device="cuda")
+    L2 = prox.prox_prepare(wg2, wu2, wd2)
+    y2_ref = prox.prox_ffn(L2, x, rho).cpu().numpy().astype(np.float64)
+    y2 = prox.prox_ffn_noalloc(L2, x, rho)
+    torch.cuda.synchronize()
+    mx, rl = y_errors(y2.cpu().numpy(), y2_ref)
+    assert mx <= ATOL_Y and rl <= RTOL_L2_Y, (mx, rl)
+
+
+def test_no_alloc_rejects_a_layer_too_large_for_the_scratch(prox):
+    d, F = 128, 32768  # proxy partials alone need 4 MiB
+    wg, wu, wd = synth.make_weights(d, F, 0.02, 54, device="cuda")
+    L = prox.prox_prepare(wg, wu, wd)
+    x = torch.ones(d, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(prox.ProxError) as e:
+        prox.prox_ffn_noalloc(L, x, 0.3)
+    assert e.value.code == prox.PROX_ERR_UNSUPPORTED_SHAPE
