@@ -206,6 +206,15 @@ __device__ __forceinline__ void select_bin_warp(const uint32_t* h, uint32_t krem
 
 // Exclusive scan of one value per thread over the block (warp shuffles, one
 // barrier); also returns the block total.  Uses ctl.warp_tot.
+// Barrier over the first NT threads: __syncthreads for the whole block,
+// named barrier 1 for a prefix of warps.
+template <int NT>
+__device__ __forceinline__ void group_sync() {
+    if (NT == kNT) __syncthreads();
+    else named_barrier_sync(1, NT);
+}
+
+template <int NT = kNT>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Ctl& ctl, uint32_t& total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     uint32_t s = v;
@@ -215,10 +224,10 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Ctl& ctl, uint32
         if (lane >= o) s += t;
     }
     if (lane == 31) ctl.warp_tot[wid] = s;
-    __syncthreads();
+    group_sync<NT>();
     uint32_t wp = 0, tt = 0;
 #pragma unroll
-    for (int w = 0; w < kNT / 32; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
         const uint32_t x = ctl.warp_tot[w];
         wp += w < wid ? x : 0u;
         tt += x;
@@ -241,7 +250,7 @@ struct TopkPlan {
     int n3;
 };
 
-template <typename KeyFn>
+template <int NT, typename KeyFn>
 __device__ __forceinline__ void topk_digits(const TopkPlan& pl, int n, int kpt, uint32_t k,
                                             KeyFn key, uint32_t* h1, uint32_t* h2, uint32_t* h3,
                                             Ctl& ctl, uint32_t& T, uint32_t& r, uint32_t& pos0,
@@ -253,7 +262,7 @@ __device__ __forceinline__ void topk_digits(const TopkPlan& pl, int n, int kpt, 
         if (pl.n1 == 2048) select_bin_warp<2048>(h1, k, ctl.sel);
         else select_bin_warp<256>(h1, k, ctl.sel);
     }
-    __syncthreads();
+    group_sync<NT>();
     const uint32_t b1 = ctl.sel[0], k1 = ctl.sel[1];
     uint32_t gt1 = 0;
     uint64_t cmask = 0;
@@ -267,21 +276,21 @@ __device__ __forceinline__ void topk_digits(const TopkPlan& pl, int n, int kpt, 
     }
     for (uint64_t m = cmask; m; m &= m - 1)
         atomicAdd(&h2[(key(i0 + __ffsll((long long)m) - 1) >> pl.s2) & (pl.n2 - 1)], 1u);
-    __syncthreads();
+    group_sync<NT>();
     if (wid == 0) {
         if (pl.n2 == 2048) select_bin_warp<2048>(h2, k1, ctl.sel);
         else select_bin_warp<128>(h2, k1, ctl.sel);
     }
-    __syncthreads();
+    group_sync<NT>();
     const uint32_t b12 = (b1 << (pl.s1 - pl.s2)) | ctl.sel[0], k2 = ctl.sel[1];
     if (pl.n3 > 1) {
         for (uint64_t m = cmask; m; m &= m - 1) {
             const uint32_t kk = key(i0 + __ffsll((long long)m) - 1);
             if ((kk >> pl.s2) == b12) atomicAdd(&h3[kk & (pl.n3 - 1)], 1u);
         }
-        __syncthreads();
+        group_sync<NT>();
         if (wid == 0) select_bin_warp<512>(h3, k2, ctl.sel);
-        __syncthreads();
+        group_sync<NT>();
         T = (b12 << pl.s2) | ctl.sel[0];
         r = ctl.sel[1];
     } else {
@@ -296,10 +305,15 @@ __device__ __forceinline__ void topk_digits(const TopkPlan& pl, int n, int kpt, 
         eq += kk == T;
     }
     uint32_t tot;
-    const uint32_t ex = block_excl_scan(gt | (eq << 16), ctl, tot);
+    const uint32_t ex = block_excl_scan<NT>(gt | (eq << 16), ctl, tot);
     ties_before = ex >> 16;
     pos0 = (ex & 0xffffu) + min(ties_before, r);  // selected keys before this range
     nsel = gt + (ties_before < r ? min(eq, r - ties_before) : 0u);
+}
+
+// Bulk prefetch of global memory into L2 (no shared-memory destination).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // fp16 bits of x * 2^shift for a bf16 x (exact whenever the result is a
@@ -572,6 +586,89 @@ __device__ void stage2(const Stage2Args& a, Ctl& ctl, uint8_t* area, int n) {
     }
 }
 
+// P3: every CTA finishes the exact top-k of the scores itself (threads
+// 0..NT-1; NT a multiple of 32, named barrier 1): the global digit-1
+// histogram and all scores arrive by bulk copy, three radix digits over each
+// thread's own candidates give the threshold, one block scan the positions;
+// the CTA keeps the channels at positions [p0, p1) in ctl.chan.  On a
+// timeout it raises ctl.abort (after letting the copy land).
+template <int NT>
+__device__ __forceinline__ void select_channels(const FusedParams& p, Ctl& ctl, uint8_t* area,
+                                                int b, int nb, int p0, int p1) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int F = p.F, Fp = p.Fp;
+    // area: global histogram copy [2048] | digit-2 histogram [2048] |
+    // digit-3 histogram [512] | scores [Fp]
+    uint32_t* h1 = reinterpret_cast<uint32_t*>(area);
+    uint32_t* h2 = h1 + kHistBins;
+    uint32_t* h3 = h2 + kHistBins;
+    float* sc = reinterpret_cast<float*>(h3 + 512);
+    if (tid == 0) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        const uint64_t pol = policy_evict_first();
+        mbar_arrive_expect_tx(&ctl.ld_bar[1], (uint32_t)(kHistBins * 4 + Fp * 4));
+        bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.ld_bar[1], pol);
+        bulk_g2s(sc, p.scores, (uint32_t)(Fp * 4), &ctl.ld_bar[1], pol);
+    }
+    for (int i = tid; i < kHistBins + 512; i += NT) h2[i] = 0u;
+    if (!mbar_wait_bounded(&ctl.ld_bar[1], 0, p.limit_ns, &ctl.abort) && lane == 0) {
+        ctl.abort = 1;
+        record_status(p.status, PROX_ERR_TIMEOUT);
+    }
+    named_barrier_sync(1, NT);
+    if (ctl.abort) {
+        // let the copy land (bounded) before the shared memory is released
+        if (tid == 0) mbar_wait_bounded(&ctl.ld_bar[1], 0, p.limit_ns, nullptr);
+        return;
+    }
+    // exact top-k of the score bit patterns: digits of 11, 11 and 9 bits;
+    // thread t owns the channels [t kpf, (t+1) kpf)
+    const int kpf = (F + NT - 1) / NT;  // <= 64
+    const int ci0 = tid * kpf;
+    auto skey = [&](int i) { return __float_as_uint(sc[i]); };
+    uint32_t T, r, cpos, cties, cn;
+    {
+        const TopkPlan pls{20, 2048, 9, 2048, 512};
+        topk_digits<NT>(pls, F, kpf, (uint32_t)p.k, skey, h1, h2, h3, ctl, T, r, cpos, cties, cn);
+    }
+    // only the threads whose positions [cpos, cpos + cn) meet [p0, p1) emit
+    if (cn && (int)(cpos + cn) > p0 && (int)cpos < p1) {
+        uint32_t pos = cpos, tie = cties;
+        for (int e = 0; e < kpf; ++e) {
+            const int c = ci0 + e;
+            if (c < F) {
+                const uint32_t kk = skey(c);
+                bool keep = kk > T;
+                if (kk == T) {
+                    keep = tie < r;
+                    ++tie;
+                }
+                if (keep) {
+                    if ((int)pos >= p0 && (int)pos < p1) ctl.chan[pos - p0] = c;
+                    ++pos;
+                }
+            }
+        }
+    }
+    // the debug channel list: every selected channel, by its owner thread
+    if (p.idx_out && b == 0 && cn) {
+        uint32_t pos = cpos, tie = cties;
+        for (int e = 0; e < kpf; ++e) {
+            const int c = ci0 + e;
+            if (c < F) {
+                const uint32_t kk = skey(c);
+                bool keep = kk > T;
+                if (kk == T) {
+                    keep = tie < r;
+                    ++tie;
+                }
+                if (keep) p.idx_out[pos++] = c;
+            }
+        }
+    }
+    (void)nb;
+}
+
 // ------------------------------------------------------------ fused kernel
 template <int CPT>
 __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
@@ -637,8 +734,8 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     uint32_t xT, xr, xpos, xties, xn;
     {
         const TopkPlan plx{7, 256, 0, 128, 1};
-        topk_digits(plx, d, kpx, (uint32_t)p.kx, xkey, hA, hA + 256, nullptr, ctl, xT, xr, xpos,
-                    xties, xn);
+        topk_digits<kNT>(plx, d, kpx, (uint32_t)p.kx, xkey, hA, hA + 256, nullptr, ctl, xT, xr,
+                         xpos, xties, xn);
     }
     const int shift = (int)ctl.sel[2];
     if (xn) {
@@ -815,8 +912,9 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     stamp(p.ts, 3);
 
     // ------------------------------------------------ P2: scores + histogram
+    const int cb0 = (int)((long long)F * b / nb), cb1 = (int)((long long)F * (b + 1) / nb);
+    float* lsc = ctl.h;  // this chunk's scores (ctl.h is Stage 2's, free until then)
     {
-        const int cb0 = (int)((long long)F * b / nb), cb1 = (int)((long long)F * (b + 1) / nb);
         for (int c00 = cb0; c00 < cb1; c00 += kNT) {
             const int c = c00 + tid;
             const bool act = c < cb1;
@@ -837,6 +935,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                 const float sc = fabsf(g / (1.0f + expf(-g)) * u);
                 p.scores[c] = sc;
                 if (p.scores_out) p.scores_out[c] = sc;
+                lsc[c - cb0] = sc;
                 key = __float_as_uint(sc);
             }
             // one reduction per distinct bin in the warp
@@ -851,87 +950,65 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         }
     }
     stamp(p.ts, 4);
-    if (!grid_barrier(p.bar, (unsigned)nb * (2u * ep + 2u), p.status, p.limit_ns, ctl, false))
-        return;
-    if (b == 0 && tid == 0) *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;
-    stamp(p.ts, 5);
-
-    // ------------------------------------------------ P3: exact top-k, this CTA's share
-    int n_mine;
-    {
-        // area: global histogram copy [2048] | digit-2 histogram [2048] |
-        // digit-3 histogram [512] | scores [Fp]
-        uint32_t* h1 = reinterpret_cast<uint32_t*>(area);
-        uint32_t* h2 = h1 + kHistBins;
-        uint32_t* h3 = h2 + kHistBins;
-        float* sc = reinterpret_cast<float*>(h3 + 512);
+    // Grid barrier 2, then the channel selection (P3) on warps 0..15 while
+    // warp 17 prefetches: the channels ranked in the top 90% of this chunk's
+    // expected share of the mask are almost surely selected, and their
+    // Stage-2 rows (gate|up, W_down^T) are prefetched into L2 so that HBM
+    // streams during the selection.  A wrong guess costs bandwidth only.  The
+    // prefetch warp stays off the selection's barriers (bulk prefetches can
+    // stall their issuing thread while the copy engine's queue is full).
+    constexpr int kSel = 512;  // threads of warps 0..15
+    const int p0 = (int)((long long)p.k * b / nb), p1 = (int)((long long)p.k * (b + 1) / nb);
+    const int n_mine = p1 - p0;
+    __syncthreads();
+    if (tid == 0) red_add_release_gpu(p.bar, 1u);
+    if (wid == kNT / 32 - 1) {
+        const int nch = cb1 - cb0;
+        const int m = (int)(0.9 * (double)p.k * nch / F);
+        for (int i = lane; i < nch; i += 32) {
+            const float mine = lsc[i];
+            int rank = 0;
+            for (int j = 0; j < nch; ++j) {
+                const float o = lsc[j];
+                rank += (o > mine) || (o == mine && j < i);
+            }
+            if (rank < m) {
+                const int c = cb0 + i;
+                prefetch_l2(p.gateup + (size_t)c * 2 * d, (uint32_t)(4 * d));
+                prefetch_l2(p.down_t + (size_t)c * d, (uint32_t)(2 * d));
+            }
+        }
+    } else if (tid < kSel) {
         if (tid == 0) {
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            const uint64_t pol = policy_evict_first();
-            mbar_arrive_expect_tx(&ctl.ld_bar[1], (uint32_t)(kHistBins * 4 + Fp * 4));
-            bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.ld_bar[1], pol);
-            bulk_g2s(sc, p.scores, (uint32_t)(Fp * 4), &ctl.ld_bar[1], pol);
-        }
-        for (int i = tid; i < kHistBins + 512; i += kNT) h2[i] = 0u;
-        if (!mbar_wait_bounded(&ctl.ld_bar[1], 0, p.limit_ns, &ctl.abort) && lane == 0) {
-            ctl.abort = 1;
-            record_status(p.status, PROX_ERR_TIMEOUT);
-        }
-        __syncthreads();
-        if (ctl.abort) {
-            // let the copy land (bounded) before the shared memory is released
-            if (tid == 0) mbar_wait_bounded(&ctl.ld_bar[1], 0, p.limit_ns, nullptr);
-            return;
-        }
-        // exact top-k of the score bit patterns: digits of 11, 11 and 9 bits;
-        // thread t owns the channels [t kpf, (t+1) kpf)
-        const int kpf = (F + kNT - 1) / kNT;  // <= 57
-        const int ci0 = tid * kpf;
-        auto skey = [&](int i) { return __float_as_uint(sc[i]); };
-        uint32_t T, r, cpos, cties, cn;
-        {
-            const TopkPlan pls{20, 2048, 9, 2048, 512};
-            topk_digits(pls, F, kpf, (uint32_t)p.k, skey, h1, h2, h3, ctl, T, r, cpos, cties, cn);
-        }
-        const int p0 = (int)((long long)p.k * b / nb), p1 = (int)((long long)p.k * (b + 1) / nb);
-        n_mine = p1 - p0;
-        // only the threads whose positions [cpos, cpos + cn) meet [p0, p1) emit
-        if (cn && (int)(cpos + cn) > p0 && (int)cpos < p1) {
-            uint32_t pos = cpos, tie = cties;
-            for (int e = 0; e < kpf; ++e) {
-                const int c = ci0 + e;
-                if (c < F) {
-                    const uint32_t kk = skey(c);
-                    bool keep = kk > T;
-                    if (kk == T) {
-                        keep = tie < r;
-                        ++tie;
-                    }
-                    if (keep) {
-                        if ((int)pos >= p0 && (int)pos < p1) ctl.chan[pos - p0] = c;
-                        ++pos;
+            const unsigned target = (unsigned)nb * (2u * ep + 2u);
+            bool ok = true;
+            uint64_t t0 = 0;
+            for (uint32_t it = 1;; ++it) {
+                if ((int)(ld_acquire_gpu(p.bar) - target) >= 0) break;
+                if ((it & 15u) == 0) {
+                    const uint64_t now = global_timer_ns();
+                    if (t0 == 0) t0 = now;
+                    else if ((long long)(now - t0) > p.limit_ns) {
+                        ok = false;
+                        break;
                     }
                 }
             }
-        }
-        // the debug channel list: every selected channel, by its owner thread
-        if (p.idx_out && b == 0 && cn) {
-            uint32_t pos = cpos, tie = cties;
-            for (int e = 0; e < kpf; ++e) {
-                const int c = ci0 + e;
-                if (c < F) {
-                    const uint32_t kk = skey(c);
-                    bool keep = kk > T;
-                    if (kk == T) {
-                        keep = tie < r;
-                        ++tie;
-                    }
-                    if (keep) p.idx_out[pos++] = c;
-                }
+            if (!ok) {
+                record_status(p.status, PROX_ERR_TIMEOUT);
+                ctl.abort = 1;
+            } else if (b == 0) {
+                *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;
             }
         }
-        __syncthreads();
+        named_barrier_sync(1, kSel);
+        if (!ctl.abort) {
+            stamp(p.ts, 5);
+            select_channels<kSel>(p, ctl, area, b, nb, p0, p1);
+        }
     }
+    __syncthreads();  // channel list ready, prefetches issued
+    if (ctl.abort) return;
 
     // ------------------------------------------------ P4: stage 2
     Stage2Args a;
