@@ -250,6 +250,12 @@ def barrier(ws):
         dist.barrier()
 
 
+def job_rate(steps: int, ms_max: float, world: int) -> float:
+    """Whole-job throughput: the steps all ranks ran over the slowest rank's
+    time (every rank runs the same number of steps)."""
+    return world * steps / (ms_max / 1e3)
+
+
 def max_over_ranks(v: float, ws: int) -> float:
     if ws == 1:
         return v
@@ -414,7 +420,7 @@ def run_gpu(args):
     for L in wl.layers:
         if prox.prox_get_status(L) != 0:
             raise SystemExit("device status set during the timed region")
-    value = ws * K / (ms_max / 1e3)
+    value = job_rate(K, ms_max, ws)
     ms_per_step = ms_max / K
 
     extras = {}
