@@ -530,6 +530,10 @@ def run_gpu(args):
                            "frac_of_measured": round(ab["dense"] / (dus * 1e-6) / 1e9 / hbm_peak, 4),
                            "speedup_prox_over_dense": round(dus / (ms_per_step * 1e3), 3)}
 
+        # ------------------------------------------------ 32-layer stack
+        if not args.no_stack:
+            extras["stack32"] = stack_extra(prox, synth, dev, stream, rho, hbm_peak)
+
     # ------------------------------------------------ end to end (host buffers)
     xh = [x.cpu().pin_memory() for x in wl.xs]
     yh = [torch.empty(d, dtype=torch.float32).pin_memory() for _ in range(N_X)]
@@ -602,6 +606,60 @@ def run_gpu(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def stack_extra(prox, synth, dev, stream, rho, hbm_peak, tokens_per_graph=8, replays=8):
+    """One decode token through 32 stacked 8B-shaped layers (seeds 1000+l):
+    per layer prox_ffn then the residual+RMSNorm glue into the next layer's
+    input.  The 32 prepared layers (13 GB) exceed L2, so no flush is needed."""
+    import torch
+
+    shape = synth.STACK32
+    d, F = shape.d_model, shape.d_ff
+    layers = []
+    for l in range(shape.layers):
+        wg, wu, wd = synth.layer(shape, seed=1000 + l, device=dev)
+        layers.append(prox.prox_prepare(wg, wu, wd))
+        del wg, wu, wd
+    torch.cuda.synchronize(dev)
+    x0 = [synth.hidden(shape, seed=1 + i, device="cpu").to(dev) for i in range(N_X)]
+    xs = [torch.empty(d, dtype=torch.bfloat16, device=dev) for _ in range(shape.layers)]
+    ys = [torch.empty(d, dtype=torch.float32, device=dev) for _ in range(shape.layers)]
+
+    def token(i):
+        x = x0[i % N_X]
+        for l, L in enumerate(layers):
+            prox.prox_ffn(L, x, rho, y=ys[l])
+            prox.prox_residual_rmsnorm(x, ys[l], out=xs[l])
+            x = xs[l]
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            token(i)
+    torch.cuda.synchronize()
+    g = capture(token, tokens_per_graph, 0, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    ms, _, _ = timed_replays([g] * replays, stream)
+    for L in layers:
+        if prox.prox_get_status(L) != 0:
+            raise SystemExit("device status set in the 32-layer stack")
+    n = tokens_per_graph * replays
+    us = ms * 1e3 / n
+    k, kx = keep_count(F, rho), keep_count(d, 0.5)
+    ab = shape.layers * (algorithmic_bytes(d, F, k, kx)["step"] + 2 * d + 4 * d + 2 * d)
+    finite = bool(torch.isfinite(xs[-1].float()).all())
+    out = {"layers": shape.layers, "keep_fraction": rho, "tokens": n,
+           "us_per_token": round(us, 2), "us_per_layer": round(us / shape.layers, 3),
+           "tokens_per_s": round(1e6 / us, 1), "alg_bytes_per_token": ab,
+           "gbs": round(ab / (us * 1e-6) / 1e9, 1),
+           "frac_of_measured": round(ab / (us * 1e-6) / 1e9 / hbm_peak, 4),
+           "launches_per_token": 2 * shape.layers, "final_hidden_finite": finite,
+           "timing": f"{replays} replays of a captured graph of {tokens_per_graph} tokens"}
+    del layers
+    torch.cuda.empty_cache()
+    return out
 
 
 # --------------------------------------------------------------------- CPU oracle
@@ -688,6 +746,8 @@ def main():
     ap.add_argument("--reference-budget", type=float, default=90.0,
                     help="time cap of the --impl reference timed region, seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack", action="store_true",
+                    help="skip the 32-layer stack measurement in the extras")
     ap.add_argument("--phases", action="store_true",
                     help="print the per-phase timeline of the decode kernel instead")
     args = ap.parse_args()

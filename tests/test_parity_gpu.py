@@ -277,3 +277,54 @@ def test_full_size_layers(prox, shape):
     x = synth.hidden(shape, seed=1)
     for rho in shape.keep_fractions:
         _check_step(prox, L, w, x, rho, px=px)
+
+
+# ------------------------------------------------------------- stack glue
+def _bf16_ulp_diff(a_bits, b_bits):
+    """|a - b| in units of the larger bf16 ulp of the pair (both finite)."""
+    a = oracle.bf16_bits_to_f64(a_bits)
+    b = oracle.bf16_bits_to_f64(b_bits)
+    m = np.maximum(np.abs(a), np.abs(b))
+    ulp = np.where(m > 0, 2.0 ** (np.floor(np.log2(np.maximum(m, 1e-300))) - 7), 1.0)
+    return np.abs(a - b) / ulp
+
+
+@pytest.mark.parametrize("d", [128, 1000, 4096, 8192, 16384])
+def test_residual_rmsnorm_matches_oracle(prox, d):
+    """x_next = bf16(RMSNorm(x + y)): the fp32 kernel and the fp64 oracle
+    round to the same bf16 except where the exact value sits next to a
+    rounding midpoint, where they may differ by one ulp."""
+    x = _x(d, max(1, d // 100), seed=d)
+    y = torch.randn(d, generator=torch.Generator().manual_seed(d + 1)) * 9.0
+    out = prox.prox_residual_rmsnorm(x.cuda(), y.cuda())
+    torch.cuda.synchronize()
+    got = host_bits(out)
+    ref = oracle.residual_rmsnorm(host_bits(x), y.double().numpy())
+    ulps = _bf16_ulp_diff(got, ref)
+    assert ulps.max() <= 1.0
+    assert np.count_nonzero(got != ref) <= max(2, d // 500)
+    # eps dominates an all-zero residual: the output is exactly zero
+    z = prox.prox_residual_rmsnorm(torch.zeros(d, dtype=torch.bfloat16, device="cuda"),
+                                   torch.zeros(d, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(z) == 0
+
+
+def test_short_stack_matches_oracle_layer_by_layer(prox):
+    """Four stacked layers, x_{l+1} = RMSNorm(x_l + y_l) on the GPU: every
+    layer's step is checked against the oracle on the GPU's own x_l (so a
+    tie-band mask difference in one layer does not propagate into the next
+    comparison), and each glue step against the oracle's glue."""
+    d, F = 1024, 2816
+    x = _x(d, 10, seed=70).cuda()
+    for l in range(4):
+        L, w = _layer(prox, d, F, seed=1000 + l)
+        r = _check_step(prox, L, w, x.cpu(), 0.3)
+        y = prox.prox_ffn(L, x, 0.3)
+        torch.cuda.synchronize()
+        x_next = prox.prox_residual_rmsnorm(x, y)
+        torch.cuda.synchronize()
+        ref = oracle.residual_rmsnorm(host_bits(x), y.cpu().double().numpy())
+        assert _bf16_ulp_diff(host_bits(x_next), ref).max() <= 1.0
+        assert torch.allclose(y, r["y"], rtol=0, atol=1e-5 * float(y.abs().max()))
+        x = x_next
