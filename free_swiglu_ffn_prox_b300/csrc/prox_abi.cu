@@ -14,14 +14,14 @@ namespace prox {
 static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t workspace_bytes(int d, int F) {
-    const int Fp = padded_ff(F);
+    const size_t Fp = (size_t)padded_ff(F);
     return align256(256) + align256((size_t)kHistWords * 4) +
-           align256((size_t)kMaxSlices * Fp * 8) + align256((size_t)Fp * 4) +
-           align256((size_t)d * 2) + align256((size_t)d * 4);
+           align256((size_t)kMaxSlices * Fp * 8) + 3 * align256((size_t)(kMaxGrid + 1) * 4) +
+           4 * align256(Fp * 4) + align256((size_t)d * 2) + align256((size_t)d * 4);
 }
 
 Workspace carve_workspace(void* base, int d, int F) {
-    const int Fp = padded_ff(F);
+    const size_t Fp = (size_t)padded_ff(F);
     uint8_t* p = static_cast<uint8_t*>(base);
     Workspace w;
     w.status = reinterpret_cast<int*>(p);
@@ -31,8 +31,19 @@ Workspace carve_workspace(void* base, int d, int F) {
     p += align256((size_t)kHistWords * 4);
     w.part = reinterpret_cast<float2*>(p);
     p += align256((size_t)kMaxSlices * Fp * 8);
-    w.scores = reinterpret_cast<float*>(p);
-    p += align256((size_t)Fp * 4);
+    int** counts[3] = {&w.selc, &w.upre, &w.selpre};
+    for (int** c : counts) {
+        *c = reinterpret_cast<int*>(p);
+        p += align256((size_t)(kMaxGrid + 1) * 4);
+    }
+    w.skey = reinterpret_cast<uint32_t*>(p);
+    p += align256(Fp * 4);
+    w.schan = reinterpret_cast<int*>(p);
+    p += align256(Fp * 4);
+    w.idx_list = reinterpret_cast<int*>(p);
+    p += align256(Fp * 4);
+    w.hch = reinterpret_cast<float*>(p);
+    p += align256(Fp * 4);
     w.x_stage = reinterpret_cast<uint16_t*>(p);
     p += align256((size_t)d * 2);
     w.y_stage = reinterpret_cast<float*>(p);
@@ -170,9 +181,10 @@ prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, const void* 
                                  static_cast<__nv_bfloat16*>(gateup),
                                  static_cast<__nv_bfloat16*>(down_t), s);
     if (e != cudaSuccess) return PROX_ERR_CUDA;
-    // one persistent CTA per SM; every CTA must hold its share of the
-    // channel list in shared memory
-    if ((d_ff + sms - 1) / sms > prox::fused_max_chan()) return PROX_ERR_UNSUPPORTED_SHAPE;
+    // one persistent CTA per SM; every CTA holds its chunk of the channels
+    // in shared memory
+    if (sms > prox::fused_max_blocks() || (d_ff + sms - 1) / sms > prox::fused_max_chunk())
+        return PROX_ERR_UNSUPPORTED_SHAPE;
     prox_layer* L = new (std::nothrow) prox_layer;
     if (!L) return PROX_ERR_INVALID_ARG;
     L->d_model = d_model;

@@ -1,7 +1,6 @@
 // prox_fused.cu -- the whole Prox decode step ("Prox: Training-Free FFN
 // Activation Sparsity via Approximate Intermediate-Channel Salience in
-// LLMs", Abstract) as ONE persistent kernel, one CTA per SM, phases
-// separated by bounded grid barriers:
+// LLMs", Abstract) as ONE persistent kernel, one CTA per SM:
 //
 //   P0  input sparsity: every CTA selects the k_x entries of largest |x|
 //       (ties -> lower index) itself from x (a few KB, L2 resident), so no
@@ -9,44 +8,57 @@
 //   P1  proxy GEMV (Stage 1): CTA (tile, slice) streams the int4 proxy rows
 //       of its slice of the kept inputs, restricted to its channel tile, with
 //       128-bit loads, and writes per-slice partial (g~, u~) sums.
-//   --- grid barrier
-//   P2  CTA i owns a chunk of channels: sums the slices in a fixed order
-//       (deterministic scores), forms |silu(g~) u~| and adds the channels to
-//       a global 11-bit histogram of the score bit patterns.
-//   --- grid barrier
-//   P3  every CTA finishes the exact top-k itself: the histogram gives the
-//       bin of the k-th score; two more digit passes over the candidates of
-//       that bin (all scores staged in shared memory) give the threshold and
-//       the number of ties to keep (lowest channels first).  A block scan
-//       places every selected channel in the ascending list; the CTA keeps
-//       positions [k i / n, k (i+1) / n).
-//   P4  Stage 2 on those channels (Eq. (1) of the PrunePath page restricted
-//       to the mask): gate|up rows and W_down^T rows arrive by bulk copies
-//       (TMA) into two shared-memory rings; 16 warps own 8-element slices of
-//       d_model, form partial dot products, reduce them across warps one
-//       batch behind (mbarrier-synchronised), compute h = silu(g) u in fp32
-//       and accumulate h * W_down^T into registers; one vector atomic per
-//       element adds the CTA's part of y at the end.
+//   --- grid barrier 1
+//   P2  CTA b owns the channel chunk [F b / n, F (b+1) / n): sums the slices
+//       in a fixed order (deterministic scores), forms |silu(g~) u~|, adds
+//       the chunk to a global histogram of the scores' top 11 bits and ranks
+//       the chunk's channels locally.
+//   P3  Stage 2 (Eq. (1) of the PrunePath page restricted to the mask) and
+//       the exact channel top-k run side by side:
+//       - the items of CTA b > 0 start with the top m channels of its own
+//         chunk, m = 0.9 x the chunk's expected share of the mask; these are
+//         in the mask with high probability, so their rows stream at once;
+//       - CTA 0 alone waits for every chunk (grid barrier 2), stages all
+//         scores in shared memory and finds the exact top-k (three radix
+//         digits, ties to the lower channel); it lists, in channel order,
+//         every selected channel that its owner will not confirm on its own
+//         and publishes the threshold and the list behind a flag;
+//       - the other CTAs' selector warp polls that flag, confirms or drops
+//         the speculative items (by the threshold) and appends the CTA's
+//         even share of the list to its items;
+//       - gate|up rows and W_down^T rows arrive by bulk copies (TMA) into two
+//         shared-memory rings; pass-A warps form h = silu(W_gate x) (W_up x)
+//         per item (one warp per row), pass-B warps own slices of d_model and
+//         accumulate h * W_down^T for the confirmed items; one vector atomic
+//         per element adds the CTA's part of y at the end.
+//       A speculative item that the exact mask drops costs bandwidth only:
+//       pass B skips it.
 //
-// The same Stage-2 code, over all channels, is the dense baseline
-// (k_dense).  Every wait is bounded: a wait that runs out records
-// PROX_ERR_TIMEOUT in the layer's status word, lets copies in flight land
-// and leaves the kernel.
+// The same Stage-2 code over all channels is the dense baseline (k_dense).
+// Every wait is bounded: a wait that runs out records PROX_ERR_TIMEOUT in
+// the layer's status word, lets copies in flight land and leaves the kernel.
 #include "prox_internal.cuh"
 
 namespace prox {
 namespace {
 
-constexpr int kNT = 576;                 // 18 warps
-constexpr int kConsumerWarps = 16;       // Stage-2 consumers
-constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kNT = 608;                  // 19 warps
+constexpr int kPassAWarps = 8;            // warps 0..7: gate|up dot products
+constexpr int kPassBWarp0 = 8;            // warps 8..15: y += h W_down^T
+constexpr int kPassBWarps = 8;
+constexpr int kPassB = 32 * kPassBWarps;
 constexpr int kGuProducerWarp = 16;
 constexpr int kDProducerWarp = 17;
+constexpr int kSelectorWarp = 18;
 constexpr int kMaxStages = 16;
-constexpr int kMaxChan = 512;            // Stage-2 channels per CTA
-constexpr int kRing = 8;                 // proxy rows in flight per thread (cp.async ring)
+constexpr int kMaxItems = 512;            // Stage-2 items per CTA
+constexpr int kMaxChunk = 256;            // channels per CTA chunk
+constexpr int kMaxBlocks = kMaxGrid;
+constexpr int kBarriers = 2;              // grid barriers per call
+constexpr int kRing = 8;                  // proxy rows in flight per thread (cp.async ring)
 static_assert((kRing & (kRing - 1)) == 0, "ring depth must be a power of two");
 constexpr int kHistBins = 2048;
+static_assert(kHistBins <= kHistWords, "histogram words");
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kPhaseStamps = 10;
 
@@ -55,17 +67,31 @@ __device__ __forceinline__ void stamp(uint64_t* ts, int i) {
     if (ts && threadIdx.x == 0) ts[(size_t)blockIdx.x * kPhaseStamps + i] = global_timer_ns();
 }
 
+// The same from whichever single thread calls it.
+__device__ __forceinline__ void stamp_here(uint64_t* ts, int i) {
+    if (ts) ts[(size_t)blockIdx.x * kPhaseStamps + i] = global_timer_ns();
+}
+
 struct Ctl {
     uint64_t gu_full[kMaxStages], gu_empty[kMaxStages];
     uint64_t d_full[kMaxStages], d_empty[kMaxStages];
+    uint64_t sel_bar;                // completes when the item list is final
+    uint64_t done_bar;               // every warp is through its Stage-2 role
+    uint64_t ld_bar;                 // bulk load of the proxy scales (P1)
+    uint64_t sel_ld;                 // bulk loads of the selection (CTA 0)
     int gu_last[kMaxStages], d_last[kMaxStages];
-    float h[kMaxChan];
+    float h[kMaxItems];              // h of each item
+    int item[kMaxItems];             // channel of each item
+    uint8_t conf[kMaxItems];         // item is in the mask (pass B adds it)
+    uint8_t hready[kMaxItems];       // h[i] written by pass A
+    float lsc[kMaxChunk];            // scores of this CTA's chunk
+    uint16_t lrank[kMaxChunk];       // rank of each chunk channel (score desc, channel asc)
+    int upre[kMaxBlocks + 1];        // prefix over chunks of the handed-out channel counts
     uint32_t warp_tot[kNT / 32 + 1];
     uint32_t sel[4];
-    uint64_t ld_bar[2];  // bulk loads of the proxy scales (P1) and the scores (P3)
     unsigned epoch;
     int abort;
-    int chan[kMaxChan];
+    int n_items;
 };
 
 constexpr size_t ctl_bytes() { return (sizeof(Ctl) + 127) / 128 * 128; }
@@ -86,16 +112,22 @@ struct FusedParams {
     int tiles, slices, tile_w;
     // workspace
     int* status;
-    unsigned* bar;
+    unsigned* bar;       // [0] barrier count, [1] call epoch, [2] result flag,
+                         // [3] T, [4] split, [5] list length (control block)
     unsigned* epoch;     // number of completed calls on this workspace
-    uint32_t* hist;      // [kHistBins]
+    uint32_t* hist;      // [kHistWords]: digit-1, digit-2, digit-3 histograms
     float2* part;        // [slices][Fp]
-    float* scores;       // [Fp]
+    uint32_t* skey;      // [Fp] per chunk at its first channel: its score bits, descending
+    int* schan;          // [Fp] ... the channels in that order (ties: lower channel first)
+    int* selc;           // [kMaxBlocks] per chunk: how many of its channels are selected
+    int* upre;           // [kMaxBlocks + 1] prefix of the per-chunk handed-out counts
+    int* selpre;         // [kMaxBlocks] debug: prefix of selc
+    int* idx_list;       // [Fp] debug: the selected channels, ascending
+    float* hch;          // [Fp] debug: h per channel
     // debug outputs (may be null)
     int32_t* kept_out;
     float* scores_out;
-    int32_t* idx_out;
-    float* h_out;
+    int debug;           // write idx_list and hch
     // stage-2 ring geometry
     int n_gu, n_d;
     long long limit_ns;
@@ -103,6 +135,20 @@ struct FusedParams {
     uint64_t* ts;        // [gridDim][kPhaseStamps] %globaltimer stamps, or null
 };
 
+// First channel of chunk b (F <= 32768 and b <= 256, so F b fits 32 bits;
+// a 64-bit division costs hundreds of instructions on the GPU).
+__host__ __device__ __forceinline__ int chunk_begin(int F, int b, int nb) {
+    return (int)((unsigned)F * (unsigned)b / (unsigned)nb);
+}
+
+// Speculative items of a chunk of nch channels: 0.9 x its expected share
+// k nch / F of the mask.
+__host__ __device__ __forceinline__ int spec_count(int k, int nch, int F) {
+    const unsigned m = 9u * (unsigned)k * (unsigned)nch / (10u * (unsigned)F);  // < 2^27
+    return (int)(m < (unsigned)nch ? m : (unsigned)nch);
+}
+
+// ----------------------------------------------------------------- helpers
 // ----------------------------------------------------------------- helpers
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;
@@ -311,11 +357,6 @@ __device__ __forceinline__ void topk_digits(const TopkPlan& pl, int n, int kpt, 
     nsel = gt + (ties_before < r ? min(eq, r - ties_before) : 0u);
 }
 
-// Bulk prefetch of global memory into L2 (no shared-memory destination).
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // fp16 bits of x * 2^shift for a bf16 x (exact whenever the result is a
 // normal fp16; the same rounding as ldexpf followed by __float2half_rn).
 __device__ __forceinline__ uint16_t scaled_fp16(uint16_t xb, int shift) {
@@ -408,11 +449,10 @@ __device__ __forceinline__ float dot8_bf16(const uint4 a, const uint4 b, float a
 struct Stage2Args {
     const __nv_bfloat16* gateup;
     const __nv_bfloat16* down_t;
-    const uint16_t* x;
     float* y;
-    float* h_out;   // [k], written at pos0 + i (may be null)
+    float* hch;     // [F] h per channel (debug, may be null)
     int* status;
-    int d, n_gu, n_d, pos0;
+    int d, F, n_gu, n_d;
     long long limit_ns;
     uint64_t* ts;   // [gridDim][kPhaseStamps] or null
 };
@@ -429,87 +469,117 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, long l
     return __all_sync(0xffffffffu, got);
 }
 
-// Stage 2 over the n channels ctl.chan[0..n).  Shared area `area`: x as bf16
-// (2 d bytes), then n_gu gate|up stages (4 d bytes each), then n_d W_down^T
-// stages (2 d bytes each).
-//   pass A: warp w < n_gu computes g_c, u_c for channels i = w, w + n_gu, ...
-//           over the whole gate|up row (warp-local reduction),
-//           h_c = silu(g_c) u_c;
-//   pass B: every consumer thread owns 8-element slices of d and adds
-//           h_c * W_down^T[c, slice] for all channels in order.
-// The W_down^T ring fills during pass A.
+// Waits (every lane polls) until the shared-memory flag is set.
+__device__ __forceinline__ bool warp_wait_flag(const uint8_t* flag, long long limit_ns, Ctl& ctl,
+                                               int* status) {
+    bool got = true;
+    uint64_t t0 = 0;
+    for (uint32_t it = 1; !*reinterpret_cast<const volatile uint8_t*>(flag); ++it) {
+        if ((it & 63u) == 0) {
+            if (*reinterpret_cast<volatile int*>(&ctl.abort)) {
+                got = false;
+                break;
+            }
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) t0 = now;
+            else if ((long long)(now - t0) > limit_ns) {
+                got = false;
+                ctl.abort = 1;
+                record_status(status, PROX_ERR_TIMEOUT);
+                break;
+            }
+        }
+    }
+    __threadfence_block();
+    return __all_sync(0xffffffffu, got);
+}
+
+// Stage-2 roles of warps 0..17 over the CTA's items ctl.item[0..n_items).
+// Items [0, m) are known when the roles start; the rest (ctl.n_items, their
+// channels and ctl.conf of every item) only once ctl.sel_bar completes.
+// Shared area: x as bf16 (2 d bytes), then n_gu gate|up stages (4 d bytes
+// each), then n_d W_down^T stages (2 d bytes each).
+//   GU producer (warp 16) / D producer (warp 17): lane 0 issues one bulk copy
+//       per item into the next stage of its ring;
+//   pass A (warp w < n_gu): the items i = w (mod n_gu), always in gate|up
+//       stage w, so one warp consumes each stage's uses in order (a parity
+//       wait is never taken two uses ahead): g, u over the whole row,
+//       h = silu(g) u, then ctl.hready[i];
+//   pass B (warps 8..15): every thread owns 8-element slices of d and, for
+//       each confirmed item in order, adds h * W_down^T[c, slice].
 template <int CPT>
-__device__ void stage2(const Stage2Args& a, Ctl& ctl, uint8_t* area, int n) {
+__device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = a.d, n_gu = a.n_gu, n_d = a.n_d;
     const size_t gu_bytes = (size_t)4 * d, d_bytes = (size_t)2 * d;
-    uint16_t* xs = reinterpret_cast<uint16_t*>(area);
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(area);
     uint8_t* gu_ring = area + (size_t)2 * d;
     uint8_t* d_ring = gu_ring + (size_t)n_gu * gu_bytes;
     const int nchunk = d / 8;  // 16-byte chunks per row
 
-    stamp(a.ts, 6);
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < n_gu; ++s) {
-            mbar_init(&ctl.gu_full[s], 1);
-            mbar_init(&ctl.gu_empty[s], 1);
-            ctl.gu_last[s] = -1;
-        }
-        for (int s = 0; s < n_d; ++s) {
-            mbar_init(&ctl.d_full[s], 1);
-            mbar_init(&ctl.d_empty[s], kConsumerWarps);
-            ctl.d_last[s] = -1;
-        }
-        fence_mbar_init();
-    }
-    __syncthreads();  // the producers start before the consumers fetch x
-
     if (warp == kGuProducerWarp || warp == kDProducerWarp) {
-        if (lane == 0) {
-            const bool gu = warp == kGuProducerWarp;
-            const int ns = gu ? n_gu : n_d;
-            const size_t sb = gu ? gu_bytes : d_bytes;
-            uint64_t* full = gu ? ctl.gu_full : ctl.d_full;
-            uint64_t* empty = gu ? ctl.gu_empty : ctl.d_empty;
-            int* last = gu ? ctl.gu_last : ctl.d_last;
-            uint8_t* base = gu ? gu_ring : d_ring;
-            const uint8_t* src = gu ? reinterpret_cast<const uint8_t*>(a.gateup)
-                                    : reinterpret_cast<const uint8_t*>(a.down_t);
-            const uint64_t pol = policy_evict_first();
-            for (int i = 0; i < n; ++i) {
-                const int s = i % ns;
-                if (i >= ns &&
-                    !mbar_wait_bounded(&empty[s], ((i / ns) - 1) & 1, a.limit_ns, &ctl.abort)) {
-                    ctl.abort = 1;
-                    record_status(a.status, PROX_ERR_TIMEOUT);
-                    break;
-                }
-                if (ctl.abort) break;
-                const int c = ctl.chan[i];
-                last[s] = i;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)sb);
-                bulk_g2s(base + (size_t)s * sb, src + (size_t)c * sb, (uint32_t)sb, &full[s], pol);
+        if (lane != 0) return;
+        const bool gu = warp == kGuProducerWarp;
+        const int ns = gu ? n_gu : n_d;
+        const size_t sb = gu ? gu_bytes : d_bytes;
+        uint64_t* full = gu ? ctl.gu_full : ctl.d_full;
+        uint64_t* empty = gu ? ctl.gu_empty : ctl.d_empty;
+        int* last = gu ? ctl.gu_last : ctl.d_last;
+        uint8_t* base = gu ? gu_ring : d_ring;
+        const uint8_t* src = gu ? reinterpret_cast<const uint8_t*>(a.gateup)
+                                : reinterpret_cast<const uint8_t*>(a.down_t);
+        const uint64_t pol = policy_evict_first();
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            if (mbar_wait_bounded(bar, parity, a.limit_ns, &ctl.abort)) return true;
+            if (!ctl.abort) {
+                ctl.abort = 1;
+                record_status(a.status, PROX_ERR_TIMEOUT);
             }
+            return false;
+        };
+        bool known = false;
+        for (int i = 0;; ++i) {
+            if (i >= m) {
+                if (!known) {
+                    if (!wait(&ctl.sel_bar, 0)) break;
+                    known = true;
+                }
+                if (i >= ctl.n_items) break;
+            }
+            const int s = i % ns;
+            if (i >= ns && !wait(&empty[s], ((i / ns) - 1) & 1)) break;
+            if (ctl.abort) break;
+            const int c = ctl.item[i];
+            if (c < 0 || c >= a.F) {  // never expected: the lists hold chunk channels
+                record_status(a.status, PROX_ERR_DEVICE_CHECK);
+                ctl.abort = 1;
+                break;
+            }
+            last[s] = i;
+            mbar_arrive_expect_tx(&full[s], (uint32_t)sb);
+            bulk_g2s(base + (size_t)s * sb, src + (size_t)c * sb, (uint32_t)sb, &full[s], pol);
         }
-    } else {
-        for (int i = threadIdx.x; i < nchunk; i += kConsumers)
-            reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
-        named_barrier_sync(1, kConsumers);
-        // ------------------------------------------------ pass A: h per channel
-        // Warp w < n_gu owns gate|up slot w and takes channels w, w + n_gu, ...
-        // Each slot's uses are consumed in order by one warp, so a parity wait
-        // can never be taken for a phase two uses ahead (which would pass at
-        // once and release the slot while its copy is still in flight).
-        bool ok = true;
-        for (int i = warp; warp < n_gu && i < n && ok; i += n_gu) {
-            const int s = warp;
-            ok = warp_wait(&ctl.gu_full[s], (i / n_gu) & 1, a.limit_ns, ctl, a.status);
-            if (!ok) break;
-            if (i == 0 && lane == 0 && a.ts)
-                a.ts[(size_t)blockIdx.x * kPhaseStamps + 7] = global_timer_ns();
+        return;
+    }
+
+    if (warp < kPassAWarps) {
+        // ------------------------------------------------ pass A: h per item
+        if (warp >= n_gu) return;
+        const uint4* xv = reinterpret_cast<const uint4*>(xs);
+        const int s = warp;
+        bool known = false;
+        for (int i = warp;; i += n_gu) {
+            if (i >= m) {
+                if (!known) {
+                    if (!warp_wait(&ctl.sel_bar, 0, a.limit_ns, ctl, a.status)) break;
+                    known = true;
+                }
+                if (i >= ctl.n_items) break;
+            }
+            if (!warp_wait(&ctl.gu_full[s], (i / n_gu) & 1, a.limit_ns, ctl, a.status)) break;
+            if (i == 0 && lane == 0) stamp_here(a.ts, 6);
             const uint4* gr = reinterpret_cast<const uint4*>(gu_ring + (size_t)s * gu_bytes);
             const uint4* ur = gr + nchunk;
-            const uint4* xv = reinterpret_cast<const uint4*>(xs);
             float g = 0.0f, u = 0.0f;
             for (int ch = lane; ch < nchunk; ch += 32) {
                 const uint4 xw = xv[ch];
@@ -525,148 +595,457 @@ __device__ void stage2(const Stage2Args& a, Ctl& ctl, uint8_t* area, int n) {
                 mbar_arrive(&ctl.gu_empty[s]);
                 const float h = g / (1.0f + expf(-g)) * u;  // silu(g) * u
                 ctl.h[i] = h;
-                if (a.h_out) a.h_out[a.pos0 + i] = h;
+                if (a.hch) a.hch[ctl.item[i]] = h;
+                __threadfence_block();
+                *reinterpret_cast<volatile uint8_t*>(&ctl.hready[i]) = 1;
             }
         }
-        named_barrier_sync(1, kConsumers);
-        // ------------------------------------------------ pass B: y += h W_down^T
-        const int t = threadIdx.x;
-        float yp[CPT][8];
-#pragma unroll
-        for (int q = 0; q < CPT; ++q)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) yp[q][e] = 0.0f;
-        ok = ok && !ctl.abort;
-        for (int i = 0; i < n && ok; ++i) {
-            const int s = i % n_d;
-            ok = warp_wait(&ctl.d_full[s], (i / n_d) & 1, a.limit_ns, ctl, a.status);
-            if (!ok) break;
-            const float hv = ctl.h[i];
-            const uint8_t* st = d_ring + (size_t)s * d_bytes;
-#pragma unroll
-            for (int q = 0; q < CPT; ++q) {
-                const int ch = t + q * kConsumers;
-                if (ch < nchunk) {
-                    const uint4 dw = *reinterpret_cast<const uint4*>(st + (size_t)ch * 16);
-                    const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        yp[q][2 * e] = fmaf(hv, __uint_as_float(dv[e] << 16), yp[q][2 * e]);
-                        yp[q][2 * e + 1] = fmaf(hv, __uint_as_float(dv[e] & 0xffff0000u), yp[q][2 * e + 1]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.d_empty[s]);
-        }
-        if (warp == 0 && lane == 0 && a.ts)
-            a.ts[(size_t)blockIdx.x * kPhaseStamps + 8] = global_timer_ns();
-        if (ok && !ctl.abort && n > 0) {
-#pragma unroll
-            for (int q = 0; q < CPT; ++q) {
-                const int ch = t + q * kConsumers;
-                if (ch < nchunk) {
-                    float* dst = a.y + (size_t)ch * 8;
-                    red_add_v4(dst, yp[q][0], yp[q][1], yp[q][2], yp[q][3]);
-                    red_add_v4(dst + 4, yp[q][4], yp[q][5], yp[q][6], yp[q][7]);
-                }
-            }
-        }
+        if (warp == 0 && lane == 0) stamp_here(a.ts, 7);
+        return;
     }
-    __syncthreads();
-    stamp(a.ts, 9);
-    if (ctl.abort && threadIdx.x == 0) {
-        // let the copies still in flight into this CTA's rings land before leaving
-        for (int s = 0; s < n_gu; ++s)
-            if (ctl.gu_last[s] >= 0)
-                mbar_wait_bounded(&ctl.gu_full[s], (ctl.gu_last[s] / n_gu) & 1, a.limit_ns, nullptr);
-        for (int s = 0; s < n_d; ++s)
-            if (ctl.d_last[s] >= 0)
-                mbar_wait_bounded(&ctl.d_full[s], (ctl.d_last[s] / n_d) & 1, a.limit_ns, nullptr);
+
+    // ---------------------------------------------------- pass B: y += h W_down^T
+    // Items [0, m) are the chunk's speculative items.  Until a warp sees the
+    // item list final it adds them tentatively (nearly all are in the mask);
+    // afterwards it skips the items the mask dropped, and at the end it takes
+    // out again the dropped items it had already added (their W_down^T rows
+    // read once more from global memory).  Each warp decides for itself, and
+    // only for its own slices of y.
+    const int t = threadIdx.x - kPassBWarp0 * 32;
+    float yp[CPT][8];
+#pragma unroll
+    for (int q = 0; q < CPT; ++q)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) yp[q][e] = 0.0f;
+    auto add_row = [&](const uint4* row, float hv, bool global) {
+#pragma unroll
+        for (int q = 0; q < CPT; ++q) {
+            const int ch = t + q * kPassB;
+            if (ch < nchunk) {
+                const uint4 dw = global ? __ldg(row + ch) : row[ch];
+                const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    yp[q][2 * e] = fmaf(hv, __uint_as_float(dv[e] << 16), yp[q][2 * e]);
+                    yp[q][2 * e + 1] =
+                        fmaf(hv, __uint_as_float(dv[e] & 0xffff0000u), yp[q][2 * e + 1]);
+                }
+            }
+        }
+    };
+    bool ok = true, known = false;
+    int n = m, first_known = 0;  // items [0, first_known) were added tentatively
+    for (int i = 0; ok; ++i) {
+        if (!known) {
+            if (i >= m) {
+                ok = warp_wait(&ctl.sel_bar, 0, a.limit_ns, ctl, a.status);
+                if (!ok) break;
+                known = true;
+            } else {
+                known = __shfl_sync(0xffffffffu, lane == 0 ? mbar_test_wait(&ctl.sel_bar, 0) : false, 0);
+            }
+            if (known) {
+                n = ctl.n_items;
+                first_known = i;
+            }
+        }
+        if (i >= n) break;
+        const int s = i % n_d;
+        ok = warp_wait(&ctl.d_full[s], (i / n_d) & 1, a.limit_ns, ctl, a.status);
+        if (!ok) break;
+        if (!known || ctl.conf[i]) {
+            ok = warp_wait_flag(&ctl.hready[i], a.limit_ns, ctl, a.status);
+            if (!ok) break;
+            add_row(reinterpret_cast<const uint4*>(d_ring + (size_t)s * d_bytes),
+                    *reinterpret_cast<const volatile float*>(&ctl.h[i]), false);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.d_empty[s]);
+    }
+    if (ok && known)
+        for (int i = 0; i < first_known; ++i)
+            if (!ctl.conf[i])
+                add_row(reinterpret_cast<const uint4*>(a.down_t + (size_t)ctl.item[i] * d),
+                        -ctl.h[i], true);
+    if (t == 0) stamp_here(a.ts, 8);
+    if (ok && !ctl.abort && n > 0) {
+#pragma unroll
+        for (int q = 0; q < CPT; ++q) {
+            const int ch = t + q * kPassB;
+            if (ch < nchunk) {
+                float* dst = a.y + (size_t)ch * 8;
+                red_add_v4(dst, yp[q][0], yp[q][1], yp[q][2], yp[q][3]);
+                red_add_v4(dst + 4, yp[q][4], yp[q][5], yp[q][6], yp[q][7]);
+            }
+        }
     }
 }
 
-// P3: every CTA finishes the exact top-k of the scores itself (threads
-// 0..NT-1; NT a multiple of 32, named barrier 1): the global digit-1
-// histogram and all scores arrive by bulk copy, three radix digits over each
-// thread's own candidates give the threshold, one block scan the positions;
-// the CTA keeps the channels at positions [p0, p1) in ctl.chan.  On a
-// timeout it raises ctl.abort (after letting the copy land).
-template <int NT>
-__device__ __forceinline__ void select_channels(const FusedParams& p, Ctl& ctl, uint8_t* area,
-                                                int b, int nb, int p0, int p1) {
-    const int tid = threadIdx.x, lane = tid & 31;
+// Initialises the Stage-2 ring barriers (thread 0; the caller synchronises).
+__device__ __forceinline__ void stage2_init(Ctl& ctl, int n_gu, int n_d) {
+    for (int s = 0; s < n_gu; ++s) {
+        mbar_init(&ctl.gu_full[s], 1);
+        mbar_init(&ctl.gu_empty[s], 1);
+        ctl.gu_last[s] = -1;
+    }
+    for (int s = 0; s < n_d; ++s) {
+        mbar_init(&ctl.d_full[s], 1);
+        mbar_init(&ctl.d_empty[s], kPassBWarps);
+        ctl.d_last[s] = -1;
+    }
+    mbar_init(&ctl.sel_bar, 1);
+    mbar_init(&ctl.done_bar, kNT / 32);
+}
+
+// End of the Stage-2 roles: every warp, once its lanes are through, arrives
+// on ctl.done_bar; thread 0 waits for all of them (the roles are warp-
+// specialised, so a block barrier is not used here), stamps the end and,
+// after an abort, lets the copies still in flight into the rings land
+// before the CTA leaves (bounded).
+__device__ __forceinline__ void stage2_join(const Stage2Args& a, Ctl& ctl) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl.done_bar);
+    if (threadIdx.x != 0) return;
+    mbar_wait_bounded(&ctl.done_bar, 0, a.limit_ns, nullptr);
+    stamp_here(a.ts, 9);
+    if (!ctl.abort) return;
+    for (int s = 0; s < a.n_gu; ++s)
+        if (ctl.gu_last[s] >= 0)
+            mbar_wait_bounded(&ctl.gu_full[s], (ctl.gu_last[s] / a.n_gu) & 1, a.limit_ns, nullptr);
+    for (int s = 0; s < a.n_d; ++s)
+        if (ctl.d_last[s] >= 0)
+            mbar_wait_bounded(&ctl.d_full[s], (ctl.d_last[s] / a.n_d) & 1, a.limit_ns, nullptr);
+}
+
+// Bulk prefetch of global memory into L2 (no shared-memory destination).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// ------------------------------------------------------------ the selection
+constexpr int kCandCap = 4096;  // digit-1 candidates kept in shared memory
+
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Block-wide digit select, called by every thread: threads t < NB/4 read
+// bins 4t..4t+3 with one 16-byte load (consecutive threads, consecutive
+// words: no bank conflict) and a suffix sum from the top bin finds the bin b
+// with sum(h[b+1..]) < krem <= sum(h[b..]); (b, krem - sum(h[b+1..])) go to
+// ctl.sel[0..1].  If the bins hold fewer than krem counts ctl.sel[0] stays
+// 0xffffffff.
+template <int NB>
+__device__ __forceinline__ void block_select(const uint32_t* h, uint32_t krem, Ctl& ctl) {
+    constexpr int NQ = NB / 4, NW = NQ / 32;
+    static_assert(NQ % 32 == 0 && NQ <= kNT, "bins");
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < NQ) v = reinterpret_cast<const uint4*>(h)[tid];
+    const uint32_t s = (v.x + v.y) + (v.z + v.w);
+    uint32_t suf = s;  // sum over this and the higher lanes of the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += t;
+    }
+    if (wid < NW && lane == 0) ctl.warp_tot[wid] = suf;
+    if (tid == 0) ctl.sel[0] = 0xffffffffu;
+    __syncthreads();
+    if (tid < NQ) {
+        uint32_t above = suf - s;
+        for (int w = wid + 1; w < NW; ++w) above += ctl.warp_tot[w];
+        if (above < krem && above + s >= krem) {
+            const uint32_t bj[4] = {v.x, v.y, v.z, v.w};
+            uint32_t a = above;
+            int j = 3;
+            while (j > 0 && a + bj[j] < krem) a += bj[j--];
+            ctl.sel[0] = (uint32_t)(4 * tid + j);
+            ctl.sel[1] = krem - a;
+        }
+    }
+    __syncthreads();
+}
+
+// Number of leading entries of the descending keys s[0..n) with pred true
+// (pred holds for a prefix).
+template <typename Pred>
+__device__ __forceinline__ int count_leading(const uint32_t* s, int n, Pred pred) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (pred(s[mid])) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Warp-wide exclusive prefix over per-chunk values v(t), t < nb (<= 256):
+// out[t] for t < nb, the total in out[nb].  Called by one whole warp.
+template <typename V>
+__device__ __forceinline__ void warp_chunk_scan(int nb, V v, int* out) {
+    const int lane = threadIdx.x & 31;
+    const int per = (nb + 31) >> 5, t0 = lane * per;
+    int run = 0;
+    for (int j = 0; j < per; ++j)
+        if (t0 + j < nb) run += v(t0 + j);
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    int base = incl - run;
+    for (int j = 0; j < per; ++j)
+        if (t0 + j < nb) {
+            out[t0 + j] = base;
+            base += v(t0 + j);
+        }
+    if (lane == 31) out[nb] = incl;
+    __syncwarp();
+}
+
+// Largest c in [0, n) with pre[c] <= q (pre non-decreasing, pre[0] = 0 <= q).
+__device__ __forceinline__ int chunk_of(const int* pre, int n, int q) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= q) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Speculative items of chunk c (the owner's rule).
+__device__ __forceinline__ int chunk_spec(const FusedParams& p, int c, int nb) {
+    return c == 0 ? 0 : spec_count(p.k, chunk_begin(p.F, c + 1, nb) - chunk_begin(p.F, c, nb), p.F);
+}
+
+// CTA 0, all threads: the exact channel top-k once every chunk is in (grid
+// barrier 2).  Every chunk has published its keys sorted descending (ties:
+// lower channel first), so the selected channels of a chunk are a prefix of
+// its sorted list, and so are its speculative items.  CTA 0 stages the
+// digit-1 histogram and all sorted keys in shared memory; the digit-1 bin
+// (bits 30..20 of the score bits) of the k-th key comes from the histogram;
+// a binary search per chunk finds that bin's candidates, which are gathered
+// and reduced to the exact k-th key T by two more digits (bits 19..9 and
+// 8..0); ties at T are kept in channel order.  Per chunk it publishes
+// selc = how many of its channels are selected and the prefix over chunks of
+// max(0, selc - its speculative count), then the result flag (epoch + 1).
+// Returns false on a timeout or a broken invariant.
+__device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, int nb,
+                               unsigned ep) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int F = p.F, Fp = p.Fp;
-    // area: global histogram copy [2048] | digit-2 histogram [2048] |
-    // digit-3 histogram [512] | scores [Fp]
-    uint32_t* h1 = reinterpret_cast<uint32_t*>(area);
+    uint32_t* h1 = reinterpret_cast<uint32_t*>(area + (size_t)2 * p.d);
     uint32_t* h2 = h1 + kHistBins;
     uint32_t* h3 = h2 + kHistBins;
-    float* sc = reinterpret_cast<float*>(h3 + 512);
-    if (tid == 0) {
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        const uint64_t pol = policy_evict_first();
-        mbar_arrive_expect_tx(&ctl.ld_bar[1], (uint32_t)(kHistBins * 4 + Fp * 4));
-        bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.ld_bar[1], pol);
-        bulk_g2s(sc, p.scores, (uint32_t)(Fp * 4), &ctl.ld_bar[1], pol);
+    uint32_t* sk = h3 + 512;                               // [Fp] sorted keys per chunk
+    int* clo = reinterpret_cast<int*>(sk + Fp);            // [kMaxBlocks] first candidate
+    int* ccn = clo + kMaxBlocks;                           // candidates
+    int* coff = ccn + kMaxBlocks;                          // [kMaxBlocks + 1]
+    int* cgt = coff + kMaxBlocks + 1;                      // keys above T
+    int* ceq = cgt + kMaxBlocks;                           // keys equal to T
+    int* epre = ceq + kMaxBlocks;                          // [kMaxBlocks + 1]
+    int* csel = epre + kMaxBlocks + 1;                     // selected
+    uint32_t* cand = reinterpret_cast<uint32_t*>(csel + kMaxBlocks);  // [kCandCap]
+    if (tid < 32) {
+        bool ok = true;
+        if (lane == 0) {
+            const unsigned target = (unsigned)nb * (kBarriers * ep + 2u);
+            uint64_t t0 = 0;
+            for (uint32_t it = 1;; ++it) {
+                if ((int)(ld_acquire_gpu(p.bar) - target) >= 0) break;
+                if ((it & 15u) == 0) {
+                    const uint64_t now = global_timer_ns();
+                    if (t0 == 0) t0 = now;
+                    else if ((long long)(now - t0) > p.limit_ns) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!ok) {
+                record_status(p.status, PROX_ERR_TIMEOUT);
+                ctl.abort = 1;
+            } else {
+                *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                const uint64_t pol = policy_evict_first();
+                mbar_arrive_expect_tx(&ctl.sel_ld, (uint32_t)(kHistBins * 4 + Fp * 4));
+                bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.sel_ld, pol);
+                bulk_g2s(sk, p.skey, (uint32_t)(Fp * 4), &ctl.sel_ld, pol);
+            }
+        }
+        __syncwarp();
     }
-    for (int i = tid; i < kHistBins + 512; i += NT) h2[i] = 0u;
-    if (!mbar_wait_bounded(&ctl.ld_bar[1], 0, p.limit_ns, &ctl.abort) && lane == 0) {
+    for (int i = tid; i < kHistBins + 512; i += kNT) h2[i] = 0u;
+    __syncthreads();
+    if (ctl.abort) return false;
+    if (!mbar_wait_bounded(&ctl.sel_ld, 0, p.limit_ns, &ctl.abort) && lane == 0) {
         ctl.abort = 1;
         record_status(p.status, PROX_ERR_TIMEOUT);
     }
-    named_barrier_sync(1, NT);
+    __syncthreads();
     if (ctl.abort) {
-        // let the copy land (bounded) before the shared memory is released
-        if (tid == 0) mbar_wait_bounded(&ctl.ld_bar[1], 0, p.limit_ns, nullptr);
+        if (tid == 0) mbar_wait_bounded(&ctl.sel_ld, 0, p.limit_ns, nullptr);  // let it land
+        return false;
+    }
+    auto broken = [&]() {
+        if (tid == 0) {
+            record_status(p.status, PROX_ERR_DEVICE_CHECK);
+            ctl.abort = 1;
+        }
+        return false;
+    };
+    // digit 1 from the histogram of every chunk
+    block_select<2048>(h1, (uint32_t)p.k, ctl);
+    if (ctl.sel[0] == 0xffffffffu) return broken();
+    const uint32_t b1 = ctl.sel[0], k1 = ctl.sel[1];
+    // per chunk: its digit-1 candidates are the sorted positions [lo, hi)
+    if (tid < nb) {
+        const int c0 = chunk_begin(F, tid, nb), n = chunk_begin(F, tid + 1, nb) - c0;
+        const int lo = count_leading(sk + c0, n, [&](uint32_t kk) { return (kk >> 20) > b1; });
+        const int hi = count_leading(sk + c0, n, [&](uint32_t kk) { return (kk >> 20) >= b1; });
+        clo[tid] = lo;
+        ccn[tid] = hi - lo;
+    }
+    __syncthreads();
+    if (wid == 0) warp_chunk_scan(nb, [&](int t) { return ccn[t]; }, coff);
+    __syncthreads();
+    const int n_c = coff[nb];
+    const bool compact = n_c <= kCandCap;
+    if (compact && tid < nb) {
+        const uint32_t* src = sk + chunk_begin(F, tid, nb) + clo[tid];
+        for (int i = 0; i < ccn[tid]; ++i) cand[coff[tid] + i] = src[i];
+    }
+    __syncthreads();
+    // the candidates (or, if there are too many, every key filtered on digit 1)
+    auto each_cand = [&](auto&& fn) {
+        if (compact) {
+            for (int i = tid; i < n_c; i += kNT) fn(cand[i]);
+        } else {
+            for (int i = tid; i < F; i += kNT) {
+                const uint32_t kk = sk[i];
+                if ((kk >> 20) == b1) fn(kk);
+            }
+        }
+    };
+    each_cand([&](uint32_t kk) { atomicAdd(&h2[(kk >> 9) & 2047u], 1u); });
+    __syncthreads();
+    block_select<2048>(h2, k1, ctl);
+    if (ctl.sel[0] == 0xffffffffu) return broken();
+    const uint32_t pre = (b1 << 11) | ctl.sel[0], k2 = ctl.sel[1];
+    each_cand([&](uint32_t kk) {
+        if ((kk >> 9) == pre) atomicAdd(&h3[kk & 511u], 1u);
+    });
+    __syncthreads();
+    block_select<512>(h3, k2, ctl);
+    if (ctl.sel[0] == 0xffffffffu) return broken();
+    const uint32_t T = (pre << 9) | ctl.sel[0];
+    const int r = (int)ctl.sel[1];  // keys equal to T to keep, lowest channels first
+    // per chunk: keys above and equal to T
+    if (tid < nb) {
+        const int c0 = chunk_begin(F, tid, nb), n = chunk_begin(F, tid + 1, nb) - c0;
+        const int gt = count_leading(sk + c0, n, [&](uint32_t kk) { return kk > T; });
+        const int ge = count_leading(sk + c0, n, [&](uint32_t kk) { return kk >= T; });
+        cgt[tid] = gt;
+        ceq[tid] = ge - gt;
+    }
+    __syncthreads();
+    if (wid == 0) {
+        warp_chunk_scan(nb, [&](int t) { return ceq[t]; }, epre);
+        for (int t = lane; t < nb; t += 32) {
+            const int sel = cgt[t] + min(max(r - epre[t], 0), ceq[t]);
+            csel[t] = sel;
+            p.selc[t] = sel;
+        }
+        __syncwarp();
+        warp_chunk_scan(nb, [&](int t) { return max(csel[t] - chunk_spec(p, t, nb), 0); }, p.upre);
+        if (p.debug) warp_chunk_scan(nb, [&](int t) { return csel[t]; }, p.selpre);
+    }
+    __syncthreads();  // the per-chunk results are out
+    if (tid == 0) {
+        st_release_gpu(p.bar + 2, ep + 1u);
+        stamp_here(p.ts, 5);
+    }
+    return true;
+}
+
+// The selector warp of every CTA: waits for CTA 0's result flag, confirms
+// its speculative items ctl.item[0..m) (those of rank < selc[b]; they are the
+// chunk's top m), appends its share [U b / n, U (b+1) / n) of the handed-out
+// channels (in chunk order, the selected channels of rank >= the chunk's
+// speculative count) and completes ctl.sel_bar.  With the debug outputs it
+// also writes the chunk's selected channels, ascending, into idx_list.
+__device__ void await_selection(const FusedParams& p, Ctl& ctl, int b, int nb, int cb0, int nch,
+                                int m, unsigned ep) {
+    const int lane = threadIdx.x & 31;
+    const unsigned below = (1u << lane) - 1u;
+    bool ok = true;
+    if (lane == 0) {
+        uint64_t t0 = 0;
+        for (uint32_t it = 1;; ++it) {
+            if (ld_acquire_gpu(p.bar + 2) == ep + 1u) break;
+            if ((it & 15u) == 0) {
+                if (*reinterpret_cast<volatile int*>(&ctl.abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint64_t now = global_timer_ns();
+                if (t0 == 0) t0 = now;
+                else if ((long long)(now - t0) > p.limit_ns) {
+                    ok = false;
+                    record_status(p.status, PROX_ERR_TIMEOUT);
+                    ctl.abort = 1;
+                    break;
+                }
+            }
+        }
+    }
+    __syncwarp();
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    for (int t = lane; t <= nb; t += 32) ctl.upre[t] = __ldcg(p.upre + t);
+    const int selb = __ldcg(p.selc + b);
+    __syncwarp();
+    for (int j = lane; j < m; j += 32) {
+        ctl.conf[j] = j < selb ? 1 : 0;
+        // a dropped speculative item may already be in y: pass B will read its
+        // W_down^T row again to take it out, so bring the row into L2 now
+        if (j >= selb)
+            prefetch_l2(p.down_t + (size_t)ctl.item[j] * p.d, (uint32_t)(2 * p.d));
+    }
+    const int U = ctl.upre[nb];
+    const int q0 = chunk_begin(U, b, nb), q1 = chunk_begin(U, b + 1, nb);
+    if (m + (q1 - q0) > kMaxItems) {
+        if (lane == 0) {
+            record_status(p.status, PROX_ERR_DEVICE_CHECK);
+            ctl.abort = 1;
+        }
         return;
     }
-    // exact top-k of the score bit patterns: digits of 11, 11 and 9 bits;
-    // thread t owns the channels [t kpf, (t+1) kpf)
-    const int kpf = (F + NT - 1) / NT;  // <= 64
-    const int ci0 = tid * kpf;
-    auto skey = [&](int i) { return __float_as_uint(sc[i]); };
-    uint32_t T, r, cpos, cties, cn;
-    {
-        const TopkPlan pls{20, 2048, 9, 2048, 512};
-        topk_digits<NT>(pls, F, kpf, (uint32_t)p.k, skey, h1, h2, h3, ctl, T, r, cpos, cties, cn);
+    for (int q = q0 + lane; q < q1; q += 32) {
+        const int c = chunk_of(ctl.upre, nb, q);
+        ctl.item[m + q - q0] =
+            __ldcg(p.schan + chunk_begin(p.F, c, nb) + chunk_spec(p, c, nb) + (q - ctl.upre[c]));
+        ctl.conf[m + q - q0] = 1;
     }
-    // only the threads whose positions [cpos, cpos + cn) meet [p0, p1) emit
-    if (cn && (int)(cpos + cn) > p0 && (int)cpos < p1) {
-        uint32_t pos = cpos, tie = cties;
-        for (int e = 0; e < kpf; ++e) {
-            const int c = ci0 + e;
-            if (c < F) {
-                const uint32_t kk = skey(c);
-                bool keep = kk > T;
-                if (kk == T) {
-                    keep = tie < r;
-                    ++tie;
-                }
-                if (keep) {
-                    if ((int)pos >= p0 && (int)pos < p1) ctl.chan[pos - p0] = c;
-                    ++pos;
-                }
-            }
+    if (p.debug) {
+        int pos = __ldcg(p.selpre + b);
+        for (int i0 = 0; i0 < nch; i0 += 32) {
+            const int i = i0 + lane;
+            const bool sel = i < nch && (int)ctl.lrank[i] < selb;
+            const unsigned bs = __ballot_sync(0xffffffffu, sel);
+            if (sel) p.idx_list[pos + __popc(bs & below)] = cb0 + i;
+            pos += __popc(bs);
         }
     }
-    // the debug channel list: every selected channel, by its owner thread
-    if (p.idx_out && b == 0 && cn) {
-        uint32_t pos = cpos, tie = cties;
-        for (int e = 0; e < kpf; ++e) {
-            const int c = ci0 + e;
-            if (c < F) {
-                const uint32_t kk = skey(c);
-                bool keep = kk > T;
-                if (kk == T) {
-                    keep = tie < r;
-                    ++tie;
-                }
-                if (keep) p.idx_out[pos++] = c;
-            }
-        }
+    if (lane == 0) {
+        ctl.n_items = m + (q1 - q0);
+        stamp_here(p.ts, 5);
     }
-    (void)nb;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.sel_bar);
 }
 
 // ------------------------------------------------------------ fused kernel
@@ -682,8 +1061,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     if (tid == 0) {
         ctl.abort = 0;
         ctl.epoch = *reinterpret_cast<volatile unsigned*>(p.epoch);
-        mbar_init(&ctl.ld_bar[0], 1);
-        mbar_init(&ctl.ld_bar[1], 1);
+        mbar_init(&ctl.ld_bar, 1);
         fence_mbar_init();
     }
 
@@ -698,7 +1076,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     for (int i = tid; i < 384; i += kNT) hA[i] = 0u;
     if (b == 0) {
         for (int i = tid; i < d; i += kNT) p.y[i] = 0.0f;
-        for (int i = tid; i < kHistBins; i += kNT) p.hist[i] = 0u;
+        for (int i = tid; i < kHistWords; i += kNT) p.hist[i] = 0u;
     }
     __syncthreads();
     // exact top-k_x of |x| (15-bit keys): digit 1 = exponent (bits 14..7),
@@ -770,8 +1148,8 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         const int R = kNT / tpr;
         const int rl = tid / tpr, cu = tid % tpr;
         const bool active = rl < R && cu * 16 < width;
-        const int r0 = (int)((long long)slice * p.kx / p.slices);
-        const int r1 = (int)((long long)(slice + 1) * p.kx / p.slices);
+        const int r0 = chunk_begin(p.kx, slice, p.slices);  // kx <= 16384, slices <= 16
+        const int r1 = chunk_begin(p.kx, slice + 1, p.slices);
         // row-lane rl takes the contiguous kept rows [q_beg, q_end)
         const int m = (r1 - r0 + R - 1) / R;
         const int q_beg = min(r1, r0 + rl * m), q_end = min(r1, q_beg + m);
@@ -793,10 +1171,10 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         const bool smem_scales = ng > 0 && (size_t)ng * W * 4 <= room;
         if (tid == 0 && smem_scales) {
             const uint64_t pol = policy_evict_first();
-            mbar_arrive_expect_tx(&ctl.ld_bar[0], (uint32_t)(ng * width * 4));
+            mbar_arrive_expect_tx(&ctl.ld_bar, (uint32_t)(ng * width * 4));
             for (int g = 0; g < ng; ++g)
                 bulk_g2s(ssc + (size_t)g * W, p.scales + (size_t)(g_lo + g) * Fp + c0,
-                         (uint32_t)(width * 4), &ctl.ld_bar[0], pol);
+                         (uint32_t)(width * 4), &ctl.ld_bar, pol);
         }
         if (active)
             for (int t = 0; t < 16; ++t) tot[((size_t)rl * 16 + t) * tpr + cu] = make_float2(0.0f, 0.0f);
@@ -810,7 +1188,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
             const uint4* src;
             if (smem_scales) {
                 if (!scales_in) {
-                    if (!mbar_wait_bounded(&ctl.ld_bar[0], 0, p.limit_ns, &ctl.abort)) {
+                    if (!mbar_wait_bounded(&ctl.ld_bar, 0, p.limit_ns, &ctl.abort)) {
                         ctl.abort = 1;
                         record_status(p.status, PROX_ERR_TIMEOUT);
                     }
@@ -882,7 +1260,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         }
         // the scale copy must have landed before this shared memory is reused
         if (smem_scales && !scales_in)
-            if (!mbar_wait_bounded(&ctl.ld_bar[0], 0, p.limit_ns, &ctl.abort)) {
+            if (!mbar_wait_bounded(&ctl.ld_bar, 0, p.limit_ns, &ctl.abort)) {
                 ctl.abort = 1;
                 record_status(p.status, PROX_ERR_TIMEOUT);
             }
@@ -906,142 +1284,145 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     }
     stamp(p.ts, 2);
     const unsigned ep = ctl.epoch;
-    if (!grid_barrier(p.bar, (unsigned)nb * (2u * ep + 1u), p.status, p.limit_ns, ctl,
+    if (!grid_barrier(p.bar, (unsigned)nb * (kBarriers * ep + 1u), p.status, p.limit_ns, ctl,
                       p.inject == 1 && b == nb - 1))
         return;
     stamp(p.ts, 3);
 
     // ------------------------------------------------ P2: scores + histogram
-    const int cb0 = (int)((long long)F * b / nb), cb1 = (int)((long long)F * (b + 1) / nb);
-    float* lsc = ctl.h;  // this chunk's scores (ctl.h is Stage 2's, free until then)
+    const int cb0 = chunk_begin(F, b, nb), cb1 = chunk_begin(F, b + 1, nb);
+    const int nch = cb1 - cb0;  // <= kMaxChunk (checked by the host)
+    const int m = b == 0 ? 0 : spec_count(p.k, nch, F);  // CTA 0 selects instead
     {
-        for (int c00 = cb0; c00 < cb1; c00 += kNT) {
-            const int c = c00 + tid;
-            const bool act = c < cb1;
-            uint32_t key = 0;
-            if (act) {
-                float2 v[kMaxSlices];
+        const bool act = tid < nch;
+        uint32_t key = 0;
+        if (act) {
+            const int c = cb0 + tid;
+            float2 v[kMaxSlices];
 #pragma unroll
-                for (int sl = 0; sl < kMaxSlices; ++sl)
-                    if (sl < p.slices) v[sl] = __ldcg(p.part + (size_t)sl * Fp + c);
-                float g = 0.0f, u = 0.0f;
+            for (int sl = 0; sl < kMaxSlices; ++sl)
+                if (sl < p.slices) v[sl] = __ldcg(p.part + (size_t)sl * Fp + c);
+            float g = 0.0f, u = 0.0f;
 #pragma unroll
-                for (int sl = 0; sl < kMaxSlices; ++sl)
-                    if (sl < p.slices) {
-                        g += v[sl].x;
-                        u += v[sl].y;
-                    }
-                // |silu(g~) * u~|, silu(z) = z / (1 + e^-z)
-                const float sc = fabsf(g / (1.0f + expf(-g)) * u);
-                p.scores[c] = sc;
-                if (p.scores_out) p.scores_out[c] = sc;
-                lsc[c - cb0] = sc;
-                key = __float_as_uint(sc);
-            }
-            // one reduction per distinct bin in the warp
-            const unsigned am = __ballot_sync(0xffffffffu, act);
-            if (act) {
-                const unsigned peers = __match_any_sync(am, key >> 20);
-                if (lane == __ffs(peers) - 1)
-                    asm volatile("red.global.add.u32 [%0], %1;" ::"l"(p.hist + (key >> 20)),
-                                 "r"((uint32_t)__popc(peers))
-                                 : "memory");
-            }
+            for (int sl = 0; sl < kMaxSlices; ++sl)
+                if (sl < p.slices) {
+                    g += v[sl].x;
+                    u += v[sl].y;
+                }
+            // |silu(g~) * u~|, silu(z) = z / (1 + e^-z)
+            const float sc = fabsf(g / (1.0f + expf(-g)) * u);
+            if (p.scores_out) p.scores_out[c] = sc;
+            ctl.lsc[tid] = sc;
+            key = __float_as_uint(sc);
+        }
+        // one reduction per distinct bin in the warp
+        const unsigned am = __ballot_sync(0xffffffffu, act);
+        if (act) {
+            const unsigned peers = __match_any_sync(am, key >> 20);
+            if (lane == __ffs(peers) - 1)
+                asm volatile("red.global.add.u32 [%0], %1;" ::"l"(p.hist + (key >> 20)),
+                             "r"((uint32_t)__popc(peers))
+                             : "memory");
         }
     }
-    stamp(p.ts, 4);
-    // Grid barrier 2, then the channel selection (P3) on warps 0..15 while
-    // warp 17 prefetches: the channels ranked in the top 90% of this chunk's
-    // expected share of the mask are almost surely selected, and their
-    // Stage-2 rows (gate|up, W_down^T) are prefetched into L2 so that HBM
-    // streams during the selection.  A wrong guess costs bandwidth only.  The
-    // prefetch warp stays off the selection's barriers (bulk prefetches can
-    // stall their issuing thread while the copy engine's queue is full).
-    constexpr int kSel = 512;  // threads of warps 0..15
-    const int p0 = (int)((long long)p.k * b / nb), p1 = (int)((long long)p.k * (b + 1) / nb);
-    const int n_mine = p1 - p0;
+    for (int i = tid; i < kMaxItems; i += kNT) {
+        ctl.conf[i] = 0;
+        ctl.hready[i] = 0;
+    }
+    if (tid == 0) {
+        stage2_init(ctl, p.n_gu, p.n_d);
+        mbar_init(&ctl.sel_ld, 1);
+        fence_mbar_init();
+    }
     __syncthreads();
-    if (tid == 0) red_add_release_gpu(p.bar, 1u);
-    if (wid == kNT / 32 - 1) {
-        const int nch = cb1 - cb0;
-        const int m = (int)(0.9 * (double)p.k * nch / F);
-        for (int i = lane; i < nch; i += 32) {
-            const float mine = lsc[i];
-            int rank = 0;
-            for (int j = 0; j < nch; ++j) {
-                const float o = lsc[j];
+    // local rank of each chunk channel (key descending, channel ascending: a
+    // total order, so the ranks are a permutation), RT threads per channel
+    // (consecutive lanes) each comparing a strided part of the chunk.  The
+    // chunk goes out sorted (keys and channels at its first channel); the
+    // top m are the speculative items, most likely first.
+    {
+        int RT = 8;
+        while (RT > 1 && RT * nch > kNT) RT >>= 1;
+        const int i = tid / RT, part = tid % RT;
+        const uint32_t mine = i < nch ? __float_as_uint(ctl.lsc[i]) : 0u;
+        int rank = 0;
+        if (i < nch)
+            for (int j = part; j < nch; j += RT) {
+                const uint32_t o = __float_as_uint(ctl.lsc[j]);
                 rank += (o > mine) || (o == mine && j < i);
             }
-            if (rank < m) {
-                const int c = cb0 + i;
-                prefetch_l2(p.gateup + (size_t)c * 2 * d, (uint32_t)(4 * d));
-                prefetch_l2(p.down_t + (size_t)c * d, (uint32_t)(2 * d));
-            }
-        }
-    } else if (tid < kSel) {
-        if (tid == 0) {
-            const unsigned target = (unsigned)nb * (2u * ep + 2u);
-            bool ok = true;
-            uint64_t t0 = 0;
-            for (uint32_t it = 1;; ++it) {
-                if ((int)(ld_acquire_gpu(p.bar) - target) >= 0) break;
-                if ((it & 15u) == 0) {
-                    const uint64_t now = global_timer_ns();
-                    if (t0 == 0) t0 = now;
-                    else if ((long long)(now - t0) > p.limit_ns) {
-                        ok = false;
-                        break;
-                    }
-                }
-            }
-            if (!ok) {
-                record_status(p.status, PROX_ERR_TIMEOUT);
-                ctl.abort = 1;
-            } else if (b == 0) {
-                *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;
-            }
-        }
-        named_barrier_sync(1, kSel);
-        if (!ctl.abort) {
-            stamp(p.ts, 5);
-            select_channels<kSel>(p, ctl, area, b, nb, p0, p1);
+        for (int o = RT >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        if (i < nch && part == 0) {
+            ctl.lrank[i] = (uint16_t)rank;
+            p.skey[cb0 + rank] = mine;
+            p.schan[cb0 + rank] = cb0 + i;
+            if (rank < m) ctl.item[rank] = cb0 + i;
         }
     }
-    __syncthreads();  // channel list ready, prefetches issued
-    if (ctl.abort) return;
+    __syncthreads();
+    if (tid == 0) red_add_release_gpu(p.bar, 1u);  // barrier 2: histogram and sorted chunk out
+    stamp(p.ts, 4);
 
-    // ------------------------------------------------ P4: stage 2
+    // ------------------------------------------------ P3: selection + stage 2
+    if (b == 0) central_select(p, ctl, area, nb, ep);
     Stage2Args a;
     a.gateup = p.gateup;
     a.down_t = p.down_t;
-    a.x = p.x;
     a.y = p.y;
-    a.h_out = p.h_out;
+    a.hch = p.debug ? p.hch : nullptr;
     a.status = p.status;
     a.d = d;
+    a.F = F;
     a.n_gu = p.n_gu;
     a.n_d = p.n_d;
-    a.pos0 = (int)((long long)p.k * b / nb);
     a.limit_ns = p.limit_ns;
     a.ts = p.ts;
-    stage2<CPT>(a, ctl, area, n_mine);
+    if (wid == kSelectorWarp) {
+        if (!ctl.abort) await_selection(p, ctl, b, nb, cb0, nch, m, ep);
+    } else {
+        stage2_roles<CPT>(a, ctl, area, m);
+    }
+    stage2_join(a, ctl);
 }
 
-// Dense baseline: Stage 2 over every channel, CTA i taking [F i/n, F (i+1)/n).
+// Dense baseline: Stage 2 over every channel, CTA i taking [F i/n, F (i+1)/n)
+// (all items known and confirmed from the start).
 template <int CPT>
-__global__ void __launch_bounds__(kNT, 1) k_dense(const Stage2Args a0, int F) {
+__global__ void __launch_bounds__(kNT, 1) k_dense(const Stage2Args a, const uint16_t* x) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
     uint8_t* area = smem_raw + ctl_bytes();
-    if (threadIdx.x == 0) ctl.abort = 0;
-    const int c0 = (int)((long long)F * blockIdx.x / gridDim.x);
-    const int c1 = (int)((long long)F * (blockIdx.x + 1) / gridDim.x);
-    for (int i = threadIdx.x; i < c1 - c0; i += kNT) ctl.chan[i] = c0 + i;
-    __syncthreads();
-    Stage2Args a = a0;
-    a.pos0 = c0;
+    const int tid = threadIdx.x;
     stamp(a.ts, 0);
-    stage2<CPT>(a, ctl, area, c1 - c0);
+    const int c0 = chunk_begin(a.F, blockIdx.x, gridDim.x);
+    const int n = chunk_begin(a.F, blockIdx.x + 1, gridDim.x) - c0;  // <= kMaxChunk
+    for (int i = tid; i < a.d / 8; i += kNT)
+        reinterpret_cast<uint4*>(area)[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
+    for (int i = tid; i < kMaxItems; i += kNT) {
+        ctl.item[i] = c0 + i;
+        ctl.conf[i] = i < n ? 1 : 0;
+        ctl.hready[i] = 0;
+    }
+    if (tid == 0) {
+        ctl.abort = 0;
+        ctl.n_items = n;
+        stage2_init(ctl, a.n_gu, a.n_d);
+        mbar_arrive(&ctl.sel_bar);  // the item list is final at once
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if ((tid >> 5) != kSelectorWarp) stage2_roles<CPT>(a, ctl, area, n);
+    stage2_join(a, ctl);
+}
+
+// Debug: the channel list and h in list order from the per-channel arrays.
+__global__ void k_gather_h(const int* idx_list, const float* hch, int k, int32_t* idx_out,
+                           float* h_out) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < k; i += gridDim.x * blockDim.x) {
+        const int c = idx_list[i];
+        if (idx_out) idx_out[i] = c;
+        if (h_out) h_out[i] = hch[c];
+    }
 }
 
 // ------------------------------------------------------------ host side
@@ -1051,23 +1432,19 @@ struct Ring {
 
 size_t area_budget() { return kSmemLimit - ctl_bytes(); }
 
-// Stage-2 rings: x (2 d bytes) plus as many gate|up (4 d) and W_down^T
-// (2 d) stages as fit, about 60% of the ring bytes for gate|up.
+// Stage-2 rings after x (2 d bytes): up to kPassAWarps gate|up stages (4 d
+// each, at most two thirds of the room) and as many W_down^T stages (2 d)
+// as fit in the rest.
 Ring ring_for(int d) {
     const size_t budget = area_budget() - (size_t)2 * d;
     const size_t gu = (size_t)4 * d, dd = (size_t)2 * d;
     Ring r{0, 0};
-    int best = -1;
-    for (int ng = 1; ng <= kMaxStages; ++ng)
-        for (int nd = 1; nd <= kMaxStages; ++nd) {
-            if ((size_t)ng * gu + (size_t)nd * dd > budget) continue;
-            const int bytes = ng * 4 + nd * 2;   // in units of d bytes
-            const int score = 4 * bytes - abs(ng * 4 - 3 * nd * 2);  // prefer full, balanced
-            if (score > best) {
-                best = score;
-                r = {ng, nd};
-            }
-        }
+    r.n_gu = (int)((budget * 2 / 3) / gu);
+    if (r.n_gu > kPassAWarps) r.n_gu = kPassAWarps;
+    if (r.n_gu < 1) r.n_gu = 1;
+    const size_t left = budget > (size_t)r.n_gu * gu ? budget - (size_t)r.n_gu * gu : 0;
+    r.n_d = (int)(left / dd);
+    if (r.n_d > kMaxStages) r.n_d = kMaxStages;
     return r;
 }
 
@@ -1107,12 +1484,15 @@ ProxyGeom proxy_geometry(int F, int kx, int num_blocks) {
 }
 
 cudaError_t fused_configure() {
-    cudaError_t e = set_smem(k_prox_fused<1>);
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = set_smem(k_prox_fused<1>);
     if (e == cudaSuccess) e = set_smem(k_prox_fused<2>);
     if (e == cudaSuccess) e = set_smem(k_prox_fused<4>);
+    if (e == cudaSuccess) e = set_smem(k_prox_fused<8>);
     if (e == cudaSuccess) e = set_smem(k_dense<1>);
     if (e == cudaSuccess) e = set_smem(k_dense<2>);
     if (e == cudaSuccess) e = set_smem(k_dense<4>);
+    if (e == cudaSuccess) e = set_smem(k_dense<8>);
     return e;
 }
 
@@ -1120,19 +1500,29 @@ size_t fused_smem_bytes() { return kSmemLimit; }
 
 int fused_threads() { return kNT; }
 
-int fused_max_chan() { return kMaxChan; }
+int fused_max_chunk() { return kMaxChunk; }
+
+int fused_max_blocks() { return kMaxBlocks; }
 
 bool fused_fits(int d, int F) {
     // P0: x (2 d) + kept list (4 d) + histogram; P1 adds the [R][W] partial
-    // table (at most 8 * 16 * kNT bytes); P3: histogram + F scores; P4: rings.
+    // table (at most 8 * 16 * kNT bytes) and the cp.async ring; P3: rings.
+    (void)F;
     const size_t p01 = (size_t)6 * d + 4096 + (size_t)8 * 16 * kNT + (size_t)16 * kRing * kNT;
-    const size_t p3 = (size_t)(2 * kHistBins + 512) * 4 + (size_t)4 * padded_ff(F);
     const Ring r = ring_for(d);
-    return p01 <= area_budget() && p3 <= area_budget() && ring_bytes(d, r) <= area_budget() &&
-           r.n_gu >= 1 && r.n_d >= 1;
+    return p01 <= area_budget() && ring_bytes(d, r) <= area_budget() && r.n_gu >= 1 &&
+           r.n_d >= 1;
 }
 
+namespace {
+template <int CPT>
+cudaError_t launch_fused_t(const cudaLaunchConfig_t& cfg, const FusedParams& p) {
+    return cudaLaunchKernelEx(&cfg, k_prox_fused<CPT>, p);
+}
+}  // namespace
+
 cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
+    if (L.num_blocks < 1 || L.num_blocks > kMaxBlocks) return cudaErrorInvalidValue;
     FusedParams p;
     p.codes = L.codes;
     p.scales = L.scales;
@@ -1154,11 +1544,16 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     p.epoch = L.ws->bar + 1;
     p.hist = L.ws->hist;
     p.part = L.ws->part;
-    p.scores = L.ws->scores;
+    p.skey = L.ws->skey;
+    p.schan = L.ws->schan;
+    p.selc = L.ws->selc;
+    p.upre = L.ws->upre;
+    p.selpre = L.ws->selpre;
+    p.idx_list = L.ws->idx_list;
+    p.hch = L.ws->hch;
     p.kept_out = L.kept_out;
     p.scores_out = L.scores_out;
-    p.idx_out = L.idx_out;
-    p.h_out = L.h_out;
+    p.debug = (L.idx_out || L.h_out) ? 1 : 0;
     const Ring r = ring_for(L.d);
     p.n_gu = r.n_gu;
     p.n_d = r.n_d;
@@ -1176,32 +1571,41 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const int nchunk = L.d / 8;
-    if (nchunk <= kConsumers) return cudaLaunchKernelEx(&cfg, k_prox_fused<1>, p);
-    if (nchunk <= 2 * kConsumers) return cudaLaunchKernelEx(&cfg, k_prox_fused<2>, p);
-    return cudaLaunchKernelEx(&cfg, k_prox_fused<4>, p);
+    cudaError_t e;
+    if (nchunk <= kPassB) e = launch_fused_t<1>(cfg, p);
+    else if (nchunk <= 2 * kPassB) e = launch_fused_t<2>(cfg, p);
+    else if (nchunk <= 4 * kPassB) e = launch_fused_t<4>(cfg, p);
+    else e = launch_fused_t<8>(cfg, p);
+    if (e == cudaSuccess && p.debug) {
+        k_gather_h<<<(L.k + 255) / 256, 256, 0, stream>>>(L.ws->idx_list, L.ws->hch, L.k,
+                                                         L.idx_out, L.h_out);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 cudaError_t launch_dense(const __nv_bfloat16* gateup, const __nv_bfloat16* down_t,
                          const uint16_t* x, int d, int F, float* y, int* status, int num_blocks,
                          long long limit_ns, uint64_t* ts, cudaStream_t stream) {
+    if (num_blocks < 1 || num_blocks > kMaxBlocks) return cudaErrorInvalidValue;
     Stage2Args a;
     a.gateup = gateup;
     a.down_t = down_t;
-    a.x = x;
     a.y = y;
-    a.h_out = nullptr;
+    a.hch = nullptr;
     a.status = status;
     a.d = d;
+    a.F = F;
     const Ring r = ring_for(d);
     a.n_gu = r.n_gu;
     a.n_d = r.n_d;
-    a.pos0 = 0;
     a.limit_ns = limit_ns;
     a.ts = ts;
     const int nchunk = d / 8;
-    if (nchunk <= kConsumers) k_dense<1><<<num_blocks, kNT, kSmemLimit, stream>>>(a, F);
-    else if (nchunk <= 2 * kConsumers) k_dense<2><<<num_blocks, kNT, kSmemLimit, stream>>>(a, F);
-    else k_dense<4><<<num_blocks, kNT, kSmemLimit, stream>>>(a, F);
+    if (nchunk <= kPassB) k_dense<1><<<num_blocks, kNT, kSmemLimit, stream>>>(a, x);
+    else if (nchunk <= 2 * kPassB) k_dense<2><<<num_blocks, kNT, kSmemLimit, stream>>>(a, x);
+    else if (nchunk <= 4 * kPassB) k_dense<4><<<num_blocks, kNT, kSmemLimit, stream>>>(a, x);
+    else k_dense<8><<<num_blocks, kNT, kSmemLimit, stream>>>(a, x);
     return cudaGetLastError();
 }
 

@@ -21,15 +21,24 @@ constexpr long long kWaitLimitNs = 2000000000LL;  // 2 s per bounded wait
 inline int padded_ff(int d_ff) { return (d_ff + kChanAlign - 1) / kChanAlign * kChanAlign; }
 
 constexpr int kMaxSlices = 16;   // proxy row slices (partial sums per channel)
-constexpr int kHistWords = 2048; // global score histogram (11-bit digit)
+constexpr int kHistWords = 2048; // score histogram (top 11 bits of the bit pattern)
+constexpr int kMaxGrid = 256;    // CTAs of the fused kernel (one per SM)
 
-// Workspace carve-out (offsets in bytes, each 256-aligned).
+// Workspace carve-out (offsets in bytes, each 256-aligned).  The first 256
+// bytes are the control block: status word, then (at +128) the grid barrier
+// count, the call epoch and the channel-selection result.
 struct Workspace {
     int* status;        // [0] device status word (0 = ok)
-    unsigned* bar;      // grid barrier word of the fused kernel
+    unsigned* bar;      // grid barrier count; bar[1] call epoch; bar[2..5] selection result
     uint32_t* hist;     // [kHistWords] score histogram, zeroed by each call
     float2* part;       // [kMaxSlices][Fp] per-slice proxy partials (g~, u~)
-    float* scores;      // [Fp] proxy ranking signal |silu(g~) u~|
+    uint32_t* skey;     // [Fp] per chunk: its score bits sorted descending
+    int* schan;         // [Fp] per chunk: the channels in that order
+    int* selc;          // [kMaxGrid] per chunk: selected channels
+    int* upre;          // [kMaxGrid + 1] prefix of the per-chunk handed-out counts
+    int* selpre;        // [kMaxGrid] debug: prefix of selc
+    int* idx_list;      // [Fp] debug: selected channels, ascending
+    float* hch;         // [Fp] debug: h per channel
     uint16_t* x_stage;  // [d] bf16 input staged from host memory (prox_ffn_host)
     float* y_stage;     // [d] fp32 output staged for host memory (prox_ffn_host)
 };
@@ -73,6 +82,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking test of a phase parity (acquire on success).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -171,7 +193,8 @@ struct FusedLaunch {
 cudaError_t fused_configure();
 bool fused_fits(int d, int F);
 int fused_threads();
-int fused_max_chan();
+int fused_max_chunk();
+int fused_max_blocks();
 size_t fused_smem_bytes();
 cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream);
 cudaError_t launch_dense(const __nv_bfloat16* gateup, const __nv_bfloat16* down_t,

@@ -25,8 +25,8 @@ PROX_ERR_TIMEOUT = 5
 PROX_ERR_DEVICE_CHECK = 6
 PROX_TRACE_EVENTS = 2
 PROX_PHASE_STAMPS = 10
-PHASES = ("start", "input_select", "proxy", "barrier1", "scores", "barrier2", "stage2_begin",
-          "first_row", "stage2_dots", "end")
+PHASES = ("start", "input_select", "proxy", "barrier1", "scores", "mask_known", "first_row",
+          "pass_a_done", "pass_b_done", "end")
 
 _lock = threading.Lock()
 _lib = None

@@ -40,8 +40,9 @@
  *   - Calls that share one prox_layer use its workspace and must be ordered
  *     with respect to each other (one stream, or events); calls on
  *     different layers are independent.
- *   - Shapes: d_model a multiple of 128 in [128, 16384]; d_ff in [1, 32768]
- *     (prox_prepare also needs ceil(d_ff / #SMs) <= 512).
+ *   - Shapes: d_model a multiple of 128 in [128, 10496] (the step's
+ *     shared-memory tables must fit one SM); d_ff in [1, 32768]
+ *     (prox_prepare also needs ceil(d_ff / #SMs) <= 256 and at most 256 SMs).
  *   - Inputs must be finite (no NaN or Inf in x or the weights).
  */
 #ifndef PROX_H
@@ -178,9 +179,10 @@ PROX_API int prox_layer_blocks(const prox_layer* layer);
  * stamps[b * PROX_PHASE_STAMPS + i] (uint64, device, prox_layer_blocks()
  * rows, zeroed first; a phase the kernel does not have stays 0):
  *   0 start; 1 input selection done; 2 proxy partials written;
- *   3 past the first grid barrier; 4 scores and histogram done;
- *   5 past the second grid barrier; 6 Stage 2 begins (channel list ready);
- *   7 first gate|up row landed; 8 Stage 2 dot products done; 9 end.
+ *   3 past the first grid barrier; 4 scores, histogram and local ranks done
+ *   (Stage 2 starts on the speculative channels); 5 exact channel mask
+ *   known (this CTA's item list final); 6 first gate|up row landed;
+ *   7 gate|up dot products done; 8 W_down^T accumulation done; 9 end.
  * The dense step stamps 0 and 6..9 only.  Same results as prox_ffn /
  * prox_dense_ffn.
  */
