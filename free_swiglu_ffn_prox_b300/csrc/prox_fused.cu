@@ -78,7 +78,8 @@ struct Ctl {
     uint64_t sel_bar;                // completes when the item list is final
     uint64_t done_bar;               // every warp is through its Stage-2 role
     uint64_t ld_bar;                 // bulk load of the proxy scales (P1)
-    uint64_t sel_ld;                 // bulk loads of the selection (CTA 0)
+    uint64_t sel_ld;                 // bulk load of the digit-1 histogram (CTA 0)
+    uint64_t key_ld;                 // bulk load of the sorted chunk keys (CTA 0)
     int gu_last[kMaxStages], d_last[kMaxStages];
     float h[kMaxItems];              // h of each item
     int item[kMaxItems];             // channel of each item
@@ -785,10 +786,14 @@ __device__ __forceinline__ int count_leading(const uint32_t* s, int n, Pred pred
 template <typename V>
 __device__ __forceinline__ void warp_chunk_scan(int nb, V v, int* out) {
     const int lane = threadIdx.x & 31;
-    const int per = (nb + 31) >> 5, t0 = lane * per;
+    const int per = (nb + 31) >> 5, t0 = lane * per;  // per <= kMaxBlocks / 32
+    int val[kMaxBlocks / 32];
     int run = 0;
-    for (int j = 0; j < per; ++j)
-        if (t0 + j < nb) run += v(t0 + j);
+#pragma unroll
+    for (int j = 0; j < kMaxBlocks / 32; ++j) {
+        val[j] = (j < per && t0 + j < nb) ? v(t0 + j) : 0;
+        run += val[j];
+    }
     int incl = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -796,10 +801,11 @@ __device__ __forceinline__ void warp_chunk_scan(int nb, V v, int* out) {
         if (lane >= o) incl += t;
     }
     int base = incl - run;
-    for (int j = 0; j < per; ++j)
-        if (t0 + j < nb) {
+#pragma unroll
+    for (int j = 0; j < kMaxBlocks / 32; ++j)
+        if (j < per && t0 + j < nb) {
             out[t0 + j] = base;
-            base += v(t0 + j);
+            base += val[j];
         }
     if (lane == 31) out[nb] = incl;
     __syncwarp();
@@ -848,7 +854,9 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
     int* ceq = cgt + kMaxBlocks;                           // keys equal to T
     int* epre = ceq + kMaxBlocks;                          // [kMaxBlocks + 1]
     int* csel = epre + kMaxBlocks + 1;                     // selected
-    uint32_t* cand = reinterpret_cast<uint32_t*>(csel + kMaxBlocks);  // [kCandCap]
+    int* cbeg = csel + kMaxBlocks;                         // [kMaxBlocks + 1] chunk starts
+    int* cspc = cbeg + kMaxBlocks + 1;                     // speculative items per chunk
+    uint32_t* cand = reinterpret_cast<uint32_t*>(cspc + kMaxBlocks);  // [kCandCap]
     if (tid < 32) {
         bool ok = true;
         if (lane == 0) {
@@ -872,25 +880,36 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
                 *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 const uint64_t pol = policy_evict_first();
-                mbar_arrive_expect_tx(&ctl.sel_ld, (uint32_t)(kHistBins * 4 + Fp * 4));
+                mbar_arrive_expect_tx(&ctl.sel_ld, (uint32_t)(kHistBins * 4));
                 bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.sel_ld, pol);
-                bulk_g2s(sk, p.skey, (uint32_t)(Fp * 4), &ctl.sel_ld, pol);
+                mbar_arrive_expect_tx(&ctl.key_ld, (uint32_t)(Fp * 4));
+                bulk_g2s(sk, p.skey, (uint32_t)(Fp * 4), &ctl.key_ld, pol);
             }
         }
         __syncwarp();
     }
     for (int i = tid; i < kHistBins + 512; i += kNT) h2[i] = 0u;
+    for (int t = tid; t <= nb; t += kNT) {
+        cbeg[t] = chunk_begin(F, t, nb);
+        if (t < nb) cspc[t] = chunk_spec(p, t, nb);
+    }
     __syncthreads();
     if (ctl.abort) return false;
-    if (!mbar_wait_bounded(&ctl.sel_ld, 0, p.limit_ns, &ctl.abort) && lane == 0) {
-        ctl.abort = 1;
-        record_status(p.status, PROX_ERR_TIMEOUT);
-    }
-    __syncthreads();
-    if (ctl.abort) {
-        if (tid == 0) mbar_wait_bounded(&ctl.sel_ld, 0, p.limit_ns, nullptr);  // let it land
+    // waits for one of the two staging copies; after a timeout lets both land
+    auto landed = [&](uint64_t* bar) {
+        if (!mbar_wait_bounded(bar, 0, p.limit_ns, &ctl.abort) && lane == 0) {
+            ctl.abort = 1;
+            record_status(p.status, PROX_ERR_TIMEOUT);
+        }
+        __syncthreads();
+        if (!ctl.abort) return true;
+        if (tid == 0) {
+            mbar_wait_bounded(&ctl.sel_ld, 0, p.limit_ns, nullptr);
+            mbar_wait_bounded(&ctl.key_ld, 0, p.limit_ns, nullptr);
+        }
         return false;
-    }
+    };
+    if (!landed(&ctl.sel_ld)) return false;
     auto broken = [&]() {
         if (tid == 0) {
             record_status(p.status, PROX_ERR_DEVICE_CHECK);
@@ -898,13 +917,14 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
         }
         return false;
     };
-    // digit 1 from the histogram of every chunk
+    // digit 1 from the histogram of every chunk (the sorted keys still landing)
     block_select<2048>(h1, (uint32_t)p.k, ctl);
     if (ctl.sel[0] == 0xffffffffu) return broken();
     const uint32_t b1 = ctl.sel[0], k1 = ctl.sel[1];
+    if (!landed(&ctl.key_ld)) return false;
     // per chunk: its digit-1 candidates are the sorted positions [lo, hi)
     if (tid < nb) {
-        const int c0 = chunk_begin(F, tid, nb), n = chunk_begin(F, tid + 1, nb) - c0;
+        const int c0 = cbeg[tid], n = cbeg[tid + 1] - c0;
         const int lo = count_leading(sk + c0, n, [&](uint32_t kk) { return (kk >> 20) > b1; });
         const int hi = count_leading(sk + c0, n, [&](uint32_t kk) { return (kk >> 20) >= b1; });
         clo[tid] = lo;
@@ -916,7 +936,7 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
     const int n_c = coff[nb];
     const bool compact = n_c <= kCandCap;
     if (compact && tid < nb) {
-        const uint32_t* src = sk + chunk_begin(F, tid, nb) + clo[tid];
+        const uint32_t* src = sk + cbeg[tid] + clo[tid];
         for (int i = 0; i < ccn[tid]; ++i) cand[coff[tid] + i] = src[i];
     }
     __syncthreads();
@@ -944,13 +964,23 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
     if (ctl.sel[0] == 0xffffffffu) return broken();
     const uint32_t T = (pre << 9) | ctl.sel[0];
     const int r = (int)ctl.sel[1];  // keys equal to T to keep, lowest channels first
-    // per chunk: keys above and equal to T
+    // per chunk: keys above and equal to T (T lies in the digit-1 bin, so
+    // every key before the chunk's candidates is above it)
     if (tid < nb) {
-        const int c0 = chunk_begin(F, tid, nb), n = chunk_begin(F, tid + 1, nb) - c0;
-        const int gt = count_leading(sk + c0, n, [&](uint32_t kk) { return kk > T; });
-        const int ge = count_leading(sk + c0, n, [&](uint32_t kk) { return kk >= T; });
+        int gt = clo[tid], eq = 0;
+        if (compact) {
+            const uint32_t* cs = cand + coff[tid];
+            for (int i = 0; i < ccn[tid]; ++i) {
+                gt += cs[i] > T;
+                eq += cs[i] == T;
+            }
+        } else {
+            const int c0 = cbeg[tid], n = cbeg[tid + 1] - c0;
+            gt = count_leading(sk + c0, n, [&](uint32_t kk) { return kk > T; });
+            eq = count_leading(sk + c0, n, [&](uint32_t kk) { return kk >= T; }) - gt;
+        }
         cgt[tid] = gt;
-        ceq[tid] = ge - gt;
+        ceq[tid] = eq;
     }
     __syncthreads();
     if (wid == 0) {
@@ -961,7 +991,7 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
             p.selc[t] = sel;
         }
         __syncwarp();
-        warp_chunk_scan(nb, [&](int t) { return max(csel[t] - chunk_spec(p, t, nb), 0); }, p.upre);
+        warp_chunk_scan(nb, [&](int t) { return max(csel[t] - cspc[t], 0); }, p.upre);
         if (p.debug) warp_chunk_scan(nb, [&](int t) { return csel[t]; }, p.selpre);
     }
     __syncthreads();  // the per-chunk results are out
@@ -1332,6 +1362,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     if (tid == 0) {
         stage2_init(ctl, p.n_gu, p.n_d);
         mbar_init(&ctl.sel_ld, 1);
+        mbar_init(&ctl.key_ld, 1);
         fence_mbar_init();
     }
     __syncthreads();
