@@ -58,6 +58,7 @@ constexpr int kBarriers = 2;              // grid barriers per call
 constexpr int kRing = 8;                  // proxy rows in flight per thread (cp.async ring)
 static_assert((kRing & (kRing - 1)) == 0, "ring depth must be a power of two");
 constexpr int kHistBins = 2048;
+constexpr int kXGroups = 3;               // 8-element x groups per thread: d <= 8 * 3 * kNT
 static_assert(kHistBins <= kHistWords, "histogram words");
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr int kPhaseStamps = 10;
@@ -1096,76 +1097,104 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     }
 
     // ------------------------------------------------ P0: input sparsity
-    // area: x bf16 [d] | kept u32 [d] | histograms u32 [1024] | P1 tables
-    // Warp w takes the x entries [w Lx, (w+1) Lx), lane-consecutive.
+    // area: x bf16 [d] | kept u32 [d] | histograms u32 [256 + 128] | P1 tables
+    // Thread t holds the x groups [t G, (t+1) G) (8 bf16 each) in registers,
+    // so the passes over the 15-bit keys |x| touch no memory; exact top-k_x in
+    // two radix digits: the exponent (bits 14..7) and the 7 mantissa bits.
     uint16_t* xs = reinterpret_cast<uint16_t*>(area);
     uint32_t* kept = reinterpret_cast<uint32_t*>(area + (size_t)2 * d);
     uint32_t* hA = kept + d;
-    for (int i = tid; i < d / 8; i += kNT)
-        reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
-    for (int i = tid; i < 384; i += kNT) hA[i] = 0u;
-    if (b == 0) {
-        for (int i = tid; i < d; i += kNT) p.y[i] = 0.0f;
-        for (int i = tid; i < kHistWords; i += kNT) p.hist[i] = 0u;
-    }
-    __syncthreads();
-    // exact top-k_x of |x| (15-bit keys): digit 1 = exponent (bits 14..7),
-    // digit 2 = the 7 mantissa bits; thread t owns [t kpx, (t+1) kpx)
-    const int kpx = (d + kNT - 1) / kNT;
-    const int xi0 = tid * kpx;
-    auto xkey = [&](int i) { return (uint32_t)(xs[i] & 0x7fffu); };
+    uint32_t* hB = hA + 256;
     {
-        uint32_t mk = 0;
-        for (int e = 0; e < kpx; ++e) {
-            const int i = xi0 + e;
-            if (i < d) {
-                const uint32_t kk = xkey(i);
-                mk = max(mk, kk);
-                atomicAdd(&hA[kk >> 7], 1u);
-            }
+        const int ng = d / 8, G = (ng + kNT - 1) / kNT, g0 = tid * G;  // G <= kXGroups
+        uint4 xv[kXGroups];
+#pragma unroll
+        for (int q = 0; q < kXGroups; ++q)
+            xv[q] = (q < G && g0 + q < ng) ? __ldg(reinterpret_cast<const uint4*>(p.x) + g0 + q)
+                                           : make_uint4(0u, 0u, 0u, 0u);
+        auto valid = [&](int q) { return q < G && g0 + q < ng; };
+        auto half = [&](const uint4& v, int e) {
+            const uint32_t w = e < 2 ? v.x : e < 4 ? v.y : e < 6 ? v.z : v.w;
+            return (e & 1) ? (w >> 16) : (w & 0xffffu);
+        };
+        for (int i = tid; i < 384; i += kNT) hA[i] = 0u;
+        if (tid == 0) ctl.sel[3] = 0u;
+        if (b == 0) {
+            for (int i = tid; i < d; i += kNT) p.y[i] = 0.0f;
+            for (int i = tid; i < kHistWords; i += kNT) p.hist[i] = 0u;
         }
+        __syncthreads();
+        uint32_t mk = 0;
+#pragma unroll
+        for (int q = 0; q < kXGroups; ++q)
+            if (valid(q)) {
+                reinterpret_cast<uint4*>(xs)[g0 + q] = xv[q];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t kk = half(xv[q], e) & 0x7fffu;
+                    mk = max(mk, kk);
+                    atomicAdd(&hA[kk >> 7], 1u);
+                }
+            }
         mk = __reduce_max_sync(0xffffffffu, mk);
-        if (lane == 0) ctl.warp_tot[wid] = mk;
-    }
-    __syncthreads();
-    if (tid == 0) {  // power-of-two prescale: max|x| * 2^shift in [2^14, 2^15)
-        uint32_t mk = 0;
-        for (int w = 0; w < kNT / 32; ++w) mk = max(mk, ctl.warp_tot[w]);
-        int sh = 0;
-        if (mk != 0) {
-            int ex;
-            frexpf(__uint_as_float(mk << 16), &ex);  // max|x| in [2^(ex-1), 2^ex)
-            sh = 15 - ex;
-        }
-        ctl.sel[2] = (uint32_t)sh;
-    }
-    uint32_t xT, xr, xpos, xties, xn;
-    {
-        const TopkPlan plx{7, 256, 0, 128, 1};
-        topk_digits<kNT>(plx, d, kpx, (uint32_t)p.kx, xkey, hA, hA + 256, nullptr, ctl, xT, xr,
-                         xpos, xties, xn);
-    }
-    const int shift = (int)ctl.sel[2];
-    if (xn) {
-        uint32_t pos = xpos, tie = xties;
-        for (int e = 0; e < kpx; ++e) {
-            const int j = xi0 + e;
-            if (j < d) {
-                const uint32_t kk = xkey(j);
-                bool keep = kk > xT;
-                if (kk == xT) {
-                    keep = tie < xr;
-                    ++tie;
-                }
-                if (keep) {
-                    kept[pos] = ((uint32_t)j << 16) | scaled_fp16(xs[j], shift);
-                    if (b == 0 && p.kept_out) p.kept_out[pos] = j;
-                    ++pos;
-                }
+        if (lane == 0) atomicMax(&ctl.sel[3], mk);
+        __syncthreads();
+        if (tid == 0) {  // power-of-two prescale: max|x| * 2^shift in [2^14, 2^15)
+            const uint32_t mx = ctl.sel[3];
+            int sh = 0;
+            if (mx != 0) {
+                int ex;
+                frexpf(__uint_as_float(mx << 16), &ex);  // max|x| in [2^(ex-1), 2^ex)
+                sh = 15 - ex;
             }
+            ctl.sel[2] = (uint32_t)sh;
         }
+        block_select<256>(hA, (uint32_t)p.kx, ctl);
+        const uint32_t b1 = ctl.sel[0], k1 = ctl.sel[1];
+#pragma unroll
+        for (int q = 0; q < kXGroups; ++q)
+            if (valid(q))
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t kk = half(xv[q], e) & 0x7fffu;
+                    if ((kk >> 7) == b1) atomicAdd(&hB[kk & 127u], 1u);
+                }
+        __syncthreads();
+        block_select<128>(hB, k1, ctl);
+        const uint32_t T = (b1 << 7) | ctl.sel[0], r = ctl.sel[1];
+        uint32_t gt = 0, eq = 0;
+#pragma unroll
+        for (int q = 0; q < kXGroups; ++q)
+            if (valid(q))
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t kk = half(xv[q], e) & 0x7fffu;
+                    gt += kk > T;
+                    eq += kk == T;
+                }
+        uint32_t tot;
+        const uint32_t ex = block_excl_scan<kNT>(gt | (eq << 16), ctl, tot);
+        uint32_t tie = ex >> 16;
+        uint32_t pos = (ex & 0xffffu) + min(tie, r);  // kept entries before this thread's
+        const int shift = (int)ctl.sel[2];
+#pragma unroll
+        for (int q = 0; q < kXGroups; ++q)
+            if (valid(q))
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t hb = half(xv[q], e), kk = hb & 0x7fffu;
+                    bool keep = kk > T;
+                    if (kk == T) keep = tie++ < r;
+                    if (keep) {
+                        const int j = (g0 + q) * 8 + e;
+                        kept[pos] = ((uint32_t)j << 16) | scaled_fp16((uint16_t)hb, shift);
+                        if (b == 0 && p.kept_out) p.kept_out[pos] = j;
+                        ++pos;
+                    }
+                }
     }
     __syncthreads();
+    const int shift = (int)ctl.sel[2];
     stamp(p.ts, 1);
 
     // ------------------------------------------------ P1: proxy partials
@@ -1542,7 +1571,7 @@ bool fused_fits(int d, int F) {
     const size_t p01 = (size_t)6 * d + 4096 + (size_t)8 * 16 * kNT + (size_t)16 * kRing * kNT;
     const Ring r = ring_for(d);
     return p01 <= area_budget() && ring_bytes(d, r) <= area_budget() && r.n_gu >= 1 &&
-           r.n_d >= 1;
+           r.n_d >= 1 && d / 8 <= kXGroups * kNT;
 }
 
 namespace {
