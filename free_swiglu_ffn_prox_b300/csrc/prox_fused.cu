@@ -55,7 +55,8 @@ constexpr int kMaxItems = 512;            // Stage-2 items per CTA
 constexpr int kMaxChunk = 256;            // channels per CTA chunk
 constexpr int kMaxBlocks = kMaxGrid;
 constexpr int kBarriers = 2;              // grid barriers per call
-constexpr int kRing = 8;                  // proxy rows in flight per thread (cp.async ring)
+constexpr int kRing = 16;                 // proxy rows in flight per thread (cp.async ring)
+static_assert(kRing >= 8, "the running-total table reuses the ring (16 x 8 bytes per thread)");
 static_assert((kRing & (kRing - 1)) == 0, "ring depth must be a power of two");
 constexpr int kHistBins = 2048;
 constexpr int kXGroups = 3;               // 8-element x groups per thread: d <= 8 * 3 * kNT
@@ -1212,12 +1213,12 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         // row-lane rl takes the contiguous kept rows [q_beg, q_end)
         const int m = (r1 - r0 + R - 1) / R;
         const int q_beg = min(r1, r0 + rl * m), q_end = min(r1, q_beg + m);
-        // running totals, [R][16][tpr] float2: channel cu * 16 + t of row-lane
-        // rl at (rl * 16 + t) * tpr + cu, so a warp's lanes (consecutive cu)
-        // touch consecutive 8-byte words
-        float2* tot = reinterpret_cast<float2*>(hA + 1024);
-        // per-thread ring of proxy row segments in flight, [kRing][kNT]
-        uint4* ring = reinterpret_cast<uint4*>(tot + (size_t)R * 16 * tpr);
+        // per-thread ring of proxy row segments in flight, [kRing][kNT]; after
+        // the rows are in, the running totals [R][16][tpr] float2 (channel
+        // cu * 16 + t of row-lane rl at (rl * 16 + t) * tpr + cu, so a warp's
+        // lanes touch consecutive 8-byte words) take its place
+        uint4* ring = reinterpret_cast<uint4*>(hA + 1024);
+        float2* tot = reinterpret_cast<float2*>(ring);
         uint8_t* after_ring = reinterpret_cast<uint8_t*>(ring + (size_t)kRing * kNT);
         const size_t room = area_budget_dev() - (size_t)(after_ring - area);
         // the slice's fp16 scale pairs, [g - g_lo][W], loaded by bulk copies
@@ -1235,11 +1236,10 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                 bulk_g2s(ssc + (size_t)g * W, p.scales + (size_t)(g_lo + g) * Fp + c0,
                          (uint32_t)(width * 4), &ctl.ld_bar, pol);
         }
-        if (active)
-            for (int t = 0; t < 16; ++t) tot[((size_t)rl * 16 + t) * tpr + cu] = make_float2(0.0f, 0.0f);
-        float ag[16], au[16];
+        // this group's sums (ag, au) and the scaled running totals (tg, tu)
+        float ag[16], au[16], tg[16], tu[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) ag[t] = au[t] = 0.0f;
+        for (int t = 0; t < 16; ++t) ag[t] = au[t] = tg[t] = tu[t] = 0.0f;
         int cur_g = -1;
         bool scales_in = false;
         auto flush = [&]() {
@@ -1257,7 +1257,6 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
             } else {
                 src = reinterpret_cast<const uint4*>(p.scales + (size_t)cur_g * Fp + c0 + cu * 16);
             }
-            float2* dst = tot + (size_t)rl * 16 * tpr + cu;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
                 const uint4 s4 = src[v];
@@ -1266,10 +1265,8 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                 for (int e = 0; e < 4; ++e) {
                     const int t = 4 * v + e;
                     const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&sv[e]));
-                    float2 o = dst[(size_t)t * tpr];
-                    o.x = fmaf(s2.x, ag[t], o.x);
-                    o.y = fmaf(s2.y, au[t], o.y);
-                    dst[(size_t)t * tpr] = o;
+                    tg[t] = fmaf(s2.x, ag[t], tg[t]);
+                    tu[t] = fmaf(s2.y, au[t], tu[t]);
                     ag[t] = 0.0f;
                     au[t] = 0.0f;
                 }
@@ -1323,6 +1320,11 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                 ctl.abort = 1;
                 record_status(p.status, PROX_ERR_TIMEOUT);
             }
+        __syncthreads();  // every thread is done with its ring slots
+        if (active)
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+                tot[((size_t)rl * 16 + t) * tpr + cu] = make_float2(tg[t], tu[t]);
         __syncthreads();
         float2* out = p.part + (size_t)slice * Fp + c0;
         // thread e sums channel (e % tpr) * 16 + e / tpr over the row-lanes:
@@ -1565,10 +1567,10 @@ int fused_max_chunk() { return kMaxChunk; }
 int fused_max_blocks() { return kMaxBlocks; }
 
 bool fused_fits(int d, int F) {
-    // P0: x (2 d) + kept list (4 d) + histogram; P1 adds the [R][W] partial
-    // table (at most 8 * 16 * kNT bytes) and the cp.async ring; P3: rings.
+    // P0: x (2 d) + kept list (4 d) + histograms; P1 adds the cp.async ring
+    // (the running-total table reuses it); P3: the Stage-2 rings.
     (void)F;
-    const size_t p01 = (size_t)6 * d + 4096 + (size_t)8 * 16 * kNT + (size_t)16 * kRing * kNT;
+    const size_t p01 = (size_t)6 * d + 4096 + (size_t)16 * kRing * kNT;
     const Ring r = ring_for(d);
     return p01 <= area_budget() && ring_bytes(d, r) <= area_budget() && r.n_gu >= 1 &&
            r.n_d >= 1 && d / 8 <= kXGroups * kNT;
