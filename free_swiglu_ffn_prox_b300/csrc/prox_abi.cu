@@ -15,9 +15,9 @@ static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t workspace_bytes(int d, int F) {
     const size_t Fp = (size_t)padded_ff(F);
-    return align256(256) + align256((size_t)kHistWords * 4) +
-           align256((size_t)kMaxSlices * Fp * 8) + 3 * align256((size_t)(kMaxGrid + 1) * 4) +
-           4 * align256(Fp * 4) + align256((size_t)d * 2) + align256((size_t)d * 4);
+    return kControlBytes + align256((size_t)kHistWords * 4) +
+           align256((size_t)kMaxSlices * Fp * 8) + 2 * align256((size_t)(kMaxGrid + 1) * 4) +
+           4 * align256(Fp * 4) + align256(Fp) + align256((size_t)d * 2) + align256((size_t)d * 4);
 }
 
 Workspace carve_workspace(void* base, int d, int F) {
@@ -26,24 +26,26 @@ Workspace carve_workspace(void* base, int d, int F) {
     Workspace w;
     w.status = reinterpret_cast<int*>(p);
     w.bar = reinterpret_cast<unsigned*>(p + 128);
-    p += align256(256);
+    w.ready = reinterpret_cast<unsigned*>(p + 1024);
+    p += kControlBytes;
     w.hist = reinterpret_cast<uint32_t*>(p);
     p += align256((size_t)kHistWords * 4);
     w.part = reinterpret_cast<float2*>(p);
     p += align256((size_t)kMaxSlices * Fp * 8);
-    int** counts[3] = {&w.selc, &w.upre, &w.selpre};
-    for (int** c : counts) {
-        *c = reinterpret_cast<int*>(p);
-        p += align256((size_t)(kMaxGrid + 1) * 4);
-    }
+    w.selc = reinterpret_cast<int*>(p);
+    p += align256((size_t)(kMaxGrid + 1) * 4);
+    w.selpre = reinterpret_cast<int*>(p);
+    p += align256((size_t)(kMaxGrid + 1) * 4);
     w.skey = reinterpret_cast<uint32_t*>(p);
     p += align256(Fp * 4);
-    w.schan = reinterpret_cast<int*>(p);
+    w.ulist = reinterpret_cast<int*>(p);
     p += align256(Fp * 4);
     w.idx_list = reinterpret_cast<int*>(p);
     p += align256(Fp * 4);
     w.hch = reinterpret_cast<float*>(p);
     p += align256(Fp * 4);
+    w.sidx = p;
+    p += align256(Fp);
     w.x_stage = reinterpret_cast<uint16_t*>(p);
     p += align256((size_t)d * 2);
     w.y_stage = reinterpret_cast<float*>(p);
@@ -183,7 +185,8 @@ prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, const void* 
     if (e != cudaSuccess) return PROX_ERR_CUDA;
     // one persistent CTA per SM; every CTA holds its chunk of the channels
     // in shared memory
-    if (sms > prox::fused_max_blocks() || (d_ff + sms - 1) / sms > prox::fused_max_chunk())
+    const int g4 = (d_ff + 3) / 4;  // chunks start on multiples of 4 channels
+    if (sms > prox::fused_max_blocks() || 4 * ((g4 + sms - 1) / sms) > prox::fused_max_chunk())
         return PROX_ERR_UNSUPPORTED_SHAPE;
     prox_layer* L = new (std::nothrow) prox_layer;
     if (!L) return PROX_ERR_INVALID_ARG;
@@ -291,7 +294,8 @@ prox_status prox_get_status(const prox_layer* layer, prox_stream_t stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     // clear the status word and, after a fault, the grid barrier word (a
     // barrier that ran out leaves it part-way)
-    if (e == cudaSuccess) e = cudaMemsetAsync(layer->ws.status, 0, v != 0 ? 256 : sizeof(int), s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(layer->ws.status, 0, v != 0 ? prox::kControlBytes : sizeof(int), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return PROX_ERR_CUDA;
     return (prox_status)v;

@@ -16,7 +16,7 @@
 //   P3  Stage 2 (Eq. (1) of the PrunePath page restricted to the mask) and
 //       the exact channel top-k run side by side:
 //       - the items of CTA b > 0 start with the top m channels of its own
-//         chunk, m = 0.9 x the chunk's expected share of the mask; these are
+//         chunk, m = the chunk's expected share k nch / F of the mask; these are
 //         in the mask with high probability, so their rows stream at once;
 //       - CTA 0 alone waits for every chunk (grid barrier 2), stages all
 //         scores in shared memory and finds the exact top-k (three radix
@@ -54,7 +54,7 @@ constexpr int kMaxStages = 16;
 constexpr int kMaxItems = 512;            // Stage-2 items per CTA
 constexpr int kMaxChunk = 256;            // channels per CTA chunk
 constexpr int kMaxBlocks = kMaxGrid;
-constexpr int kBarriers = 2;              // grid barriers per call
+constexpr int kBarriers = 1;              // grid-barrier arrivals per CTA per call
 constexpr int kRing = 16;                 // proxy rows in flight per thread (cp.async ring)
 static_assert(kRing >= 8, "the running-total table reuses the ring (16 x 8 bytes per thread)");
 static_assert((kRing & (kRing - 1)) == 0, "ring depth must be a power of two");
@@ -81,7 +81,7 @@ struct Ctl {
     uint64_t done_bar;               // every warp is through its Stage-2 role
     uint64_t ld_bar;                 // bulk load of the proxy scales (P1)
     uint64_t sel_ld;                 // bulk load of the digit-1 histogram (CTA 0)
-    uint64_t key_ld;                 // bulk load of the sorted chunk keys (CTA 0)
+    uint64_t key_ld;                 // bulk loads of the sorted chunk lists (CTA 0)
     int gu_last[kMaxStages], d_last[kMaxStages];
     float h[kMaxItems];              // h of each item
     int item[kMaxItems];             // channel of each item
@@ -89,7 +89,6 @@ struct Ctl {
     uint8_t hready[kMaxItems];       // h[i] written by pass A
     float lsc[kMaxChunk];            // scores of this CTA's chunk
     uint16_t lrank[kMaxChunk];       // rank of each chunk channel (score desc, channel asc)
-    int upre[kMaxBlocks + 1];        // prefix over chunks of the handed-out channel counts
     uint32_t warp_tot[kNT / 32 + 1];
     uint32_t sel[4];
     unsigned epoch;
@@ -121,10 +120,11 @@ struct FusedParams {
     uint32_t* hist;      // [kHistWords]: digit-1, digit-2, digit-3 histograms
     float2* part;        // [slices][Fp]
     uint32_t* skey;      // [Fp] per chunk at its first channel: its score bits, descending
-    int* schan;          // [Fp] ... the channels in that order (ties: lower channel first)
+    uint8_t* sidx;       // [Fp] ... their chunk-local channel indices in that order (ties: lower first)
     int* selc;           // [kMaxBlocks] per chunk: how many of its channels are selected
-    int* upre;           // [kMaxBlocks + 1] prefix of the per-chunk handed-out counts
     int* selpre;         // [kMaxBlocks] debug: prefix of selc
+    int* ulist;          // [Fp] the handed-out channels (selected, not speculated), chunk order
+    unsigned* ready;     // [kMaxBlocks] per chunk: epoch + 1 once its sorted list is out
     int* idx_list;       // [Fp] debug: the selected channels, ascending
     float* hch;          // [Fp] debug: h per channel
     // debug outputs (may be null)
@@ -144,10 +144,18 @@ __host__ __device__ __forceinline__ int chunk_begin(int F, int b, int nb) {
     return (int)((unsigned)F * (unsigned)b / (unsigned)nb);
 }
 
-// Speculative items of a chunk of nch channels: 0.9 x its expected share
+// First channel of CTA b's chunk in the fused kernel: chunk starts are
+// multiples of 4 channels (so per-chunk arrays copy in 16-byte pieces); the
+// last chunk ends at F.
+__host__ __device__ __forceinline__ int chunk_lo(int F, int b, int nb) {
+    const int c = 4 * chunk_begin((F + 3) >> 2, b, nb);
+    return c < F ? c : F;
+}
+
+// Speculative items of a chunk of nch channels: its expected share
 // k nch / F of the mask.
 __host__ __device__ __forceinline__ int spec_count(int k, int nch, int F) {
-    const unsigned m = 9u * (unsigned)k * (unsigned)nch / (10u * (unsigned)F);  // < 2^27
+    const unsigned m = (unsigned)k * (unsigned)nch / (unsigned)F;  // < 2^23
     return (int)(m < (unsigned)nch ? m : (unsigned)nch);
 }
 
@@ -726,7 +734,7 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 }
 
 // ------------------------------------------------------------ the selection
-constexpr int kCandCap = 4096;  // digit-1 candidates kept in shared memory
+constexpr int kCandCap = 2048;  // digit-1 candidates kept in shared memory
 
 __device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -826,7 +834,7 @@ __device__ __forceinline__ int chunk_of(const int* pre, int n, int q) {
 
 // Speculative items of chunk c (the owner's rule).
 __device__ __forceinline__ int chunk_spec(const FusedParams& p, int c, int nb) {
-    return c == 0 ? 0 : spec_count(p.k, chunk_begin(p.F, c + 1, nb) - chunk_begin(p.F, c, nb), p.F);
+    return c == 0 ? 0 : spec_count(p.k, chunk_lo(p.F, c + 1, nb) - chunk_lo(p.F, c, nb), p.F);
 }
 
 // CTA 0, all threads: the exact channel top-k once every chunk is in (grid
@@ -849,7 +857,8 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
     uint32_t* h2 = h1 + kHistBins;
     uint32_t* h3 = h2 + kHistBins;
     uint32_t* sk = h3 + 512;                               // [Fp] sorted keys per chunk
-    int* clo = reinterpret_cast<int*>(sk + Fp);            // [kMaxBlocks] first candidate
+    uint8_t* sidx = reinterpret_cast<uint8_t*>(sk + Fp);   // [Fp] their chunk-local channels
+    int* clo = reinterpret_cast<int*>(sidx + Fp);          // [kMaxBlocks] first candidate
     int* ccn = clo + kMaxBlocks;                           // candidates
     int* coff = ccn + kMaxBlocks;                          // [kMaxBlocks + 1]
     int* cgt = coff + kMaxBlocks + 1;                      // keys above T
@@ -858,45 +867,47 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
     int* csel = epre + kMaxBlocks + 1;                     // selected
     int* cbeg = csel + kMaxBlocks;                         // [kMaxBlocks + 1] chunk starts
     int* cspc = cbeg + kMaxBlocks + 1;                     // speculative items per chunk
-    uint32_t* cand = reinterpret_cast<uint32_t*>(cspc + kMaxBlocks);  // [kCandCap]
-    if (tid < 32) {
-        bool ok = true;
-        if (lane == 0) {
-            const unsigned target = (unsigned)nb * (kBarriers * ep + 2u);
-            uint64_t t0 = 0;
-            for (uint32_t it = 1;; ++it) {
-                if ((int)(ld_acquire_gpu(p.bar) - target) >= 0) break;
-                if ((it & 15u) == 0) {
-                    const uint64_t now = global_timer_ns();
-                    if (t0 == 0) t0 = now;
-                    else if ((long long)(now - t0) > p.limit_ns) {
-                        ok = false;
-                        break;
-                    }
-                }
-            }
-            if (!ok) {
-                record_status(p.status, PROX_ERR_TIMEOUT);
-                ctl.abort = 1;
-            } else {
-                *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                const uint64_t pol = policy_evict_first();
-                mbar_arrive_expect_tx(&ctl.sel_ld, (uint32_t)(kHistBins * 4));
-                bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.sel_ld, pol);
-                mbar_arrive_expect_tx(&ctl.key_ld, (uint32_t)(Fp * 4));
-                bulk_g2s(sk, p.skey, (uint32_t)(Fp * 4), &ctl.key_ld, pol);
-            }
-        }
-        __syncwarp();
-    }
+    int* upre = cspc + kMaxBlocks;                         // [kMaxBlocks + 1]
+    uint32_t* cand = reinterpret_cast<uint32_t*>(upre + kMaxBlocks + 1);  // [kCandCap]
     for (int i = tid; i < kHistBins + 512; i += kNT) h2[i] = 0u;
     for (int t = tid; t <= nb; t += kNT) {
-        cbeg[t] = chunk_begin(F, t, nb);
+        cbeg[t] = chunk_lo(F, t, nb);
         if (t < nb) cspc[t] = chunk_spec(p, t, nb);
+    }
+    // thread t < nb waits for chunk t's ready flag; then the histogram, all
+    // sorted keys and the chunk-local indices arrive by three bulk copies
+    // (the histogram on its own barrier, so digit 1 runs while the rest lands)
+    if (tid < nb) {
+        bool ok = true;
+        uint64_t t0 = 0;
+        for (uint32_t it = 1;; ++it) {
+            if (ld_acquire_gpu(p.ready + tid) == ep + 1u) break;
+            if ((it & 15u) == 0) {
+                const uint64_t now = global_timer_ns();
+                if (t0 == 0) t0 = now;
+                else if ((long long)(now - t0) > p.limit_ns) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        if (!ok) {
+            record_status(p.status, PROX_ERR_TIMEOUT);
+            ctl.abort = 1;
+        }
     }
     __syncthreads();
     if (ctl.abort) return false;
+    if (tid == 0) {
+        *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;  // every CTA has read it
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        const uint64_t pol = policy_evict_first();
+        mbar_arrive_expect_tx(&ctl.sel_ld, (uint32_t)(kHistBins * 4));
+        bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.sel_ld, pol);
+        mbar_arrive_expect_tx(&ctl.key_ld, (uint32_t)(Fp * 5));
+        bulk_g2s(sk, p.skey, (uint32_t)(Fp * 4), &ctl.key_ld, pol);
+        bulk_g2s(sidx, p.sidx, (uint32_t)Fp, &ctl.key_ld, pol);
+    }
     // waits for one of the two staging copies; after a timeout lets both land
     auto landed = [&](uint64_t* bar) {
         if (!mbar_wait_bounded(bar, 0, p.limit_ns, &ctl.abort) && lane == 0) {
@@ -993,12 +1004,21 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
             p.selc[t] = sel;
         }
         __syncwarp();
-        warp_chunk_scan(nb, [&](int t) { return max(csel[t] - cspc[t], 0); }, p.upre);
+        warp_chunk_scan(nb, [&](int t) { return max(csel[t] - cspc[t], 0); }, upre);
         if (p.debug) warp_chunk_scan(nb, [&](int t) { return csel[t]; }, p.selpre);
     }
-    __syncthreads();  // the per-chunk results are out
+    __syncthreads();
+    // the handed-out list: per chunk, in chunk order, its selected channels of
+    // rank >= its speculative count
+    const int U = upre[nb];
+    for (int q = tid; q < U; q += kNT) {
+        const int c = chunk_of(upre, nb, q);
+        p.ulist[q] = cbeg[c] + sidx[cbeg[c] + cspc[c] + (q - upre[c])];
+    }
+    __syncthreads();  // the per-chunk results and the list are out
     if (tid == 0) {
-        st_release_gpu(p.bar + 2, ep + 1u);
+        // the flag carries the list length: (U << 16) | (epoch + 1) mod 2^16
+        st_release_gpu(p.bar + 2, ((unsigned)U << 16) | ((ep + 1u) & 0xffffu));
         stamp_here(p.ts, 5);
     }
     return true;
@@ -1015,10 +1035,12 @@ __device__ void await_selection(const FusedParams& p, Ctl& ctl, int b, int nb, i
     const int lane = threadIdx.x & 31;
     const unsigned below = (1u << lane) - 1u;
     bool ok = true;
+    unsigned flag = 0;
     if (lane == 0) {
         uint64_t t0 = 0;
         for (uint32_t it = 1;; ++it) {
-            if (ld_acquire_gpu(p.bar + 2) == ep + 1u) break;
+            flag = ld_acquire_gpu(p.bar + 2);
+            if ((flag & 0xffffu) == ((ep + 1u) & 0xffffu)) break;
             if ((it & 15u) == 0) {
                 if (*reinterpret_cast<volatile int*>(&ctl.abort)) {
                     ok = false;
@@ -1037,17 +1059,7 @@ __device__ void await_selection(const FusedParams& p, Ctl& ctl, int b, int nb, i
     }
     __syncwarp();
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-    for (int t = lane; t <= nb; t += 32) ctl.upre[t] = __ldcg(p.upre + t);
-    const int selb = __ldcg(p.selc + b);
-    __syncwarp();
-    for (int j = lane; j < m; j += 32) {
-        ctl.conf[j] = j < selb ? 1 : 0;
-        // a dropped speculative item may already be in y: pass B will read its
-        // W_down^T row again to take it out, so bring the row into L2 now
-        if (j >= selb)
-            prefetch_l2(p.down_t + (size_t)ctl.item[j] * p.d, (uint32_t)(2 * p.d));
-    }
-    const int U = ctl.upre[nb];
+    const int U = (int)(__shfl_sync(0xffffffffu, flag, 0) >> 16);
     const int q0 = chunk_begin(U, b, nb), q1 = chunk_begin(U, b + 1, nb);
     if (m + (q1 - q0) > kMaxItems) {
         if (lane == 0) {
@@ -1056,11 +1068,17 @@ __device__ void await_selection(const FusedParams& p, Ctl& ctl, int b, int nb, i
         }
         return;
     }
+    const int selb = __ldcg(p.selc + b);
     for (int q = q0 + lane; q < q1; q += 32) {
-        const int c = chunk_of(ctl.upre, nb, q);
-        ctl.item[m + q - q0] =
-            __ldcg(p.schan + chunk_begin(p.F, c, nb) + chunk_spec(p, c, nb) + (q - ctl.upre[c]));
+        ctl.item[m + q - q0] = __ldcg(p.ulist + q);
         ctl.conf[m + q - q0] = 1;
+    }
+    for (int j = lane; j < m; j += 32) {
+        ctl.conf[j] = j < selb ? 1 : 0;
+        // a dropped speculative item may already be in y: pass B will read its
+        // W_down^T row again to take it out, so bring the row into L2 now
+        if (j >= selb)
+            prefetch_l2(p.down_t + (size_t)ctl.item[j] * p.d, (uint32_t)(2 * p.d));
     }
     if (p.debug) {
         int pos = __ldcg(p.selpre + b);
@@ -1351,7 +1369,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     stamp(p.ts, 3);
 
     // ------------------------------------------------ P2: scores + histogram
-    const int cb0 = chunk_begin(F, b, nb), cb1 = chunk_begin(F, b + 1, nb);
+    const int cb0 = chunk_lo(F, b, nb), cb1 = chunk_lo(F, b + 1, nb);
     const int nch = cb1 - cb0;  // <= kMaxChunk (checked by the host)
     const int m = b == 0 ? 0 : spec_count(p.k, nch, F);  // CTA 0 selects instead
     {
@@ -1417,12 +1435,14 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         if (i < nch && part == 0) {
             ctl.lrank[i] = (uint16_t)rank;
             p.skey[cb0 + rank] = mine;
-            p.schan[cb0 + rank] = cb0 + i;
+            p.sidx[cb0 + rank] = (uint8_t)i;
             if (rank < m) ctl.item[rank] = cb0 + i;
         }
     }
     __syncthreads();
-    if (tid == 0) red_add_release_gpu(p.bar, 1u);  // barrier 2: histogram and sorted chunk out
+    // this chunk's histogram counts and sorted list are out (CTA 0 waits for
+    // every chunk's flag); the test hook makes the last CTA withhold its flag
+    if (tid == 0 && !(p.inject == 1 && b == nb - 1)) st_release_gpu(p.ready + b, ep + 1u);
     stamp(p.ts, 4);
 
     // ------------------------------------------------ P3: selection + stage 2
@@ -1572,8 +1592,13 @@ bool fused_fits(int d, int F) {
     (void)F;
     const size_t p01 = (size_t)6 * d + 4096 + (size_t)16 * kRing * kNT;
     const Ring r = ring_for(d);
-    return p01 <= area_budget() && ring_bytes(d, r) <= area_budget() && r.n_gu >= 1 &&
-           r.n_d >= 1 && d / 8 <= kXGroups * kNT;
+    // the channel selection (CTA 0): x, three digit histograms, the sorted
+    // keys and chunk-local indices of every chunk, per-chunk tables, candidates
+    const size_t sel = (size_t)2 * d + (size_t)4 * (2 * kHistBins + 512) +
+                       (size_t)5 * padded_ff(F) + (size_t)4 * (11 * kMaxBlocks + 4) +
+                       (size_t)4 * kCandCap;
+    return p01 <= area_budget() && ring_bytes(d, r) <= area_budget() && sel <= area_budget() &&
+           r.n_gu >= 1 && r.n_d >= 1 && d / 8 <= kXGroups * kNT;
 }
 
 namespace {
@@ -1607,10 +1632,11 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     p.hist = L.ws->hist;
     p.part = L.ws->part;
     p.skey = L.ws->skey;
-    p.schan = L.ws->schan;
+    p.sidx = L.ws->sidx;
     p.selc = L.ws->selc;
-    p.upre = L.ws->upre;
     p.selpre = L.ws->selpre;
+    p.ulist = L.ws->ulist;
+    p.ready = L.ws->ready;
     p.idx_list = L.ws->idx_list;
     p.hch = L.ws->hch;
     p.kept_out = L.kept_out;

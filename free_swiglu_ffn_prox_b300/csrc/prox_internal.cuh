@@ -23,20 +23,23 @@ inline int padded_ff(int d_ff) { return (d_ff + kChanAlign - 1) / kChanAlign * k
 constexpr int kMaxSlices = 16;   // proxy row slices (partial sums per channel)
 constexpr int kHistWords = 2048; // score histogram (top 11 bits of the bit pattern)
 constexpr int kMaxGrid = 256;    // CTAs of the fused kernel (one per SM)
+constexpr size_t kControlBytes = 2048;
 
-// Workspace carve-out (offsets in bytes, each 256-aligned).  The first 256
-// bytes are the control block: status word, then (at +128) the grid barrier
-// count, the call epoch and the channel-selection result.
+// Workspace carve-out (offsets in bytes, each 256-aligned).  The first
+// kControlBytes are the control block: status word, then (at +128) the grid
+// barrier count, the call epoch and the channel-selection result flag, then
+// (at +1024) the per-chunk ready flags; a fault clears the whole block.
 struct Workspace {
     int* status;        // [0] device status word (0 = ok)
     unsigned* bar;      // grid barrier count; bar[1] call epoch; bar[2..5] selection result
     uint32_t* hist;     // [kHistWords] score histogram, zeroed by each call
     float2* part;       // [kMaxSlices][Fp] per-slice proxy partials (g~, u~)
     uint32_t* skey;     // [Fp] per chunk: its score bits sorted descending
-    int* schan;         // [Fp] per chunk: the channels in that order
+    uint8_t* sidx;      // [Fp] per chunk: the chunk-local channel indices in that order
     int* selc;          // [kMaxGrid] per chunk: selected channels
-    int* upre;          // [kMaxGrid + 1] prefix of the per-chunk handed-out counts
     int* selpre;        // [kMaxGrid] debug: prefix of selc
+    int* ulist;         // [Fp] the channels handed out by the selection
+    unsigned* ready;    // [kMaxGrid] per-chunk ready flags (in the control block)
     int* idx_list;      // [Fp] debug: selected channels, ascending
     float* hch;         // [Fp] debug: h per channel
     uint16_t* x_stage;  // [d] bf16 input staged from host memory (prox_ffn_host)

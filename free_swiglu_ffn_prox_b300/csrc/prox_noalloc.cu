@@ -66,10 +66,11 @@ extern "C" PROX_API prox_status prox_ffn_noalloc(const prox_layer* layer, const 
     void* base = nullptr;
     if (prox::scratch_address(dev, &base) != cudaSuccess) return PROX_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents: restart the grid-barrier
-    // count and epoch (the first 256 bytes) from zero.  The histogram is
-    // cleared by the kernel; partials and scores are overwritten.
-    if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return PROX_ERR_CUDA;
+    // The array keeps the previous call's contents: restart the control block
+    // (grid-barrier count, epoch, selection and chunk flags) from zero.  The
+    // histogram is cleared by the kernel; everything else is overwritten
+    // before it is read.
+    if (cudaMemsetAsync(base, 0, prox::kControlBytes, s) != cudaSuccess) return PROX_ERR_CUDA;
     prox::Workspace ws = prox::carve_workspace(base, layer->d_model, layer->d_ff);
     ws.status = layer->ws.status;  // faults stay visible to prox_get_status(layer)
     prox::FusedLaunch f;
