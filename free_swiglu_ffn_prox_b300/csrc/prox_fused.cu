@@ -51,6 +51,8 @@ constexpr int kGuProducerWarp = 16;
 constexpr int kDProducerWarp = 17;
 constexpr int kSelectorWarp = 18;
 constexpr int kMaxStages = 16;
+constexpr size_t kGuRingBytes = 112 * 1024; // gate|up bytes in flight per SM
+constexpr size_t kDRingBytes = 48 * 1024;   // W_down^T bytes in flight per SM
 constexpr int kMaxItems = 512;            // Stage-2 items per CTA
 constexpr int kMaxChunk = 256;            // channels per CTA chunk
 constexpr int kMaxBlocks = kMaxGrid;
@@ -81,7 +83,8 @@ struct Ctl {
     uint64_t done_bar;               // every warp is through its Stage-2 role
     uint64_t ld_bar;                 // bulk load of the proxy scales (P1)
     uint64_t sel_ld;                 // bulk load of the digit-1 histogram (CTA 0)
-    uint64_t key_ld;                 // bulk loads of the sorted chunk lists (CTA 0)
+    uint64_t key_ld;                 // bulk load of the sorted chunk keys (CTA 0)
+    uint64_t idx_ld;                 // bulk load of the chunk-local indices (CTA 0)
     int gu_last[kMaxStages], d_last[kMaxStages];
     float h[kMaxItems];              // h of each item
     int item[kMaxItems];             // channel of each item
@@ -904,11 +907,12 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
         const uint64_t pol = policy_evict_first();
         mbar_arrive_expect_tx(&ctl.sel_ld, (uint32_t)(kHistBins * 4));
         bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.sel_ld, pol);
-        mbar_arrive_expect_tx(&ctl.key_ld, (uint32_t)(Fp * 5));
+        mbar_arrive_expect_tx(&ctl.key_ld, (uint32_t)(Fp * 4));
         bulk_g2s(sk, p.skey, (uint32_t)(Fp * 4), &ctl.key_ld, pol);
-        bulk_g2s(sidx, p.sidx, (uint32_t)Fp, &ctl.key_ld, pol);
+        mbar_arrive_expect_tx(&ctl.idx_ld, (uint32_t)Fp);
+        bulk_g2s(sidx, p.sidx, (uint32_t)Fp, &ctl.idx_ld, pol);
     }
-    // waits for one of the two staging copies; after a timeout lets both land
+    // waits for one of the three staging copies; after a timeout lets all land
     auto landed = [&](uint64_t* bar) {
         if (!mbar_wait_bounded(bar, 0, p.limit_ns, &ctl.abort) && lane == 0) {
             ctl.abort = 1;
@@ -919,6 +923,7 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
         if (tid == 0) {
             mbar_wait_bounded(&ctl.sel_ld, 0, p.limit_ns, nullptr);
             mbar_wait_bounded(&ctl.key_ld, 0, p.limit_ns, nullptr);
+            mbar_wait_bounded(&ctl.idx_ld, 0, p.limit_ns, nullptr);
         }
         return false;
     };
@@ -1010,6 +1015,7 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
     __syncthreads();
     // the handed-out list: per chunk, in chunk order, its selected channels of
     // rank >= its speculative count
+    if (!landed(&ctl.idx_ld)) return false;
     const int U = upre[nb];
     for (int q = tid; q < U; q += kNT) {
         const int c = chunk_of(upre, nb, q);
@@ -1412,6 +1418,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         stage2_init(ctl, p.n_gu, p.n_d);
         mbar_init(&ctl.sel_ld, 1);
         mbar_init(&ctl.key_ld, 1);
+        mbar_init(&ctl.idx_ld, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -1514,19 +1521,22 @@ struct Ring {
 
 size_t area_budget() { return kSmemLimit - ctl_bytes(); }
 
-// Stage-2 rings after x (2 d bytes): up to kPassAWarps gate|up stages (4 d
-// each, at most two thirds of the room) and as many W_down^T stages (2 d)
-// as fit in the rest.
+// Stage-2 rings after x (2 d bytes): gate|up stages (4 d bytes each) up to
+// kGuRingBytes and kPassAWarps stages, W_down^T stages (2 d bytes each) up to
+// kDRingBytes, both within the shared memory left.  The caps keep ~160 KB in
+// flight per SM: enough to saturate HBM, and every extra byte in flight only
+// lengthens the queues that the channel selection's loads wait in.
 Ring ring_for(int d) {
     const size_t budget = area_budget() - (size_t)2 * d;
     const size_t gu = (size_t)4 * d, dd = (size_t)2 * d;
     Ring r{0, 0};
-    r.n_gu = (int)((budget * 2 / 3) / gu);
+    r.n_gu = (int)(min(budget * 2 / 3, kGuRingBytes) / gu);
     if (r.n_gu > kPassAWarps) r.n_gu = kPassAWarps;
     if (r.n_gu < 1) r.n_gu = 1;
     const size_t left = budget > (size_t)r.n_gu * gu ? budget - (size_t)r.n_gu * gu : 0;
-    r.n_d = (int)(left / dd);
+    r.n_d = (int)(min(left, kDRingBytes) / dd);
     if (r.n_d > kMaxStages) r.n_d = kMaxStages;
+    if (r.n_d < 1 && left >= dd) r.n_d = 1;
     return r;
 }
 
