@@ -8,31 +8,35 @@
 //   P1  proxy GEMV (Stage 1): CTA (tile, slice) streams the int4 proxy rows
 //       of its slice of the kept inputs, restricted to its channel tile, with
 //       128-bit loads, and writes per-slice partial (g~, u~) sums.
-//   --- grid barrier 1
-//   P2  CTA b owns the channel chunk [F b / n, F (b+1) / n): sums the slices
-//       in a fixed order (deterministic scores), forms |silu(g~) u~|, adds
-//       the chunk to a global histogram of the scores' top 11 bits and ranks
-//       the chunk's channels locally.
+//   --- grid barrier
+//   P2  CTA b owns the channel chunk [cb0, cb1) (chunk starts on multiples of
+//       4 channels, ~F/n wide): sums the slices in a fixed order
+//       (deterministic scores), forms |silu(g~) u~|, adds the chunk to a
+//       global histogram of the scores' top 11 bits, ranks the chunk, publishes
+//       it sorted (score keys and chunk-local channel bytes) and raises its
+//       epoch-tagged ready flag.
 //   P3  Stage 2 (Eq. (1) of the PrunePath page restricted to the mask) and
 //       the exact channel top-k run side by side:
 //       - the items of CTA b > 0 start with the top m channels of its own
-//         chunk, m = the chunk's expected share k nch / F of the mask; these are
-//         in the mask with high probability, so their rows stream at once;
-//       - CTA 0 alone waits for every chunk (grid barrier 2), stages all
-//         scores in shared memory and finds the exact top-k (three radix
-//         digits, ties to the lower channel); it lists, in channel order,
-//         every selected channel that its owner will not confirm on its own
-//         and publishes the threshold and the list behind a flag;
-//       - the other CTAs' selector warp polls that flag, confirms or drops
-//         the speculative items (by the threshold) and appends the CTA's
-//         even share of the list to its items;
+//         chunk, m = the chunk's expected share k nch / F of the mask; most
+//         are in the mask, so their rows stream at once;
+//       - CTA 0 alone waits for every chunk's flag, stages the histogram and
+//         the sorted chunks in shared memory and finds the exact k-th score
+//         (three radix digits over the candidates, ties to the lower
+//         channel); per chunk it publishes how many channels are selected (a
+//         prefix of the chunk's sorted list) and writes the list of selected
+//         channels that no owner speculated on; one flag word carries the
+//         list length and the call epoch;
+//       - every CTA's selector warp then confirms its speculative items by
+//         rank and reads an even share of that list;
 //       - gate|up rows and W_down^T rows arrive by bulk copies (TMA) into two
-//         shared-memory rings; pass-A warps form h = silu(W_gate x) (W_up x)
-//         per item (one warp per row), pass-B warps own slices of d_model and
-//         accumulate h * W_down^T for the confirmed items; one vector atomic
-//         per element adds the CTA's part of y at the end.
-//       A speculative item that the exact mask drops costs bandwidth only:
-//       pass B skips it.
+//         shared-memory rings (bytes in flight capped); pass-A warps form
+//         h = silu(W_gate x) (W_up x) per item (one warp per row), pass-B
+//         warps own slices of d_model and accumulate h * W_down^T,
+//         speculative items included before the mask is known (a dropped one
+//         is subtracted again at the end); one vector atomic per element adds
+//         the CTA's part of y at the end.
+//       A speculative item that the exact mask drops costs bandwidth only.
 //
 // The same Stage-2 code over all channels is the dense baseline (k_dense).
 // Every wait is bounded: a wait that runs out records PROX_ERR_TIMEOUT in
@@ -137,7 +141,7 @@ struct FusedParams {
     // stage-2 ring geometry
     int n_gu, n_d;
     long long limit_ns;
-    int inject;          // 1: the last CTA skips the first grid barrier (test hook)
+    int inject;          // 1: the last CTA withholds its grid-barrier arrival (test hook)
     uint64_t* ts;        // [gridDim][kPhaseStamps] %globaltimer stamps, or null
 };
 

@@ -179,7 +179,7 @@ PROX_API int prox_layer_blocks(const prox_layer* layer);
  * stamps[b * PROX_PHASE_STAMPS + i] (uint64, device, prox_layer_blocks()
  * rows, zeroed first; a phase the kernel does not have stays 0):
  *   0 start; 1 input selection done; 2 proxy partials written;
- *   3 past the first grid barrier; 4 scores, histogram and local ranks done
+ *   3 past the grid barrier; 4 scores, histogram and local ranks done
  *   (Stage 2 starts on the speculative channels); 5 exact channel mask
  *   known (this CTA's item list final); 6 first gate|up row landed;
  *   7 gate|up dot products done; 8 W_down^T accumulation done; 9 end.
@@ -256,7 +256,7 @@ PROX_API prox_status prox_get_status(const prox_layer* layer, prox_stream_t stre
 
 /*
  * Failure-detection test hook (not for production use): runs one decode
- * step in which one CTA withholds its arrival at the first grid barrier and
+ * step in which one CTA withholds its arrival at the grid barrier and
  * every bounded wait gives up after 20 ms, then synchronises and returns
  * the layer's status, which is PROX_ERR_TIMEOUT when the bounded waits work
  * (the status and barrier words are reset as by prox_get_status).  y is
