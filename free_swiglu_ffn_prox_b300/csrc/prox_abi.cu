@@ -85,7 +85,9 @@ cudaError_t record(cudaEvent_t ev, cudaStream_t stream) {
 prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, float input_keep,
                      float* y, int32_t* kept_out, float* scores_out, int32_t* idx_out,
                      float* h_out, cudaStream_t stream, long long limit_ns, int inject,
-                     cudaEvent_t const* ev = nullptr, uint64_t* ts = nullptr) {
+                     cudaEvent_t const* ev = nullptr, uint64_t* ts = nullptr,
+                     const void* x_prev = nullptr, const float* y_prev = nullptr,
+                     void* x_out = nullptr, float eps = 0.0f) {
     prox::FusedLaunch f;
     f.codes = L->codes;
     f.scales = L->scales;
@@ -106,10 +108,20 @@ prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, fl
     f.limit_ns = limit_ns;
     f.inject = inject;
     f.ts = ts;
+    f.x_prev = static_cast<const uint16_t*>(x_prev);
+    f.y_prev = y_prev;
+    f.x_out = static_cast<uint16_t*>(x_out);
+    f.eps = eps;
     cudaError_t e = ev ? record(ev[0], stream) : cudaSuccess;
     if (e == cudaSuccess) e = prox::launch_fused(f, stream);
     if (e == cudaSuccess && ev) e = record(ev[1], stream);
     return cuda_status(e);
+}
+
+// Whether the byte ranges [a, a + na) and [b, b + nb) overlap.
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
 }
 
 prox_status check_call(const prox_layer* L, const void* x, const float* y) {
@@ -247,6 +259,24 @@ prox_status prox_ffn_traced(const prox_layer* layer, const void* x, float keep_f
     return run_prox(layer, x, keep_fraction, input_keep, y, nullptr, nullptr, nullptr, nullptr,
                     reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0,
                     reinterpret_cast<cudaEvent_t const*>(events));
+}
+
+prox_status prox_ffn_resnorm(const prox_layer* layer, const void* x_prev, const float* y_prev,
+                             float eps, void* x_out, float keep_fraction, float* y,
+                             prox_stream_t stream) {
+    if (!layer || !x_prev || !y_prev || !x_out || !y) return PROX_ERR_INVALID_ARG;
+    if (!aligned16(x_prev) || !aligned16(y_prev) || !aligned16(x_out) || !aligned16(y))
+        return PROX_ERR_MISALIGNED;
+    if (!frac_ok(keep_fraction) || !(eps >= 0.0f) || !isfinite(eps)) return PROX_ERR_INVALID_ARG;
+    const size_t d = (size_t)layer->d_model;
+    // every CTA reads x_prev and y_prev while CTA 0 writes x_out and clears y
+    if (overlap(x_out, 2 * d, x_prev, 2 * d) || overlap(x_out, 2 * d, y_prev, 4 * d) ||
+        overlap(x_out, 2 * d, y, 4 * d) || overlap(y, 4 * d, y_prev, 4 * d) ||
+        overlap(y, 4 * d, x_prev, 2 * d))
+        return PROX_ERR_INVALID_ARG;
+    return run_prox(layer, nullptr, keep_fraction, 0.5f, y, nullptr, nullptr, nullptr, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0, nullptr,
+                    nullptr, x_prev, y_prev, x_out, eps);
 }
 
 prox_status prox_dense_ffn(const prox_layer* layer, const void* x, float* y,

@@ -117,6 +117,11 @@ struct FusedParams {
     const uint16_t* x;
     float* y;
     int kx, k;
+    // optional stack glue in front of the step: x = bf16(RMSNorm(x_prev + y_prev))
+    const uint16_t* x_prev;  // null: x is given
+    const float* y_prev;
+    uint16_t* x_out;         // the normalised x, written by CTA 0 (may be null)
+    float eps;
     // proxy geometry
     int tiles, slices, tile_w;
     // workspace
@@ -1137,11 +1142,57 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     {
         const int ng = d / 8, G = (ng + kNT - 1) / kNT, g0 = tid * G;  // G <= kXGroups
         uint4 xv[kXGroups];
-#pragma unroll
-        for (int q = 0; q < kXGroups; ++q)
-            xv[q] = (q < G && g0 + q < ng) ? __ldg(reinterpret_cast<const uint4*>(p.x) + g0 + q)
-                                           : make_uint4(0u, 0u, 0u, 0u);
         auto valid = [&](int q) { return q < G && g0 + q < ng; };
+        if (p.x_prev == nullptr) {
+#pragma unroll
+            for (int q = 0; q < kXGroups; ++q)
+                xv[q] = valid(q) ? __ldg(reinterpret_cast<const uint4*>(p.x) + g0 + q)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            // stack glue: z = x_prev + y_prev, x = bf16_rne(z / sqrt(mean(z^2) + eps)).
+            // Every CTA sums z^2 in the same fixed order (thread-local, warp
+            // butterfly, then the warps in order), so all CTAs get the same x.
+            float z[kXGroups][8];
+            float ss = 0.0f;
+#pragma unroll
+            for (int q = 0; q < kXGroups; ++q) {
+                uint4 xb = make_uint4(0u, 0u, 0u, 0u);
+                float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+                if (valid(q)) {
+                    xb = __ldg(reinterpret_cast<const uint4*>(p.x_prev) + g0 + q);
+                    y0 = __ldg(reinterpret_cast<const float4*>(p.y_prev) + 2 * (g0 + q));
+                    y1 = __ldg(reinterpret_cast<const float4*>(p.y_prev) + 2 * (g0 + q) + 1);
+                }
+                const uint32_t w[4] = {xb.x, xb.y, xb.z, xb.w};
+                const float yy[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t hb = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xffffu);
+                    z[q][e] = __uint_as_float(hb << 16) + yy[e];
+                    ss = fmaf(z[q][e], z[q][e], ss);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (lane == 0) ctl.warp_tot[wid] = __float_as_uint(ss);
+            __syncthreads();
+            float tot = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kNT / 32; ++w) tot += __uint_as_float(ctl.warp_tot[w]);
+            const float inv = 1.0f / sqrtf(tot / (float)d + p.eps);
+#pragma unroll
+            for (int q = 0; q < kXGroups; ++q) {
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    o[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(z[q][2 * e] * inv)) |
+                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(z[q][2 * e + 1] * inv)) << 16);
+                xv[q] = make_uint4(o[0], o[1], o[2], o[3]);
+                if (valid(q) && b == 0 && p.x_out)
+                    reinterpret_cast<uint4*>(p.x_out)[g0 + q] = xv[q];
+            }
+            __syncthreads();  // ctl.warp_tot is reused below
+        }
         auto half = [&](const uint4& v, int e) {
             const uint32_t w = e < 2 ? v.x : e < 4 ? v.y : e < 6 ? v.z : v.w;
             return (e & 1) ? (w >> 16) : (w & 0xffffu);
@@ -1636,6 +1687,10 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     p.y = L.y;
     p.kx = L.kx;
     p.k = L.k;
+    p.x_prev = L.x_prev;
+    p.y_prev = L.y_prev;
+    p.x_out = L.x_out;
+    p.eps = L.eps;
     const ProxyGeom geo = proxy_geometry(L.F, L.kx, L.num_blocks);
     p.tiles = geo.tiles;
     p.slices = geo.slices;

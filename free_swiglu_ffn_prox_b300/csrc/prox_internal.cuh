@@ -182,6 +182,12 @@ struct FusedLaunch {
     const uint16_t* x;
     float* y;
     int kx, k;
+    // optional stack glue: x = bf16(RMSNorm(x_prev + y_prev)) computed in the
+    // step itself (x unused, x_out receives it); x_prev null: plain step
+    const uint16_t* x_prev = nullptr;
+    const float* y_prev = nullptr;
+    uint16_t* x_out = nullptr;
+    float eps = 0.0f;
     const Workspace* ws;
     int32_t* kept_out;   // debug outputs, may be null
     float* scores_out;

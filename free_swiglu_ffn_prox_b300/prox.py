@@ -65,6 +65,7 @@ def _load():
             "prox_dense_ffn": (i32, [vp, vp, vp, vp]),
             "prox_ffn_debug": (i32, [vp, vp, f32, f32, vp, vp, vp, vp, vp, vp]),
             "prox_residual_rmsnorm": (i32, [i32, vp, vp, f32, vp, vp]),
+            "prox_ffn_resnorm": (i32, [vp, vp, vp, f32, vp, f32, vp, vp]),
             "prox_get_status": (i32, [vp, vp]),
             "prox_test_barrier_timeout": (i32, [vp, vp, vp, vp]),
             "prox_layer_blocks": (i32, [vp]),
@@ -288,6 +289,26 @@ def prox_residual_rmsnorm(x: torch.Tensor, y: torch.Tensor, eps: float = 1e-6, o
     _check(_load().prox_residual_rmsnorm(d, _ptr(x), _ptr(y), float(eps), _ptr(out),
                                          _stream(stream)), "prox_residual_rmsnorm")
     return out
+
+
+def prox_ffn_resnorm(layer: ProxLayer, x_prev: torch.Tensor, y_prev: torch.Tensor,
+                     keep_fraction: float, eps: float = 1e-6, x_out=None, y=None, stream=None):
+    """One stacked layer with the residual + RMSNorm glue fused into the step:
+    x = bf16(RMSNorm(x_prev + y_prev)) (written to x_out), y = the step on x.
+    Returns (x_out, y)."""
+    d = layer.d_model
+    _need(x_prev, torch.bfloat16, (d,), "x_prev")
+    _need(y_prev, torch.float32, (d,), "y_prev")
+    if x_out is None:
+        x_out = torch.empty(d, dtype=torch.bfloat16, device=x_prev.device)
+    if y is None:
+        y = torch.empty(d, dtype=torch.float32, device=x_prev.device)
+    _need(x_out, torch.bfloat16, (d,), "x_out")
+    _need(y, torch.float32, (d,), "y")
+    _check(_load().prox_ffn_resnorm(layer.handle, _ptr(x_prev), _ptr(y_prev), float(eps),
+                                    _ptr(x_out), float(keep_fraction), _ptr(y), _stream(stream)),
+           "prox_ffn_resnorm")
+    return x_out, y
 
 
 def prox_get_status(layer: ProxLayer, stream=None) -> int:

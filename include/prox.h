@@ -218,6 +218,22 @@ PROX_API prox_status prox_residual_rmsnorm(int d_model, const void* x, const flo
                                   void* x_next, prox_stream_t stream);
 
 /*
+ * One layer of a stack with the glue fused into the step (the pages define
+ * no glue; plain reading of a residual stream, as prox_residual_rmsnorm):
+ * x = bf16_rne(z / sqrt(mean(z^2) + eps)) with z = x_prev + y_prev, then
+ * y = prox_ffn(layer, x, keep_fraction).  Every CTA of the step computes x
+ * itself (in the same order, so all agree); x is also written to x_out for
+ * the next layer's residual.  Saves the separate glue launch per layer.
+ *   x_prev bf16 [d_model], y_prev fp32 [d_model] (the previous layer's input
+ *   and output), x_out bf16 [d_model], y fp32 [d_model]; all device, 16-byte
+ *   aligned.  x_out and y must not overlap x_prev, y_prev or each other
+ *   (PROX_ERR_INVALID_ARG).  Same status and ordering rules as prox_ffn.
+ */
+PROX_API prox_status prox_ffn_resnorm(const prox_layer* layer, const void* x_prev,
+                                      const float* y_prev, float eps, void* x_out,
+                                      float keep_fraction, float* y, prox_stream_t stream);
+
+/*
  * prox_ffn without any caller-provided scratch (the pages have no
  * counterpart: this is a deployment variant).  For callers that cannot
  * allocate device memory when they run a step -- a host framework or server

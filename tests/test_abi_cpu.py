@@ -111,4 +111,6 @@ def test_bad_arguments_are_rejected_before_any_device_work(lib):
     assert lib.prox_residual_rmsnorm(256, None, good[1], ctypes.c_float(1e-6), good[2], None) == 1
     assert lib.prox_residual_rmsnorm(256, good[0], good[1], ctypes.c_float(-1.0), good[2], None) == 1
     assert lib.prox_residual_rmsnorm(256, vp(0x10002), good[1], ctypes.c_float(1e-6), good[2], None) == 3
+    f = ctypes.c_float
+    assert lib.prox_ffn_resnorm(None, good[0], good[1], f(1e-6), good[2], f(0.3), good[3], None) == 1
     lib.prox_destroy(None)  # accepted, no-op

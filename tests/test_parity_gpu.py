@@ -328,3 +328,35 @@ def test_short_stack_matches_oracle_layer_by_layer(prox):
         assert _bf16_ulp_diff(host_bits(x_next), ref).max() <= 1.0
         assert torch.allclose(y, r["y"], rtol=0, atol=1e-5 * float(y.abs().max()))
         x = x_next
+
+
+def test_fused_stack_glue_matches_the_separate_glue_and_the_oracle(prox):
+    """prox_ffn_resnorm computes x = bf16(RMSNorm(x_prev + y_prev)) inside the
+    step: x_out is the oracle's glue to within one bf16 ulp (in every CTA the
+    same value: the mask and y then match the oracle as for prox_ffn), and the
+    step on it matches the oracle layer by layer."""
+    d, F = 1024, 2816
+    L0, _ = _layer(prox, d, F, seed=1200)
+    x = _x(d, 10, seed=72).cuda()
+    y = prox.prox_ffn(L0, x, 0.3)
+    torch.cuda.synchronize()
+    for l in range(1, 4):
+        L, w = _layer(prox, d, F, seed=1200 + l)
+        x_out, y_next = prox.prox_ffn_resnorm(L, x, y, 0.3)
+        torch.cuda.synchronize()
+        assert prox.prox_get_status(L) == 0
+        ref = oracle.residual_rmsnorm(host_bits(x), y.cpu().double().numpy())
+        assert _bf16_ulp_diff(host_bits(x_out), ref).max() <= 1.0
+        sep = prox.prox_residual_rmsnorm(x, y)
+        torch.cuda.synchronize()
+        assert _bf16_ulp_diff(host_bits(x_out), host_bits(sep)).max() <= 1.0
+        r = _check_step(prox, L, w, x_out.cpu(), 0.3)
+        assert torch.allclose(y_next, r["y"], rtol=0, atol=1e-5 * float(y_next.abs().max()))
+        x, y = x_out, y_next
+    # outputs may not overlap the inputs (CTA 0 writes them while all CTAs read)
+    with pytest.raises(prox.ProxError) as e:
+        prox.prox_ffn_resnorm(L, x, y, 0.3, x_out=x)
+    assert e.value.code == prox.PROX_ERR_INVALID_ARG
+    with pytest.raises(prox.ProxError) as e:
+        prox.prox_ffn_resnorm(L, x, y, 0.3, y=y)
+    assert e.value.code == prox.PROX_ERR_INVALID_ARG
