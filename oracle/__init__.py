@@ -74,9 +74,12 @@ def _load():
             lib.oracle_dense_ffn.argtypes = [_i32, _i32] + [_ptr] * 6
             lib.oracle_prox_ffn.argtypes = [_i32, _i32] + [_ptr] * 8 + [_i32, _i32] + [_ptr] * 5
             lib.oracle_residual_rmsnorm.argtypes = [_i32, _ptr, _ptr, ctypes.c_double, _ptr]
+            lib.oracle_quantize_rows_q8.argtypes = [_i32, _i32, _ptr, _ptr, _ptr]
+            lib.oracle_sparse_ffn_q8.argtypes = [_i32, _i32] + [_ptr] * 7 + [_i32, _ptr, _ptr, _ptr]
             for name in ("oracle_quantize", "oracle_input_topk", "oracle_proxy_scores",
                          "oracle_channel_topk", "oracle_sparse_ffn", "oracle_dense_ffn",
-                         "oracle_prox_ffn", "oracle_residual_rmsnorm"):
+                         "oracle_prox_ffn", "oracle_residual_rmsnorm", "oracle_quantize_rows_q8",
+                         "oracle_sparse_ffn_q8"):
                 getattr(lib, name).restype = _i32
             _lib = lib
     return _lib
@@ -248,3 +251,40 @@ def residual_rmsnorm(x_bits, y, eps: float = 1e-6) -> np.ndarray:
     _check(lib.oracle_residual_rmsnorm(x.size, _p(x), _p(yy), float(eps), _p(out)),
            "residual_rmsnorm")
     return out
+
+
+# ---------------------------------------------------------------- int8 Stage 2
+def quantize_rows_q8(w_bits):
+    """Per-row symmetric int8 of a [rows][n] bf16 matrix (reading of "compatible
+    with quantization", Prox Abstract): returns (q int8 [rows][n], s float32 [rows])."""
+    lib = _load()
+    w = _c(w_bits, np.uint16)
+    rows, n = w.shape
+    q = np.empty((rows, n), dtype=np.int8)
+    s = np.empty(rows, dtype=np.float32)
+    _check(lib.oracle_quantize_rows_q8(rows, n, _p(w), _p(q), _p(s)), "quantize_rows_q8")
+    return q, s
+
+
+def stage2_q8(w_gate, w_up, w_down):
+    """int8 Stage-2 weights: rows of W_gate and W_up, rows of W_down^T."""
+    qg, sg = quantize_rows_q8(w_gate)
+    qu, su = quantize_rows_q8(w_up)
+    qd, sd = quantize_rows_q8(np.ascontiguousarray(np.asarray(w_down).T))
+    return {"q_gate": qg, "s_gate": sg, "q_up": qu, "s_up": su, "q_down": qd, "s_down": sd}
+
+
+def sparse_ffn_q8(q8, x_bits, idx):
+    """Stage 2 with int8 weights on the channels idx: returns (h, y) in fp64."""
+    lib = _load()
+    x = _c(x_bits, np.uint16).ravel()
+    idx = _c(idx, np.int32).ravel()
+    F, d = q8["q_gate"].shape
+    h = np.empty(max(idx.size, 1), dtype=np.float64)
+    y = np.empty(d, dtype=np.float64)
+    arrs = [_c(q8[k], t) for k, t in (("q_gate", np.int8), ("s_gate", np.float32),
+                                      ("q_up", np.int8), ("s_up", np.float32),
+                                      ("q_down", np.int8), ("s_down", np.float32))]
+    _check(lib.oracle_sparse_ffn_q8(F, d, *[_p(a) for a in arrs], _p(x), idx.size, _p(idx),
+                                    _p(h), _p(y)), "sparse_ffn_q8")
+    return h[: idx.size], y

@@ -285,6 +285,71 @@ int oracle_sparse_ffn(int F, int d, const uint16_t* w_gate, const uint16_t* w_up
     return ORACLE_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Next row (int8 Stage-2 weights): [Prox] Abstract, the method is          */
+/* "compatible with quantization"; the scheme is a reading.                 */
+/* ------------------------------------------------------------------------ */
+/* Symmetric int8, one fp32 scale per row of a [rows][n] bf16 matrix:
+ *   amax = max_j |W[r][j]| (binary32, exact), s = fl32(amax / 127),
+ *   q_j  = clamp(rne(fl32(W[r][j] / s)), -127, 127), or 0 when s == 0.
+ * Stage 2 quantizes the rows of W_gate and W_up and the rows of W_down^T
+ * (the columns of W_down). */
+int oracle_quantize_rows_q8(int rows, int n, const uint16_t* W, int8_t* q, float* s) {
+    if (rows <= 0 || n <= 0 || !W || !q || !s) return ORACLE_BAD_ARG;
+    for (int r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int j = 0; j < n; ++j) {
+            float aw = fabsf((float)oracle_bf16_to_double(W[(size_t)r * n + j]));
+            if (aw > amax) amax = aw;
+        }
+        float sr = amax / 127.0f;                    /* binary32 division */
+        s[r] = sr;
+        for (int j = 0; j < n; ++j) {
+            int code = 0;
+            if (sr != 0.0f) {
+                float w = (float)oracle_bf16_to_double(W[(size_t)r * n + j]);
+                float t = rintf(w / sr);             /* binary32 division, ties to even */
+                if (t < -127.0f) t = -127.0f;
+                if (t > 127.0f) t = 127.0f;
+                code = (int)t;
+            }
+            q[(size_t)r * n + j] = (int8_t)code;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Stage 2 on int8 weights ([PP] Eq. (1) with the dequantized rows): for c in
+ * idx, g_c = s_gate[c] sum_j q_gate[c][j] x_j, u_c likewise,
+ * h_c = silu(g_c) u_c, y_i = sum_c h_c s_down[c] q_down[c][i], where
+ * q_down / s_down quantize the rows of W_down^T.  fp64, full bf16 x. */
+int oracle_sparse_ffn_q8(int F, int d, const int8_t* q_gate, const float* s_gate,
+                         const int8_t* q_up, const float* s_up, const int8_t* q_down,
+                         const float* s_down, const uint16_t* x, int k, const int32_t* idx,
+                         double* h, double* y) {
+    if (F <= 0 || d <= 0 || k < 0 || k > F || !q_gate || !s_gate || !q_up || !s_up ||
+        !q_down || !s_down || !x || !y || (k > 0 && !idx))
+        return ORACLE_BAD_ARG;
+    for (int i = 0; i < d; ++i) y[i] = 0.0;
+    for (int t = 0; t < k; ++t) {
+        int c = idx[t];
+        if (c < 0 || c >= F) return ORACLE_BAD_ARG;
+        double g = 0.0, u = 0.0;
+        for (int j = 0; j < d; ++j) {
+            double xj = oracle_bf16_to_double(x[j]);
+            g += (double)q_gate[(size_t)c * d + j] * xj;
+            u += (double)q_up[(size_t)c * d + j] * xj;
+        }
+        g *= (double)s_gate[c];
+        u *= (double)s_up[c];
+        double hc = silu(g) * u;
+        if (h) h[t] = hc;
+        double hs = hc * (double)s_down[c];
+        for (int i = 0; i < d; ++i) y[i] += hs * (double)q_down[(size_t)c * d + i];
+    }
+    return ORACLE_OK;
+}
+
 /* a6: the dense SwiGLU FFN, [PP] Eq. (1), written directly: the intermediate
  * state h over all channels, then the down projection row by row. */
 int oracle_dense_ffn(int F, int d, const uint16_t* w_gate, const uint16_t* w_up,

@@ -359,3 +359,88 @@ def test_residual_rmsnorm_closed_forms(oracle_mod):
     assert abs(rms - 1.0) < 5e-3
     z = oracle_mod.bf16_bits_to_f64(xb) + y
     assert np.all(np.sign(o1[np.abs(z) > 1e-3]) == np.sign(z[np.abs(z) > 1e-3]))
+
+
+# ---------------------------------------------------------------- int8 Stage 2
+def _exact_bf16_bits(v):
+    """bf16 bit patterns of float values that are exact in bf16."""
+    a = np.asarray(v, dtype=np.float32).view(np.uint32)
+    assert np.all(a & 0xFFFF == 0), "values must be exact in bf16"
+    return (a >> 16).astype(np.uint16)
+
+
+def test_q8_quantizer_invariants(oracle_mod):
+    """Per-row symmetric int8: |q| <= 127; the row's largest magnitude maps to
+    +-127; |w - s q| <= s/2 (plus the binary32 rounding of w/s); zero rows give q = 0,
+    s = 0; each row's scale is amax / 127 of that row alone."""
+    rng = np.random.default_rng(5)
+    w = (rng.standard_normal((37, 256)) * rng.uniform(0.001, 3.0, size=(37, 1))).astype(np.float32)
+    w[4] = 0.0
+    bits = oracle_mod.double_to_bf16(w)
+    q, s = oracle_mod.quantize_rows_q8(bits)
+    wf = oracle_mod.bf16_bits_to_f64(bits)
+    assert np.all(np.abs(q.astype(int)) <= 127)
+    assert np.all(q[4] == 0) and s[4] == 0.0
+    amax = np.abs(wf).max(axis=1)
+    for r in range(37):
+        if r == 4:
+            continue
+        assert s[r] == np.float32(np.float32(amax[r]) / np.float32(127.0))
+        j = int(np.argmax(np.abs(wf[r])))
+        assert abs(int(q[r, j])) == 127 and np.sign(q[r, j]) == np.sign(wf[r, j])
+        # w / s is rounded to binary32 before rint: |w/s| <= 127 moves it by
+        # at most 127 * 2^-24, so the midpoint can be crossed by that much
+        err = np.abs(wf[r] - float(s[r]) * q[r].astype(np.float64))
+        assert np.all(err <= float(s[r]) * (0.5 + 127 * 2.0 ** -24))
+
+
+def test_q8_stage2_reduces_to_bf16_stage2_on_exact_weights(oracle_mod):
+    """Weights w = 2^-6 q_true with integer |q_true| <= 127 and every row (and
+    W_down column) reaching 127 are exact in bf16 and quantize exactly (s =
+    2^-6), so the int8 Stage 2 equals the bf16 Stage 2 (an independent
+    function of the oracle) on any channel set."""
+    rng = np.random.default_rng(6)
+    F, d = 96, 128
+    def exact(rows, cols, col_major=False):
+        qt = rng.integers(-127, 128, size=(rows, cols))
+        if col_major:
+            qt[rng.integers(0, rows, size=cols), np.arange(cols)] = 127
+        else:
+            qt[np.arange(rows), rng.integers(0, cols, size=rows)] = -127
+        return qt, _exact_bf16_bits(qt.astype(np.float32) * np.float32(2.0 ** -6))
+    qg_t, wg = exact(F, d)
+    qu_t, wu = exact(F, d)
+    qd_t, wd = exact(d, F, col_major=True)   # W_down [d][F]: each column reaches 127
+    x = synth.bits(synth.make_x(d, 3, 20.0, 9))
+    q8 = oracle_mod.stage2_q8(wg, wu, wd)
+    assert np.array_equal(q8["q_gate"], qg_t) and np.array_equal(q8["q_up"], qu_t)
+    assert np.array_equal(q8["q_down"], qd_t.T)
+    assert np.all(q8["s_gate"] == np.float32(2.0 ** -6)) and np.all(q8["s_down"] == np.float32(2.0 ** -6))
+    idx = np.sort(rng.choice(F, size=40, replace=False)).astype(np.int32)
+    h8, y8 = oracle_mod.sparse_ffn_q8(q8, x, idx)
+    h, y = oracle_mod.sparse_ffn(wg, wu, wd, x, idx)
+    assert np.allclose(h8, h, rtol=1e-12, atol=1e-12 * np.abs(h).max())
+    assert np.allclose(y8, y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
+
+
+def test_q8_stage2_one_channel_closed_form(oracle_mod):
+    """One selected channel: y = silu(s_g q_g.x) (s_u q_u.x) s_d q_d, written
+    out for a tiny case with hand-set codes."""
+    d, F = 128, 2
+    q8 = {"q_gate": np.zeros((F, d), np.int8), "s_gate": np.array([0.5, 1.0], np.float32),
+          "q_up": np.zeros((F, d), np.int8), "s_up": np.array([0.25, 1.0], np.float32),
+          "q_down": np.zeros((F, d), np.int8), "s_down": np.array([2.0, 1.0], np.float32)}
+    q8["q_gate"][0, 3] = 4      # g = 0.5 * 4 * x3
+    q8["q_up"][0, 5] = -8       # u = 0.25 * -8 * x5
+    q8["q_down"][0, 7] = 3      # y7 = h * 2 * 3
+    q8["q_down"][1, 7] = 100    # channel 1 is not selected
+    xs = np.zeros(d, np.float32)
+    xs[3], xs[5] = 1.5, -2.0
+    x = _exact_bf16_bits(xs)
+    h, y = oracle_mod.sparse_ffn_q8(q8, x, np.array([0], np.int32))
+    g, u = 0.5 * 4 * 1.5, 0.25 * -8 * -2.0
+    hh = g / (1 + np.exp(-g)) * u
+    assert np.isclose(h[0], hh, rtol=1e-15)
+    expect = np.zeros(d)
+    expect[7] = hh * 2.0 * 3
+    assert np.allclose(y, expect, rtol=1e-15, atol=0)
