@@ -22,8 +22,10 @@ from CUDA events recorded between the kernels (prox_ffn_traced, captured the
 same way) and the roofline of the dominant kernel; the end-to-end number
 through the host-buffer entry point prox_ffn_host (x copied in and y copied
 out every step, inside the timed region); latency and GB/s at keep fractions
-0.5 / 0.3 / 0.1; the in-library dense GEMV and the speedup over it; and the
-CPU oracle timed on this host's cores (a reported baseline, not the target).
+0.5 / 0.3 / 0.1; the in-library dense GEMV and the speedup over it; the
+same step and dense GEMV on layers with int8 Stage-2 rows (prox_prepare_q8);
+the 32-layer stack; and the CPU oracle timed on this host's cores (a
+reported baseline, not the target).
 
 ``--impl reference`` times the CPU oracle alone on the same workload and
 metric: there is no runnable reference implementation of the method.
@@ -75,6 +77,15 @@ def algorithmic_bytes(d: int, F: int, k: int, kx: int) -> dict:
         "step": step,
         "dense": 6 * F * d + 2 * d + 4 * d,
     }
+
+
+def algorithmic_bytes_q8(d: int, F: int, k: int, kx: int) -> dict:
+    """As algorithmic_bytes with int8 Stage-2 rows: per selected channel the
+    gate|up codes 2*d bytes plus 16 bytes of row scales, and d bytes of
+    W_down^T codes."""
+    G = d // 128
+    step = F * kx + 4 * F * G + k * (3 * d + 16) + 2 * d + 4 * d + 4 * k
+    return {"step": step, "dense": F * (3 * d + 16) + 2 * d + 4 * d}
 
 
 def keep_count(n: int, frac: float) -> int:
@@ -530,6 +541,11 @@ def run_gpu(args):
                            "frac_of_measured": round(ab["dense"] / (dus * 1e-6) / 1e9 / hbm_peak, 4),
                            "speedup_prox_over_dense": round(dus / (ms_per_step * 1e3), 3)}
 
+        # ------------------------------------------------ int8 Stage-2 rows
+        if not args.no_q8:
+            extras["int8_stage2"] = q8_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak,
+                                             l2, ms_per_step, dus)
+
         # ------------------------------------------------ 32-layer stack
         if not args.no_stack:
             extras["stack32"] = stack_extra(prox, synth, dev, stream, rho, hbm_peak)
@@ -606,6 +622,59 @@ def run_gpu(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def q8_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak, l2, bf16_us_per_step,
+             bf16_dense_us):
+    """The same step and the dense GEMV on layers prepared with int8 Stage-2
+    rows (prox_prepare_q8), enough copies to exceed the L2 between reuses."""
+    import torch
+
+    d, F = shape.d_model, shape.d_ff
+    k = keep_count(F, rho)
+    ab = algorithmic_bytes_q8(d, F, k, kx)
+    R = 4
+    while R < 16 and R * ab["step"] < 4 * l2:
+        R *= 2
+    layers = []
+    for r in range(R):
+        wg, wu, wd = synth.layer(shape, seed=r, device=dev)
+        layers.append(prox.prox_prepare_q8(wg, wu, wd))
+        del wg, wu, wd
+    xs = [synth.hidden(shape, seed=1 + i, device="cpu").to(dev) for i in range(N_X)]
+    ys = [torch.empty(d, dtype=torch.float32, device=dev) for _ in range(N_X)]
+    torch.cuda.synchronize()
+    out = {"layers": R, "k": k}
+    for mode in ("step", "dense"):
+        def fn(i, mode=mode):
+            L, x, y = layers[i % R], xs[i % N_X], ys[i % N_X]
+            if mode == "step":
+                prox.prox_ffn(L, x, rho, y=y)
+            else:
+                prox.prox_dense_ffn(L, x, y=y)
+
+        with torch.cuda.stream(stream):
+            for i in range(4):
+                fn(i)
+        torch.cuda.synchronize()
+        n = 4 * CHUNK if mode == "step" else 2 * CHUNK
+        gs = graphs_for(fn, n, stream)
+        with torch.cuda.stream(stream):
+            gs[0].replay()
+        torch.cuda.synchronize()
+        m, _, _ = timed_replays(gs, stream)
+        us = m * 1e3 / n
+        gbs = ab[mode] / (us * 1e-6) / 1e9
+        out[mode] = {"us_per_token": round(us, 3), "alg_bytes": ab[mode], "gbs": round(gbs, 1),
+                     "frac_of_measured": round(gbs / hbm_peak, 4)}
+    for L in layers:
+        if prox.prox_get_status(L) != 0:
+            raise SystemExit("device status set in the int8 Stage-2 measurement")
+    out["step"]["speedup_over_bf16_step"] = round(bf16_us_per_step * 1e3 / out["step"]["us_per_token"], 3)
+    out["dense"]["speedup_over_bf16_dense"] = round(bf16_dense_us / out["dense"]["us_per_token"], 3)
+    del layers
+    torch.cuda.empty_cache()
+    return out
 
 
 def stack_extra(prox, synth, dev, stream, rho, hbm_peak, tokens_per_graph=8, replays=8):
@@ -752,6 +821,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stack", action="store_true",
                     help="skip the 32-layer stack measurement in the extras")
+    ap.add_argument("--no-q8", action="store_true",
+                    help="skip the int8 Stage-2 measurement in the extras")
     ap.add_argument("--phases", action="store_true",
                     help="print the per-phase timeline of the decode kernel instead")
     args = ap.parse_args()

@@ -93,6 +93,7 @@ prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, fl
     f.scales = L->scales;
     f.gateup = L->gateup;
     f.down_t = L->down_t;
+    f.q8 = L->q8;
     f.d = L->d_model;
     f.F = L->d_ff;
     f.x = static_cast<const uint16_t*>(x);
@@ -130,6 +131,68 @@ prox_status check_call(const prox_layer* L, const void* x, const float* y) {
     return PROX_OK;
 }
 
+prox_status query_sizes(int d_model, int d_ff, int q8, prox_sizes* out) {
+    if (!out) return PROX_ERR_INVALID_ARG;
+    if (!shape_ok(d_model, d_ff)) return PROX_ERR_UNSUPPORTED_SHAPE;
+    const size_t Fp = (size_t)prox::padded_ff(d_ff);
+    out->proxy_codes = (size_t)d_model * Fp;
+    out->proxy_scales = (size_t)(d_model / prox::kGroup) * Fp * 4;
+    out->gateup = (size_t)d_ff * prox::gu_row_bytes(d_model, q8);
+    out->down_t = (size_t)d_ff * prox::down_row_bytes(d_model, q8);
+    out->workspace = prox::workspace_bytes(d_model, d_ff);
+    return PROX_OK;
+}
+
+prox_status prepare(int d_model, int d_ff, const void* w_gate, const void* w_up,
+                    const void* w_down, void* proxy_codes, void* proxy_scales, void* gateup,
+                    void* down_t, void* workspace, prox_stream_t stream, int q8,
+                    prox_layer** out) {
+    if (!out) return PROX_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!shape_ok(d_model, d_ff)) return PROX_ERR_UNSUPPORTED_SHAPE;
+    const void* ptrs[] = {w_gate, w_up, w_down, proxy_codes, proxy_scales, gateup, down_t, workspace};
+    for (const void* p : ptrs) {
+        if (!p) return PROX_ERR_INVALID_ARG;
+        if (!aligned16(p)) return PROX_ERR_MISALIGNED;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = prox::fused_configure();
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(workspace, 0, prox::workspace_bytes(d_model, d_ff), s);
+    if (e == cudaSuccess)
+        e = prox::launch_prepare(d_model, d_ff, static_cast<const __nv_bfloat16*>(w_gate),
+                                 static_cast<const __nv_bfloat16*>(w_up),
+                                 static_cast<const __nv_bfloat16*>(w_down),
+                                 static_cast<uint8_t*>(proxy_codes),
+                                 static_cast<__half2*>(proxy_scales),
+                                 gateup, down_t, q8, s);
+    if (e != cudaSuccess) return PROX_ERR_CUDA;
+    // one persistent CTA per SM; every CTA holds its chunk of the channels
+    // in shared memory
+    const int g4 = (d_ff + 3) / 4;  // chunks start on multiples of 4 channels
+    if (sms > prox::fused_max_blocks() || 4 * ((g4 + sms - 1) / sms) > prox::fused_max_chunk())
+        return PROX_ERR_UNSUPPORTED_SHAPE;
+    prox_layer* L = new (std::nothrow) prox_layer;
+    if (!L) return PROX_ERR_INVALID_ARG;
+    L->d_model = d_model;
+    L->d_ff = d_ff;
+    L->Fp = prox::padded_ff(d_ff);
+    L->device = dev;
+    L->num_sms = sms;
+    L->num_blocks = sms;
+    L->codes = static_cast<const uint8_t*>(proxy_codes);
+    L->scales = static_cast<const __half2*>(proxy_scales);
+    L->gateup = gateup;
+    L->down_t = down_t;
+    L->q8 = q8;
+    L->ws = prox::carve_workspace(workspace, d_model, d_ff);
+    *out = L;
+    return PROX_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -156,65 +219,27 @@ const char* prox_status_string(prox_status s) {
 }
 
 prox_status prox_query_sizes(int d_model, int d_ff, prox_sizes* out) {
-    if (!out) return PROX_ERR_INVALID_ARG;
-    if (!shape_ok(d_model, d_ff)) return PROX_ERR_UNSUPPORTED_SHAPE;
-    const size_t Fp = (size_t)prox::padded_ff(d_ff);
-    out->proxy_codes = (size_t)d_model * Fp;
-    out->proxy_scales = (size_t)(d_model / prox::kGroup) * Fp * 4;
-    out->gateup = (size_t)d_ff * 2 * d_model * 2;
-    out->down_t = (size_t)d_ff * d_model * 2;
-    out->workspace = prox::workspace_bytes(d_model, d_ff);
-    return PROX_OK;
+    return query_sizes(d_model, d_ff, 0, out);
+}
+
+prox_status prox_query_sizes_q8(int d_model, int d_ff, prox_sizes* out) {
+    return query_sizes(d_model, d_ff, 1, out);
 }
 
 prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, const void* w_up,
                          const void* w_down, void* proxy_codes, void* proxy_scales,
                          void* gateup, void* down_t, void* workspace, prox_stream_t stream,
                          prox_layer** out) {
-    if (!out) return PROX_ERR_INVALID_ARG;
-    *out = nullptr;
-    if (!shape_ok(d_model, d_ff)) return PROX_ERR_UNSUPPORTED_SHAPE;
-    const void* ptrs[] = {w_gate, w_up, w_down, proxy_codes, proxy_scales, gateup, down_t, workspace};
-    for (const void* p : ptrs) {
-        if (!p) return PROX_ERR_INVALID_ARG;
-        if (!aligned16(p)) return PROX_ERR_MISALIGNED;
-    }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = prox::fused_configure();
-    if (e == cudaSuccess)
-        e = cudaMemsetAsync(workspace, 0, prox::workspace_bytes(d_model, d_ff), s);
-    if (e == cudaSuccess)
-        e = prox::launch_prepare(d_model, d_ff, static_cast<const __nv_bfloat16*>(w_gate),
-                                 static_cast<const __nv_bfloat16*>(w_up),
-                                 static_cast<const __nv_bfloat16*>(w_down),
-                                 static_cast<uint8_t*>(proxy_codes),
-                                 static_cast<__half2*>(proxy_scales),
-                                 static_cast<__nv_bfloat16*>(gateup),
-                                 static_cast<__nv_bfloat16*>(down_t), s);
-    if (e != cudaSuccess) return PROX_ERR_CUDA;
-    // one persistent CTA per SM; every CTA holds its chunk of the channels
-    // in shared memory
-    const int g4 = (d_ff + 3) / 4;  // chunks start on multiples of 4 channels
-    if (sms > prox::fused_max_blocks() || 4 * ((g4 + sms - 1) / sms) > prox::fused_max_chunk())
-        return PROX_ERR_UNSUPPORTED_SHAPE;
-    prox_layer* L = new (std::nothrow) prox_layer;
-    if (!L) return PROX_ERR_INVALID_ARG;
-    L->d_model = d_model;
-    L->d_ff = d_ff;
-    L->Fp = prox::padded_ff(d_ff);
-    L->device = dev;
-    L->num_sms = sms;
-    L->num_blocks = sms;
-    L->codes = static_cast<const uint8_t*>(proxy_codes);
-    L->scales = static_cast<const __half2*>(proxy_scales);
-    L->gateup = static_cast<const __nv_bfloat16*>(gateup);
-    L->down_t = static_cast<const __nv_bfloat16*>(down_t);
-    L->ws = prox::carve_workspace(workspace, d_model, d_ff);
-    *out = L;
-    return PROX_OK;
+    return prepare(d_model, d_ff, w_gate, w_up, w_down, proxy_codes, proxy_scales, gateup, down_t,
+                   workspace, stream, 0, out);
+}
+
+prox_status prox_prepare_q8(int d_model, int d_ff, const void* w_gate, const void* w_up,
+                            const void* w_down, void* proxy_codes, void* proxy_scales,
+                            void* gateup_q8, void* down_q8, void* workspace, prox_stream_t stream,
+                            prox_layer** out) {
+    return prepare(d_model, d_ff, w_gate, w_up, w_down, proxy_codes, proxy_scales, gateup_q8,
+                   down_q8, workspace, stream, 1, out);
 }
 
 prox_status prox_ffn_ex(const prox_layer* layer, const void* x, float keep_fraction,
@@ -286,9 +311,10 @@ prox_status prox_dense_ffn(const prox_layer* layer, const void* x, float* y,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(y, 0, (size_t)layer->d_model * sizeof(float), s);
     if (e == cudaSuccess)
-        e = prox::launch_dense(layer->gateup, layer->down_t, static_cast<const uint16_t*>(x),
-                               layer->d_model, layer->d_ff, y, layer->ws.status,
-                               layer->num_blocks, prox::kWaitLimitNs, nullptr, s);
+        e = prox::launch_dense(layer->gateup, layer->down_t, layer->q8,
+                               static_cast<const uint16_t*>(x), layer->d_model, layer->d_ff, y,
+                               layer->ws.status, layer->num_blocks, prox::kWaitLimitNs, nullptr,
+                               s);
     return cuda_status(e);
 }
 
@@ -346,9 +372,10 @@ prox_status prox_ffn_phase_times(const prox_layer* layer, const void* x, float k
     if (dense) {
         e = cudaMemsetAsync(y, 0, (size_t)layer->d_model * sizeof(float), s);
         if (e == cudaSuccess)
-            e = prox::launch_dense(layer->gateup, layer->down_t, static_cast<const uint16_t*>(x),
-                                   layer->d_model, layer->d_ff, y, layer->ws.status,
-                                   layer->num_blocks, prox::kWaitLimitNs, stamps, s);
+            e = prox::launch_dense(layer->gateup, layer->down_t, layer->q8,
+                                   static_cast<const uint16_t*>(x), layer->d_model, layer->d_ff,
+                                   y, layer->ws.status, layer->num_blocks, prox::kWaitLimitNs,
+                                   stamps, s);
         return cuda_status(e);
     }
     return run_prox(layer, x, keep_fraction, 0.5f, y, nullptr, nullptr, nullptr, nullptr, s,

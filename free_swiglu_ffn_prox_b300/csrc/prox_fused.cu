@@ -55,8 +55,9 @@ constexpr int kGuProducerWarp = 16;
 constexpr int kDProducerWarp = 17;
 constexpr int kSelectorWarp = 18;
 constexpr int kMaxStages = 16;
-constexpr size_t kGuRingBytes = 112 * 1024; // gate|up bytes in flight per SM
-constexpr size_t kDRingBytes = 48 * 1024;   // W_down^T bytes in flight per SM
+constexpr size_t kGuRingBytes = 112 * 1024;   // gate|up bytes in flight per SM (bf16)
+constexpr size_t kGuRingBytesQ8 = 136 * 1024; // ... (int8 rows: 16 stages at d = 4096)
+constexpr size_t kDRingBytes = 48 * 1024;     // W_down^T bytes in flight per SM
 constexpr int kMaxItems = 512;            // Stage-2 items per CTA
 constexpr int kMaxChunk = 256;            // channels per CTA chunk
 constexpr int kMaxBlocks = kMaxGrid;
@@ -110,8 +111,9 @@ struct FusedParams {
     // layer
     const uint8_t* codes;
     const __half2* scales;
-    const __nv_bfloat16* gateup;
-    const __nv_bfloat16* down_t;
+    const uint8_t* gateup;  // Stage-2 rows, bf16 or (q8) int8 with scales
+    const uint8_t* down_t;
+    int q8;
     int d, F, Fp;
     // call
     const uint16_t* x;
@@ -143,8 +145,9 @@ struct FusedParams {
     int32_t* kept_out;
     float* scores_out;
     int debug;           // write idx_list and hch
-    // stage-2 ring geometry
-    int n_gu, n_d;
+    // stage-2 ring geometry: n_gu gate|up stages consumed by n_a pass-A
+    // warps (n_a divides n_gu), n_d W_down^T stages
+    int n_gu, n_d, n_a;
     long long limit_ns;
     int inject;          // 1: the last CTA withholds its grid-barrier arrival (test hook)
     uint64_t* ts;        // [gridDim][kPhaseStamps] %globaltimer stamps, or null
@@ -469,13 +472,36 @@ __device__ __forceinline__ float dot8_bf16(const uint4 a, const uint4 b, float a
     return acc;
 }
 
+// int8 weights: a word of four two's-complement codes, flipped to offset
+// binary (w ^ 0x80808080), gives code e as the exact float 2^23 + (q + 128)
+// by placing its byte under the exponent of 2^23 (one PRMT); subtracting
+// 2^23 + 128 leaves q exactly.
+__device__ __forceinline__ float q8_value(uint32_t wo, int e) {
+    return __uint_as_float(__byte_perm(wo, 0x4Bu, 0x4550u | (unsigned)e)) - 8388736.0f;
+}
+
+// acc += sum over 8 elements of q_e * x_e (int8 codes w, bf16 x; every
+// product is exact in fp32)
+__device__ __forceinline__ float dot8_q8(const uint2 w, const uint4 x, float acc) {
+    const uint32_t w0 = w.x ^ 0x80808080u, w1 = w.y ^ 0x80808080u;
+    acc = fmaf(q8_value(w0, 0), __uint_as_float(x.x << 16), acc);
+    acc = fmaf(q8_value(w0, 1), __uint_as_float(x.x & 0xffff0000u), acc);
+    acc = fmaf(q8_value(w0, 2), __uint_as_float(x.y << 16), acc);
+    acc = fmaf(q8_value(w0, 3), __uint_as_float(x.y & 0xffff0000u), acc);
+    acc = fmaf(q8_value(w1, 0), __uint_as_float(x.z << 16), acc);
+    acc = fmaf(q8_value(w1, 1), __uint_as_float(x.z & 0xffff0000u), acc);
+    acc = fmaf(q8_value(w1, 2), __uint_as_float(x.w << 16), acc);
+    acc = fmaf(q8_value(w1, 3), __uint_as_float(x.w & 0xffff0000u), acc);
+    return acc;
+}
+
 struct Stage2Args {
-    const __nv_bfloat16* gateup;
-    const __nv_bfloat16* down_t;
+    const uint8_t* gateup;  // [F] rows of gu_row_bytes(d, Q8)
+    const uint8_t* down_t;  // [F] rows of down_row_bytes(d, Q8)
     float* y;
     float* hch;     // [F] h per channel (debug, may be null)
     int* status;
-    int d, F, n_gu, n_d;
+    int d, F, n_gu, n_d, n_a;
     long long limit_ns;
     uint64_t* ts;   // [gridDim][kPhaseStamps] or null
 };
@@ -520,25 +546,28 @@ __device__ __forceinline__ bool warp_wait_flag(const uint8_t* flag, long long li
 // Stage-2 roles of warps 0..17 over the CTA's items ctl.item[0..n_items).
 // Items [0, m) are known when the roles start; the rest (ctl.n_items, their
 // channels and ctl.conf of every item) only once ctl.sel_bar completes.
-// Shared area: x as bf16 (2 d bytes), then n_gu gate|up stages (4 d bytes
-// each), then n_d W_down^T stages (2 d bytes each).
+// Shared area: x as bf16 (2 d bytes), then n_gu gate|up stages and n_d
+// W_down^T stages, one row each (bf16: 4 d and 2 d bytes; Q8: the int8 codes
+// 2 d + 16 bytes with the row's scales s_gate, s_up, s_down, and d bytes).
 //   GU producer (warp 16) / D producer (warp 17): lane 0 issues one bulk copy
 //       per item into the next stage of its ring;
-//   pass A (warp w < n_gu): the items i = w (mod n_gu), always in gate|up
-//       stage w, so one warp consumes each stage's uses in order (a parity
-//       wait is never taken two uses ahead): g, u over the whole row,
-//       h = silu(g) u, then ctl.hready[i];
+//   pass A (warp w < n_a, n_a dividing n_gu): the items i = w (mod n_a); item
+//       i sits in gate|up stage i mod n_gu, whose items are all = w (mod
+//       n_a), so one warp consumes each stage's uses in order (a parity wait
+//       is never taken two uses ahead): g, u over the whole row,
+//       h = silu(g) u, then ctl.hready[i] (Q8: g and u times the row scales,
+//       and ctl.h[i] = h s_down, the factor of the int8 W_down^T row);
 //   pass B (warps 8..15): every thread owns 8-element slices of d and, for
 //       each confirmed item in order, adds h * W_down^T[c, slice].
-template <int CPT>
+template <int CPT, bool Q8>
 __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int d = a.d, n_gu = a.n_gu, n_d = a.n_d;
-    const size_t gu_bytes = (size_t)4 * d, d_bytes = (size_t)2 * d;
+    const int d = a.d, n_gu = a.n_gu, n_d = a.n_d, n_a = a.n_a;
+    const size_t gu_bytes = gu_row_bytes(d, Q8), d_bytes = down_row_bytes(d, Q8);
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(area);
     uint8_t* gu_ring = area + (size_t)2 * d;
     uint8_t* d_ring = gu_ring + (size_t)n_gu * gu_bytes;
-    const int nchunk = d / 8;  // 16-byte chunks per row
+    const int nchunk = d / 8;  // 8-element chunks per row (16 bytes bf16, 8 bytes int8)
 
     if (warp == kGuProducerWarp || warp == kDProducerWarp) {
         if (lane != 0) return;
@@ -549,8 +578,7 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
         uint64_t* empty = gu ? ctl.gu_empty : ctl.d_empty;
         int* last = gu ? ctl.gu_last : ctl.d_last;
         uint8_t* base = gu ? gu_ring : d_ring;
-        const uint8_t* src = gu ? reinterpret_cast<const uint8_t*>(a.gateup)
-                                : reinterpret_cast<const uint8_t*>(a.down_t);
+        const uint8_t* src = gu ? a.gateup : a.down_t;
         const uint64_t pol = policy_evict_first();
         auto wait = [&](uint64_t* bar, uint32_t parity) {
             if (mbar_wait_bounded(bar, parity, a.limit_ns, &ctl.abort)) return true;
@@ -587,11 +615,11 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
 
     if (warp < kPassAWarps) {
         // ------------------------------------------------ pass A: h per item
-        if (warp >= n_gu) return;
+        if (warp >= n_a) return;
         const uint4* xv = reinterpret_cast<const uint4*>(xs);
-        const int s = warp;
         bool known = false;
-        for (int i = warp;; i += n_gu) {
+        for (int i = warp;; i += n_a) {
+            const int s = i % n_gu;
             if (i >= m) {
                 if (!known) {
                     if (!warp_wait(&ctl.sel_bar, 0, a.limit_ns, ctl, a.status)) break;
@@ -601,13 +629,24 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
             }
             if (!warp_wait(&ctl.gu_full[s], (i / n_gu) & 1, a.limit_ns, ctl, a.status)) break;
             if (i == 0 && lane == 0) stamp_here(a.ts, 6);
-            const uint4* gr = reinterpret_cast<const uint4*>(gu_ring + (size_t)s * gu_bytes);
-            const uint4* ur = gr + nchunk;
+            const uint8_t* st = gu_ring + (size_t)s * gu_bytes;
             float g = 0.0f, u = 0.0f;
-            for (int ch = lane; ch < nchunk; ch += 32) {
-                const uint4 xw = xv[ch];
-                g = dot8_bf16(gr[ch], xw, g);
-                u = dot8_bf16(ur[ch], xw, u);
+            if constexpr (Q8) {
+                const uint2* gr = reinterpret_cast<const uint2*>(st);
+                const uint2* ur = gr + nchunk;
+                for (int ch = lane; ch < nchunk; ch += 32) {
+                    const uint4 xw = xv[ch];
+                    g = dot8_q8(gr[ch], xw, g);
+                    u = dot8_q8(ur[ch], xw, u);
+                }
+            } else {
+                const uint4* gr = reinterpret_cast<const uint4*>(st);
+                const uint4* ur = gr + nchunk;
+                for (int ch = lane; ch < nchunk; ch += 32) {
+                    const uint4 xw = xv[ch];
+                    g = dot8_bf16(gr[ch], xw, g);
+                    u = dot8_bf16(ur[ch], xw, u);
+                }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -615,9 +654,16 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
                 u += __shfl_xor_sync(0xffffffffu, u, o);
             }
             if (lane == 0) {
+                float hs = 1.0f;  // factor of the W_down^T row
+                if constexpr (Q8) {
+                    const float4 sc = *reinterpret_cast<const float4*>(st + (size_t)2 * d);
+                    g *= sc.x;
+                    u *= sc.y;
+                    hs = sc.z;
+                }
                 mbar_arrive(&ctl.gu_empty[s]);
                 const float h = g / (1.0f + expf(-g)) * u;  // silu(g) * u
-                ctl.h[i] = h;
+                ctl.h[i] = Q8 ? h * hs : h;
                 if (a.hch) a.hch[ctl.item[i]] = h;
                 __threadfence_block();
                 *reinterpret_cast<volatile uint8_t*>(&ctl.hready[i]) = 1;
@@ -640,18 +686,30 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
     for (int q = 0; q < CPT; ++q)
 #pragma unroll
         for (int e = 0; e < 8; ++e) yp[q][e] = 0.0f;
-    auto add_row = [&](const uint4* row, float hv, bool global) {
+    auto add_row = [&](const uint8_t* row, float hv, bool global) {
 #pragma unroll
         for (int q = 0; q < CPT; ++q) {
             const int ch = t + q * kPassB;
             if (ch < nchunk) {
-                const uint4 dw = global ? __ldg(row + ch) : row[ch];
-                const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
+                if constexpr (Q8) {
+                    const uint2* r8 = reinterpret_cast<const uint2*>(row);
+                    const uint2 dw = global ? __ldg(r8 + ch) : r8[ch];
+                    const uint32_t w0 = dw.x ^ 0x80808080u, w1 = dw.y ^ 0x80808080u;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    yp[q][2 * e] = fmaf(hv, __uint_as_float(dv[e] << 16), yp[q][2 * e]);
-                    yp[q][2 * e + 1] =
-                        fmaf(hv, __uint_as_float(dv[e] & 0xffff0000u), yp[q][2 * e + 1]);
+                    for (int e = 0; e < 4; ++e) {
+                        yp[q][e] = fmaf(hv, q8_value(w0, e), yp[q][e]);
+                        yp[q][4 + e] = fmaf(hv, q8_value(w1, e), yp[q][4 + e]);
+                    }
+                } else {
+                    const uint4* r16 = reinterpret_cast<const uint4*>(row);
+                    const uint4 dw = global ? __ldg(r16 + ch) : r16[ch];
+                    const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        yp[q][2 * e] = fmaf(hv, __uint_as_float(dv[e] << 16), yp[q][2 * e]);
+                        yp[q][2 * e + 1] =
+                            fmaf(hv, __uint_as_float(dv[e] & 0xffff0000u), yp[q][2 * e + 1]);
+                    }
                 }
             }
         }
@@ -679,8 +737,8 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
         if (!known || ctl.conf[i]) {
             ok = warp_wait_flag(&ctl.hready[i], a.limit_ns, ctl, a.status);
             if (!ok) break;
-            add_row(reinterpret_cast<const uint4*>(d_ring + (size_t)s * d_bytes),
-                    *reinterpret_cast<const volatile float*>(&ctl.h[i]), false);
+            add_row(d_ring + (size_t)s * d_bytes, *reinterpret_cast<const volatile float*>(&ctl.h[i]),
+                    false);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.d_empty[s]);
@@ -688,8 +746,7 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
     if (ok && known)
         for (int i = 0; i < first_known; ++i)
             if (!ctl.conf[i])
-                add_row(reinterpret_cast<const uint4*>(a.down_t + (size_t)ctl.item[i] * d),
-                        -ctl.h[i], true);
+                add_row(a.down_t + (size_t)ctl.item[i] * d_bytes, -ctl.h[i], true);
     if (t == 0) stamp_here(a.ts, 8);
     if (ok && !ctl.abort && n > 0) {
 #pragma unroll
@@ -1093,7 +1150,8 @@ __device__ void await_selection(const FusedParams& p, Ctl& ctl, int b, int nb, i
         // a dropped speculative item may already be in y: pass B will read its
         // W_down^T row again to take it out, so bring the row into L2 now
         if (j >= selb)
-            prefetch_l2(p.down_t + (size_t)ctl.item[j] * p.d, (uint32_t)(2 * p.d));
+            prefetch_l2(p.down_t + (size_t)ctl.item[j] * down_row_bytes(p.d, p.q8),
+                        (uint32_t)down_row_bytes(p.d, p.q8));
     }
     if (p.debug) {
         int pos = __ldcg(p.selpre + b);
@@ -1114,7 +1172,7 @@ __device__ void await_selection(const FusedParams& p, Ctl& ctl, int b, int nb, i
 }
 
 // ------------------------------------------------------------ fused kernel
-template <int CPT>
+template <int CPT, bool Q8>
 __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
@@ -1519,19 +1577,20 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     a.F = F;
     a.n_gu = p.n_gu;
     a.n_d = p.n_d;
+    a.n_a = p.n_a;
     a.limit_ns = p.limit_ns;
     a.ts = p.ts;
     if (wid == kSelectorWarp) {
         if (!ctl.abort) await_selection(p, ctl, b, nb, cb0, nch, m, ep);
     } else {
-        stage2_roles<CPT>(a, ctl, area, m);
+        stage2_roles<CPT, Q8>(a, ctl, area, m);
     }
     stage2_join(a, ctl);
 }
 
 // Dense baseline: Stage 2 over every channel, CTA i taking [F i/n, F (i+1)/n)
 // (all items known and confirmed from the start).
-template <int CPT>
+template <int CPT, bool Q8>
 __global__ void __launch_bounds__(kNT, 1) k_dense(const Stage2Args a, const uint16_t* x) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
@@ -1555,7 +1614,7 @@ __global__ void __launch_bounds__(kNT, 1) k_dense(const Stage2Args a, const uint
         fence_mbar_init();
     }
     __syncthreads();
-    if ((tid >> 5) != kSelectorWarp) stage2_roles<CPT>(a, ctl, area, n);
+    if ((tid >> 5) != kSelectorWarp) stage2_roles<CPT, Q8>(a, ctl, area, n);
     stage2_join(a, ctl);
 }
 
@@ -1571,23 +1630,28 @@ __global__ void k_gather_h(const int* idx_list, const float* hch, int k, int32_t
 
 // ------------------------------------------------------------ host side
 struct Ring {
-    int n_gu, n_d;
+    int n_gu, n_d, n_a;
 };
 
 size_t area_budget() { return kSmemLimit - ctl_bytes(); }
 
-// Stage-2 rings after x (2 d bytes): gate|up stages (4 d bytes each) up to
-// kGuRingBytes and kPassAWarps stages, W_down^T stages (2 d bytes each) up to
-// kDRingBytes, both within the shared memory left.  The caps keep ~160 KB in
-// flight per SM: enough to saturate HBM, and every extra byte in flight only
-// lengthens the queues that the channel selection's loads wait in.
-Ring ring_for(int d) {
+// Stage-2 rings after x (2 d bytes): gate|up stages (one row each) up to
+// kGuRingBytes (bf16) or kGuRingBytesQ8 (int8) and kMaxStages, consumed by
+// n_a = min(stages, kPassAWarps) pass-A warps (the stage count rounded down
+// to a multiple of n_a), then W_down^T stages up to kDRingBytes, both within
+// the shared memory left.  The bf16 caps keep ~160 KB in flight per SM:
+// enough to saturate HBM, and every extra byte in flight only lengthens the
+// queues that the channel selection's loads wait in.  Rows of int8 are half
+// as long, so their ring holds more of them.
+Ring ring_for(int d, int q8) {
     const size_t budget = area_budget() - (size_t)2 * d;
-    const size_t gu = (size_t)4 * d, dd = (size_t)2 * d;
-    Ring r{0, 0};
-    r.n_gu = (int)(min(budget * 2 / 3, kGuRingBytes) / gu);
-    if (r.n_gu > kPassAWarps) r.n_gu = kPassAWarps;
+    const size_t gu = gu_row_bytes(d, q8), dd = down_row_bytes(d, q8);
+    Ring r{0, 0, 0};
+    r.n_gu = (int)(min(budget * 2 / 3, q8 ? kGuRingBytesQ8 : kGuRingBytes) / gu);
+    if (r.n_gu > kMaxStages) r.n_gu = kMaxStages;
     if (r.n_gu < 1) r.n_gu = 1;
+    r.n_a = r.n_gu < kPassAWarps ? r.n_gu : kPassAWarps;
+    r.n_gu -= r.n_gu % r.n_a;
     const size_t left = budget > (size_t)r.n_gu * gu ? budget - (size_t)r.n_gu * gu : 0;
     r.n_d = (int)(min(left, kDRingBytes) / dd);
     if (r.n_d > kMaxStages) r.n_d = kMaxStages;
@@ -1595,8 +1659,9 @@ Ring ring_for(int d) {
     return r;
 }
 
-size_t ring_bytes(int d, const Ring& r) {
-    return (size_t)2 * d + (size_t)r.n_gu * 4 * d + (size_t)r.n_d * 2 * d;
+size_t ring_bytes(int d, int q8, const Ring& r) {
+    return (size_t)2 * d + (size_t)r.n_gu * gu_row_bytes(d, q8) +
+           (size_t)r.n_d * down_row_bytes(d, q8);
 }
 
 template <typename K>
@@ -1632,14 +1697,22 @@ ProxyGeom proxy_geometry(int F, int kx, int num_blocks) {
 
 cudaError_t fused_configure() {
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<1>);
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<2>);
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<4>);
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<8>);
-    if (e == cudaSuccess) e = set_smem(k_dense<1>);
-    if (e == cudaSuccess) e = set_smem(k_dense<2>);
-    if (e == cudaSuccess) e = set_smem(k_dense<4>);
-    if (e == cudaSuccess) e = set_smem(k_dense<8>);
+    if (e == cudaSuccess) e = set_smem(k_prox_fused<1, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_fused<2, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_fused<4, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_fused<8, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_fused<1, true>);
+    if (e == cudaSuccess) e = set_smem(k_prox_fused<2, true>);
+    if (e == cudaSuccess) e = set_smem(k_prox_fused<4, true>);
+    if (e == cudaSuccess) e = set_smem(k_prox_fused<8, true>);
+    if (e == cudaSuccess) e = set_smem(k_dense<1, false>);
+    if (e == cudaSuccess) e = set_smem(k_dense<2, false>);
+    if (e == cudaSuccess) e = set_smem(k_dense<4, false>);
+    if (e == cudaSuccess) e = set_smem(k_dense<8, false>);
+    if (e == cudaSuccess) e = set_smem(k_dense<1, true>);
+    if (e == cudaSuccess) e = set_smem(k_dense<2, true>);
+    if (e == cudaSuccess) e = set_smem(k_dense<4, true>);
+    if (e == cudaSuccess) e = set_smem(k_dense<8, true>);
     return e;
 }
 
@@ -1656,20 +1729,22 @@ bool fused_fits(int d, int F) {
     // (the running-total table reuses it); P3: the Stage-2 rings.
     (void)F;
     const size_t p01 = (size_t)6 * d + 4096 + (size_t)16 * kRing * kNT;
-    const Ring r = ring_for(d);
+    const Ring r = ring_for(d, 0);  // the bf16 rings are the larger
     // the channel selection (CTA 0): x, three digit histograms, the sorted
     // keys and chunk-local indices of every chunk, per-chunk tables, candidates
     const size_t sel = (size_t)2 * d + (size_t)4 * (2 * kHistBins + 512) +
                        (size_t)5 * padded_ff(F) + (size_t)4 * (11 * kMaxBlocks + 4) +
                        (size_t)4 * kCandCap;
-    return p01 <= area_budget() && ring_bytes(d, r) <= area_budget() && sel <= area_budget() &&
+    return p01 <= area_budget() && ring_bytes(d, 0, r) <= area_budget() &&
+           ring_bytes(d, 1, ring_for(d, 1)) <= area_budget() && sel <= area_budget() &&
            r.n_gu >= 1 && r.n_d >= 1 && d / 8 <= kXGroups * kNT;
 }
 
 namespace {
 template <int CPT>
 cudaError_t launch_fused_t(const cudaLaunchConfig_t& cfg, const FusedParams& p) {
-    return cudaLaunchKernelEx(&cfg, k_prox_fused<CPT>, p);
+    return p.q8 ? cudaLaunchKernelEx(&cfg, k_prox_fused<CPT, true>, p)
+                : cudaLaunchKernelEx(&cfg, k_prox_fused<CPT, false>, p);
 }
 }  // namespace
 
@@ -1678,8 +1753,9 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     FusedParams p;
     p.codes = L.codes;
     p.scales = L.scales;
-    p.gateup = L.gateup;
-    p.down_t = L.down_t;
+    p.gateup = static_cast<const uint8_t*>(L.gateup);
+    p.down_t = static_cast<const uint8_t*>(L.down_t);
+    p.q8 = L.q8;
     p.d = L.d;
     p.F = L.F;
     p.Fp = padded_ff(L.F);
@@ -1711,9 +1787,10 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     p.kept_out = L.kept_out;
     p.scores_out = L.scores_out;
     p.debug = (L.idx_out || L.h_out) ? 1 : 0;
-    const Ring r = ring_for(L.d);
+    const Ring r = ring_for(L.d, L.q8);
     p.n_gu = r.n_gu;
     p.n_d = r.n_d;
+    p.n_a = r.n_a;
     p.limit_ns = L.limit_ns;
     p.inject = L.inject;
     p.ts = L.ts;
@@ -1741,29 +1818,36 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     return e;
 }
 
-cudaError_t launch_dense(const __nv_bfloat16* gateup, const __nv_bfloat16* down_t,
-                         const uint16_t* x, int d, int F, float* y, int* status, int num_blocks,
-                         long long limit_ns, uint64_t* ts, cudaStream_t stream) {
+cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const uint16_t* x, int d,
+                         int F, float* y, int* status, int num_blocks, long long limit_ns,
+                         uint64_t* ts, cudaStream_t stream) {
     if (num_blocks < 1 || num_blocks > kMaxBlocks) return cudaErrorInvalidValue;
     Stage2Args a;
-    a.gateup = gateup;
-    a.down_t = down_t;
+    a.gateup = static_cast<const uint8_t*>(gateup);
+    a.down_t = static_cast<const uint8_t*>(down_t);
     a.y = y;
     a.hch = nullptr;
     a.status = status;
     a.d = d;
     a.F = F;
-    const Ring r = ring_for(d);
+    const Ring r = ring_for(d, q8);
     a.n_gu = r.n_gu;
     a.n_d = r.n_d;
+    a.n_a = r.n_a;
     a.limit_ns = limit_ns;
     a.ts = ts;
     const int nchunk = d / 8;
-    if (nchunk <= kPassB) k_dense<1><<<num_blocks, kNT, kSmemLimit, stream>>>(a, x);
-    else if (nchunk <= 2 * kPassB) k_dense<2><<<num_blocks, kNT, kSmemLimit, stream>>>(a, x);
-    else if (nchunk <= 4 * kPassB) k_dense<4><<<num_blocks, kNT, kSmemLimit, stream>>>(a, x);
-    else k_dense<8><<<num_blocks, kNT, kSmemLimit, stream>>>(a, x);
-    return cudaGetLastError();
+    const int cpt = nchunk <= kPassB ? 1 : nchunk <= 2 * kPassB ? 2 : nchunk <= 4 * kPassB ? 4 : 8;
+    auto go = [&](auto kern) {
+        kern<<<num_blocks, kNT, kSmemLimit, stream>>>(a, x);
+        return cudaGetLastError();
+    };
+    switch (cpt) {
+        case 1: return q8 ? go(k_dense<1, true>) : go(k_dense<1, false>);
+        case 2: return q8 ? go(k_dense<2, true>) : go(k_dense<2, false>);
+        case 4: return q8 ? go(k_dense<4, true>) : go(k_dense<4, false>);
+        default: return q8 ? go(k_dense<8, true>) : go(k_dense<8, false>);
+    }
 }
 
 }  // namespace prox

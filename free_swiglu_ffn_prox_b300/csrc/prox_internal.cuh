@@ -162,9 +162,16 @@ __device__ __forceinline__ void record_status(int* status, int code) {
 
 // ----------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  All run on `stream`.
+// q8 = 0: gateup/down_t receive the bf16 Stage-2 layouts; q8 = 1: the int8
+// ones (gate|up rows of 2 d + 16 bytes with their scales, W_down^T rows of d
+// bytes), see prox_prepare_q8.
 cudaError_t launch_prepare(int d, int F, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
                            const __nv_bfloat16* w_down, uint8_t* codes, __half2* scales,
-                           __nv_bfloat16* gateup, __nv_bfloat16* down_t, cudaStream_t stream);
+                           void* gateup, void* down_t, int q8, cudaStream_t stream);
+
+// Bytes of one Stage-2 gate|up row and one W_down^T row in device memory.
+constexpr size_t gu_row_bytes(int d, int q8) { return q8 ? (size_t)2 * d + 16 : (size_t)4 * d; }
+constexpr size_t down_row_bytes(int d, int q8) { return q8 ? (size_t)d : (size_t)2 * d; }
 
 // Proxy work split: `tiles` channel tiles of `tile_w` channels (a multiple
 // of 16) times `slices` slices of the kept inputs, tiles * slices <= blocks.
@@ -176,8 +183,9 @@ ProxyGeom proxy_geometry(int F, int kx, int num_blocks);
 struct FusedLaunch {
     const uint8_t* codes;
     const __half2* scales;
-    const __nv_bfloat16* gateup;
-    const __nv_bfloat16* down_t;
+    const void* gateup;  // Stage-2 rows, bf16 or int8 (q8)
+    const void* down_t;
+    int q8 = 0;
     int d, F;
     const uint16_t* x;
     float* y;
@@ -206,9 +214,9 @@ int fused_max_chunk();
 int fused_max_blocks();
 size_t fused_smem_bytes();
 cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream);
-cudaError_t launch_dense(const __nv_bfloat16* gateup, const __nv_bfloat16* down_t,
-                         const uint16_t* x, int d, int F, float* y, int* status, int num_blocks,
-                         long long limit_ns, uint64_t* ts, cudaStream_t stream);
+cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const uint16_t* x, int d,
+                         int F, float* y, int* status, int num_blocks, long long limit_ns,
+                         uint64_t* ts, cudaStream_t stream);
 
 cudaError_t launch_residual_rmsnorm(int d, const uint16_t* x, const float* y, float eps,
                                     uint16_t* x_next, cudaStream_t stream);
@@ -222,7 +230,8 @@ struct prox_layer {
     int device, num_sms, num_blocks;
     const uint8_t* codes;
     const __half2* scales;
-    const __nv_bfloat16* gateup;
-    const __nv_bfloat16* down_t;
+    const void* gateup;  // bf16 layouts, or the int8 ones when q8 is set
+    const void* down_t;
+    int q8;
     prox::Workspace ws;
 };

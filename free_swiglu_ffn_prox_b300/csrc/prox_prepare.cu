@@ -5,7 +5,10 @@
 // file builds:
 //   * the int4 group-128 symmetric proxy, packed input-dim-major so that one
 //     kept input dimension is one contiguous row of d_ff bytes;
-//   * the channel-interleaved gate|up rows and the channel-major W_down^T.
+//   * the channel-interleaved gate|up rows and the channel-major W_down^T,
+//     either as bf16 copies or quantized to int8 per row (symmetric, one fp32
+//     scale amax / 127 per row; the scales travel at the end of each gate|up
+//     row so that one bulk copy brings a channel's codes and scales).
 #include "prox_internal.cuh"
 
 namespace prox {
@@ -63,25 +66,126 @@ k_transpose(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ d
     }
 }
 
+// int8 code of w on a row with scale s: round-to-nearest-even of the binary32
+// quotient w / s, clamped to [-127, 127]; 0 on an all-zero row.
+__device__ __forceinline__ int8_t q8_code(float w, float s) {
+    if (s == 0.0f) return 0;
+    return (int8_t)min(127, max(-127, __float2int_rn(__fdiv_rn(w, s))));
+}
+
+// One CTA per channel c: the int8 gate and up rows of c and their scales,
+// row c of the output = q_gate[c][0..d) | q_up[c][0..d) | s_gate s_up s_down 0
+// (s_down is written by k_q8_down).
+__global__ void __launch_bounds__(256)
+k_q8_gateup(const __nv_bfloat16* __restrict__ w_gate, const __nv_bfloat16* __restrict__ w_up,
+            uint8_t* __restrict__ out, int d) {
+    __shared__ float red[2][8];
+    const int c = blockIdx.x, tid = threadIdx.x;
+    const __nv_bfloat16* rg = w_gate + (size_t)c * d;
+    const __nv_bfloat16* ru = w_up + (size_t)c * d;
+    float ag = 0.0f, au = 0.0f;
+    for (int j = tid; j < d; j += 256) {
+        ag = fmaxf(ag, fabsf(__bfloat162float(rg[j])));
+        au = fmaxf(au, fabsf(__bfloat162float(ru[j])));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ag = fmaxf(ag, __shfl_xor_sync(0xffffffffu, ag, o));
+        au = fmaxf(au, __shfl_xor_sync(0xffffffffu, au, o));
+    }
+    if ((tid & 31) == 0) {
+        red[0][tid >> 5] = ag;
+        red[1][tid >> 5] = au;
+    }
+    __syncthreads();
+    float mg = 0.0f, mu = 0.0f;
+    for (int w = 0; w < 8; ++w) {
+        mg = fmaxf(mg, red[0][w]);
+        mu = fmaxf(mu, red[1][w]);
+    }
+    const float sg = __fdiv_rn(mg, 127.0f), su = __fdiv_rn(mu, 127.0f);
+    uint8_t* row = out + (size_t)c * gu_row_bytes(d, 1);
+    int8_t* qg = reinterpret_cast<int8_t*>(row);
+    int8_t* qu = qg + d;
+    for (int j = tid; j < d; j += 256) {
+        qg[j] = q8_code(__bfloat162float(rg[j]), sg);
+        qu[j] = q8_code(__bfloat162float(ru[j]), su);
+    }
+    if (tid == 0) {
+        float* t = reinterpret_cast<float*>(row + (size_t)2 * d);
+        t[0] = sg;
+        t[1] = su;
+        t[3] = 0.0f;
+    }
+}
+
+// W_down [d][F] -> int8 W_down^T [F][d], one scale per channel (a column of
+// W_down): 32 channels per CTA, the column maxima first, then 32 x 32 tiles
+// through shared memory.  s_down[c] goes to the scale slot of gate|up row c.
+__global__ void __launch_bounds__(256)
+k_q8_down(const __nv_bfloat16* __restrict__ w_down, int8_t* __restrict__ down_q8,
+          uint8_t* __restrict__ gateup_q8, int d, int F) {
+    __shared__ float tile[32][33];
+    __shared__ float red[8][32];
+    __shared__ float sc[32];
+    const int c0 = blockIdx.x * 32, tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int c = c0 + tx;
+    float amax = 0.0f;
+    if (c < F)
+        for (int r = ty; r < d; r += 8)
+            amax = fmaxf(amax, fabsf(__bfloat162float(w_down[(size_t)r * F + c])));
+    red[ty][tx] = amax;
+    __syncthreads();
+    if (ty == 0) {
+        float m = red[0][tx];
+        for (int j = 1; j < 8; ++j) m = fmaxf(m, red[j][tx]);
+        const float sd = __fdiv_rn(m, 127.0f);
+        sc[tx] = sd;
+        if (c < F)
+            *reinterpret_cast<float*>(gateup_q8 + (size_t)c * gu_row_bytes(d, 1) + (size_t)2 * d +
+                                      8) = sd;
+    }
+    __syncthreads();
+    for (int r0 = 0; r0 < d; r0 += 32) {  // d is a multiple of 128
+        for (int i = ty; i < 32; i += 8)
+            tile[i][tx] = c < F ? __bfloat162float(w_down[(size_t)(r0 + i) * F + c]) : 0.0f;
+        __syncthreads();
+        for (int i = ty; i < 32; i += 8) {
+            const int cc = c0 + i;
+            if (cc < F) down_q8[(size_t)cc * d + r0 + tx] = q8_code(tile[tx][i], sc[i]);
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_prepare(int d, int F, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
                            const __nv_bfloat16* w_down, uint8_t* codes, __half2* scales,
-                           __nv_bfloat16* gateup, __nv_bfloat16* down_t, cudaStream_t stream) {
+                           void* gateup, void* down_t, int q8, cudaStream_t stream) {
     const int Fp = padded_ff(F);
     const int G = d / kGroup;
     dim3 qgrid((Fp + 127) / 128, G);
     k_quantize_pack<<<qgrid, 128, 0, stream>>>(w_gate, w_up, codes, scales, d, F, Fp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (q8) {
+        k_q8_gateup<<<F, 256, 0, stream>>>(w_gate, w_up, static_cast<uint8_t*>(gateup), d);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        k_q8_down<<<(F + 31) / 32, 256, 0, stream>>>(w_down, static_cast<int8_t*>(down_t),
+                                                     static_cast<uint8_t*>(gateup), d, F);
+        return cudaGetLastError();
+    }
     // gate|up interleave: two strided 2-D copies into the [F][2][d] rows
     const size_t row = (size_t)d * sizeof(__nv_bfloat16);
-    e = cudaMemcpy2DAsync(gateup, 2 * row, w_gate, row, row, F, cudaMemcpyDeviceToDevice, stream);
+    __nv_bfloat16* gu = static_cast<__nv_bfloat16*>(gateup);
+    e = cudaMemcpy2DAsync(gu, 2 * row, w_gate, row, row, F, cudaMemcpyDeviceToDevice, stream);
     if (e != cudaSuccess) return e;
-    e = cudaMemcpy2DAsync(gateup + d, 2 * row, w_up, row, row, F, cudaMemcpyDeviceToDevice, stream);
+    e = cudaMemcpy2DAsync(gu + d, 2 * row, w_up, row, row, F, cudaMemcpyDeviceToDevice, stream);
     if (e != cudaSuccess) return e;
     dim3 tgrid((F + 31) / 32, (d + 31) / 32);
-    k_transpose<<<tgrid, 256, 0, stream>>>(w_down, down_t, d, F);
+    k_transpose<<<tgrid, 256, 0, stream>>>(w_down, static_cast<__nv_bfloat16*>(down_t), d, F);
     return cudaGetLastError();
 }
 

@@ -58,6 +58,9 @@ def _load():
             "prox_query_sizes": (i32, [i32, i32, ctypes.POINTER(_Sizes)]),
             "prox_prepare": (i32, [i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                    ctypes.POINTER(vp)]),
+            "prox_query_sizes_q8": (i32, [i32, i32, ctypes.POINTER(_Sizes)]),
+            "prox_prepare_q8": (i32, [i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      ctypes.POINTER(vp)]),
             "prox_ffn": (i32, [vp, vp, f32, vp, vp]),
             "prox_ffn_ex": (i32, [vp, vp, f32, f32, vp, vp]),
             "prox_ffn_host": (i32, [vp, vp, f32, vp, vp]),
@@ -125,9 +128,11 @@ def prox_keep_count(n: int, frac: float) -> int:
     return int(_load().prox_keep_count(int(n), float(frac)))
 
 
-def prox_query_sizes(d_model: int, d_ff: int) -> dict:
+def prox_query_sizes(d_model: int, d_ff: int, q8: bool = False) -> dict:
+    """Buffer sizes for prox_prepare (q8: for prox_prepare_q8)."""
     s = _Sizes()
-    _check(_load().prox_query_sizes(int(d_model), int(d_ff), ctypes.byref(s)), "prox_query_sizes")
+    name = "prox_query_sizes_q8" if q8 else "prox_query_sizes"
+    _check(getattr(_load(), name)(int(d_model), int(d_ff), ctypes.byref(s)), name)
     return {n: int(getattr(s, n)) for n, _ in _Sizes._fields_}
 
 
@@ -135,8 +140,9 @@ class ProxLayer:
     """A prepared layer: the device buffers (owned here, as torch tensors)
     and the library's host handle."""
 
-    def __init__(self, d_model, d_ff, bufs, handle, device):
+    def __init__(self, d_model, d_ff, bufs, handle, device, q8=False):
         self.d_model, self.d_ff = int(d_model), int(d_ff)
+        self.q8 = bool(q8)
         self.bufs = bufs
         self.handle = handle
         self.device = device
@@ -153,9 +159,7 @@ class ProxLayer:
             pass
 
 
-def prox_prepare(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
-                 stream=None) -> ProxLayer:
-    """Builds the proxy and Stage-2 layouts of one layer (see prox.h)."""
+def _prepare(w_gate, w_up, w_down, stream, q8):
     lib = _load()
     if w_gate.dim() != 2:
         raise ValueError("w_gate must be [d_ff, d_model]")
@@ -163,17 +167,32 @@ def prox_prepare(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
     for t, shp, nm in ((w_gate, (d_ff, d_model), "w_gate"), (w_up, (d_ff, d_model), "w_up"),
                        (w_down, (d_model, d_ff), "w_down")):
         _need(t, torch.bfloat16, shp, nm)
-    sz = prox_query_sizes(d_model, d_ff)
+    sz = prox_query_sizes(d_model, d_ff, q8)
     dev = w_gate.device
     bufs = {n: torch.empty(sz[n], dtype=torch.uint8, device=dev) for n in sz}
     h = ctypes.c_void_p()
+    name = "prox_prepare_q8" if q8 else "prox_prepare"
     with torch.cuda.device(dev):
-        _check(lib.prox_prepare(d_model, d_ff, _ptr(w_gate), _ptr(w_up), _ptr(w_down),
-                                _ptr(bufs["proxy_codes"]), _ptr(bufs["proxy_scales"]),
-                                _ptr(bufs["gateup"]), _ptr(bufs["down_t"]),
-                                _ptr(bufs["workspace"]), _stream(stream), ctypes.byref(h)),
-               "prox_prepare")
-    return ProxLayer(d_model, d_ff, bufs, h, dev)
+        _check(getattr(lib, name)(d_model, d_ff, _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                  _ptr(bufs["proxy_codes"]), _ptr(bufs["proxy_scales"]),
+                                  _ptr(bufs["gateup"]), _ptr(bufs["down_t"]),
+                                  _ptr(bufs["workspace"]), _stream(stream), ctypes.byref(h)),
+               name)
+    return ProxLayer(d_model, d_ff, bufs, h, dev, q8)
+
+
+def prox_prepare(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
+                 stream=None) -> ProxLayer:
+    """Builds the proxy and Stage-2 layouts of one layer (see prox.h)."""
+    return _prepare(w_gate, w_up, w_down, stream, False)
+
+
+def prox_prepare_q8(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
+                    stream=None) -> ProxLayer:
+    """As prox_prepare with int8 Stage-2 rows (see prox.h); every step call on
+    the returned layer runs Stage 2 on them.  bufs["gateup"] and
+    bufs["down_t"] hold the int8 layouts."""
+    return _prepare(w_gate, w_up, w_down, stream, True)
 
 
 def _x_y(layer: ProxLayer, x, y):

@@ -98,11 +98,23 @@ typedef struct prox_layer prox_layer;
  *   proxy_scales fp16  [G][Fp][2]: (s_gate[c][g], s_up[c][g]); padding 0.
  *   gateup       bf16  [F][2][d]: row c = (W_gate[c][:], W_up[c][:]).
  *   down_t       bf16  [F][d]:    row c = W_down[:][c].
+ * prox_prepare_q8 writes int8 Stage-2 layouts instead of the last two.
+ * Every Stage-2 row r (W_gate[c], W_up[c], W_down[:][c]) is quantized
+ * symmetrically on its own: s_r = fl32(max_j |r_j| / 127) and
+ * q_r[j] = clamp(rne(fl32(r_j / s_r)), -127, 127), q_r = 0 where s_r = 0:
+ *   gateup_q8    [F] rows of 2 d + 16 bytes: int8 q_gate[c][0..d),
+ *                int8 q_up[c][0..d), then fp32 s_gate[c], s_up[c],
+ *                s_down[c] and 4 zero bytes.
+ *   down_q8      int8 [F][d]: row c = q_down[c][:], the codes of W_down[:][c].
  */
 
 /* Sizes of the buffers above for a layer shape.  Host only; queues nothing.
  * Returns PROX_ERR_UNSUPPORTED_SHAPE for shapes outside the limits. */
 PROX_API prox_status prox_query_sizes(int d_model, int d_ff, prox_sizes* out);
+
+/* As prox_query_sizes for prox_prepare_q8: gateup and down_t hold the sizes
+ * of gateup_q8 (d_ff * (2 d_model + 16)) and down_q8 (d_ff * d_model). */
+PROX_API prox_status prox_query_sizes_q8(int d_model, int d_ff, prox_sizes* out);
 
 /*
  * One-off per-layer preparation ("Prox", Abstract: quantized proxy weights
@@ -120,6 +132,24 @@ PROX_API prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, con
                          const void* w_down, void* proxy_codes, void* proxy_scales,
                          void* gateup, void* down_t, void* workspace, prox_stream_t stream,
                          prox_layer** out);
+
+/*
+ * As prox_prepare, with int8 Stage-2 weights ("Prox", Abstract: the method
+ * composes with weight quantization; here the selected rows themselves are
+ * int8, which halves the Stage-2 bytes per channel): gateup_q8
+ * and down_q8 (sizes from prox_query_sizes_q8) receive the int8 layouts
+ * above; the proxy is the same.  Every step entry point (prox_ffn, _ex,
+ * _host, _traced, _resnorm, _debug, _noalloc, prox_dense_ffn,
+ * prox_ffn_phase_times) then runs Stage 2 on the int8 rows:
+ *   g_c = s_gate[c] sum_j q_gate[c][j] x_j,  u_c likewise,
+ *   y   = sum_{c in mask} silu(g_c) u_c s_down[c] q_down[c][:]
+ * in fp32 (each code-times-bf16 product is exact).  The channel mask is the
+ * one of the bf16 layer: it depends on the proxy only.
+ */
+PROX_API prox_status prox_prepare_q8(int d_model, int d_ff, const void* w_gate, const void* w_up,
+                            const void* w_down, void* proxy_codes, void* proxy_scales,
+                            void* gateup_q8, void* down_q8, void* workspace,
+                            prox_stream_t stream, prox_layer** out);
 
 /*
  * The Prox decode step ("Prox", Abstract; Eq. (1) of the PrunePath page for

@@ -59,9 +59,23 @@ def test_query_sizes(lib):
     s = prox.prox_query_sizes(256, 688)  # ragged d_ff: padded to 704 proxy columns
     assert s["proxy_codes"] == 256 * 704 and s["proxy_scales"] == 2 * 704 * 4
     for d, F in ((100, 64), (0, 64), (256, 0), (16384 + 128, 64), (256, 32769)):
-        with pytest.raises(prox.ProxError) as e:
-            prox.prox_query_sizes(d, F)
-        assert e.value.code == prox.PROX_ERR_UNSUPPORTED_SHAPE
+        for q8 in (False, True):
+            with pytest.raises(prox.ProxError) as e:
+                prox.prox_query_sizes(d, F, q8)
+            assert e.value.code == prox.PROX_ERR_UNSUPPORTED_SHAPE
+
+
+def test_query_sizes_q8(lib):
+    """int8 Stage-2 rows: gate|up codes plus 16 bytes of scales per channel,
+    W_down^T codes; the proxy and the workspace are those of the bf16 layer."""
+    from free_swiglu_ffn_prox_b300 import prox
+
+    for d, F in ((4096, 14336), (256, 688), (8192, 28672)):
+        s, s8 = prox.prox_query_sizes(d, F), prox.prox_query_sizes(d, F, q8=True)
+        assert s8["gateup"] == F * (2 * d + 16)
+        assert s8["down_t"] == F * d
+        for n in ("proxy_codes", "proxy_scales", "workspace"):
+            assert s8[n] == s[n]
 
 
 def test_keep_count_agrees_with_oracle(lib):
@@ -98,6 +112,15 @@ def test_bad_arguments_are_rejected_before_any_device_work(lib):
     args[5] = vp(0x10008)
     assert lib.prox_prepare(256, 64, *args, None, ctypes.byref(h)) == 3
     assert lib.prox_prepare(256, 64, *good, None, None) == 1
+    # the int8 preparation checks the same way
+    assert lib.prox_prepare_q8(100, 64, *good, None, ctypes.byref(h)) == 2
+    args = list(good)
+    args[6] = None
+    assert lib.prox_prepare_q8(256, 64, *args, None, ctypes.byref(h)) == 1
+    args = list(good)
+    args[6] = vp(0x10004)
+    assert lib.prox_prepare_q8(256, 64, *args, None, ctypes.byref(h)) == 3
+    assert lib.prox_prepare_q8(256, 64, *good, None, None) == 1
     # calls on a null layer
     assert lib.prox_ffn(None, good[0], ctypes.c_float(0.3), good[1], None) == 1
     assert lib.prox_ffn_ex(None, good[0], ctypes.c_float(0.3), ctypes.c_float(0.5), good[1], None) == 1
