@@ -37,6 +37,9 @@
 //         is subtracted again at the end); one vector atomic per element adds
 //         the CTA's part of y at the end.
 //       A speculative item that the exact mask drops costs bandwidth only.
+//   Stage-2 rows are bf16, or int8 with one fp32 scale per row (the kernels'
+//   Q8 instances): the codes are decoded exactly to fp32 and the scales are
+//   applied to g, u and h.
 //
 // The same Stage-2 code over all channels is the dense baseline (k_dense).
 // Every wait is bounded: a wait that runs out records PROX_ERR_TIMEOUT in
