@@ -76,10 +76,11 @@ def _load():
             lib.oracle_residual_rmsnorm.argtypes = [_i32, _ptr, _ptr, ctypes.c_double, _ptr]
             lib.oracle_quantize_rows_q8.argtypes = [_i32, _i32, _ptr, _ptr, _ptr]
             lib.oracle_sparse_ffn_q8.argtypes = [_i32, _i32] + [_ptr] * 7 + [_i32, _ptr, _ptr, _ptr]
+            lib.oracle_block_topk.argtypes = [_i32, _ptr, _i32, _i32, _ptr, _ptr]
             for name in ("oracle_quantize", "oracle_input_topk", "oracle_proxy_scores",
                          "oracle_channel_topk", "oracle_sparse_ffn", "oracle_dense_ffn",
                          "oracle_prox_ffn", "oracle_residual_rmsnorm", "oracle_quantize_rows_q8",
-                         "oracle_sparse_ffn_q8"):
+                         "oracle_sparse_ffn_q8", "oracle_block_topk"):
                 getattr(lib, name).restype = _i32
             _lib = lib
     return _lib
@@ -182,6 +183,19 @@ def channel_topk(score: np.ndarray, k: int) -> np.ndarray:
     idx = np.empty(k, dtype=np.int32)
     _check(lib.oracle_channel_topk(sc.size, _p(sc), int(k), _p(idx)), "channel_topk")
     return idx
+
+
+def block_topk(score: np.ndarray, bw: int, K: int):
+    """f3: channels of the K blocks of bw contiguous channels whose summed
+    score is largest (ties -> lower block), ascending; returns (idx, S[E])."""
+    lib = _load()
+    sc = _c(score, np.float64).ravel()
+    E = sc.size // int(bw) if bw > 0 else 0
+    idx = np.empty(max(int(K), 0) * max(int(bw), 0), dtype=np.int32)
+    S = np.empty(max(E, 1))
+    _check(lib.oracle_block_topk(sc.size, _p(sc), int(bw), int(K), _p(S), _p(idx)),
+           "block_topk")
+    return idx, S[:E]
 
 
 def sparse_ffn(w_gate, w_up, w_down, x_bits, idx):

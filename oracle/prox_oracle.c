@@ -256,6 +256,43 @@ int oracle_channel_topk(int F, const double* score, int k, int32_t* idx) {
     return topk_ascending(F, score, k, idx);
 }
 
+/* f3: block-granular mask ([PP] Sec. 2.2 Eq. (2): after a permutation the
+ * intermediate dimension splits into E = F / bw contiguous experts of width
+ * bw, and the FFN is the sum of the experts' outputs; Sec. 3.1 activates a
+ * subset of experts).  Reading for the training-free Prox signal: the score
+ * of expert e is the sum of its channels' scores,
+ *   S_e = sum_{c = e bw}^{(e+1) bw - 1} score_c   (fp64, channel order),
+ * the K experts with the largest S_e are kept (ties -> lower expert), and
+ * the mask is every channel of those experts, in ascending channel order
+ * (K bw channels).  The permutation is the identity: the weights passed in
+ * are taken to be already permuted.  block_score (length E) may be NULL. */
+int oracle_block_topk(int F, const double* score, int bw, int K, double* block_score,
+                      int32_t* idx) {
+    if (F <= 0 || !score || !idx || bw < 1 || F % bw != 0) return ORACLE_BAD_ARG;
+    int E = F / bw;
+    if (K < 1 || K > E) return ORACLE_BAD_ARG;
+    double* S = (double*)malloc(sizeof(double) * (size_t)E);
+    int32_t* blocks = (int32_t*)malloc(sizeof(int32_t) * (size_t)K);
+    if (!S || !blocks) {
+        free(S);
+        free(blocks);
+        return ORACLE_BAD_ARG;
+    }
+    for (int e = 0; e < E; ++e) {
+        double acc = 0.0;
+        for (int t = 0; t < bw; ++t) acc += score[(size_t)e * bw + t];
+        S[e] = acc;
+        if (block_score) block_score[e] = acc;
+    }
+    int rc = topk_ascending(E, S, K, blocks);
+    if (rc == ORACLE_OK)
+        for (int i = 0; i < K; ++i)
+            for (int t = 0; t < bw; ++t) idx[(size_t)i * bw + t] = blocks[i] * bw + t;
+    free(S);
+    free(blocks);
+    return rc;
+}
+
 /* a4-a5: Stage 2 ([Prox] Abstract: selected channels computed exactly;
  * [PP] Eq. (1)).  For c in idx (any order, no repeats):
  *   g_c = W_gate[c] . x,  u_c = W_up[c] . x,  h_c = silu(g_c) * u_c

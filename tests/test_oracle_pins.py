@@ -444,3 +444,69 @@ def test_q8_stage2_one_channel_closed_form(oracle_mod):
     expect = np.zeros(d)
     expect[7] = hh * 2.0 * 3
     assert np.allclose(y, expect, rtol=1e-15, atol=0)
+
+
+# ------------------------------------------------------ block-granular mask
+def test_block_topk_golden_cases(oracle_mod):
+    """Hand-worked cases of the block mask (PrunePath Sec. 2.2 Eq. (2) blocks;
+    expert score = sum of its channels' scores, ties to the lower expert)."""
+    n = 0
+    for line in open(os.path.join(GOLDEN, "block_topk_cases.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        bw, K, sc, want = [f.strip() for f in line.split("|")]
+        sc = np.array([float(v) for v in sc.split()])
+        want = np.array([int(v) for v in want.split()], dtype=np.int32)
+        idx, S = oracle_mod.block_topk(sc, int(bw), int(K))
+        assert np.array_equal(idx, want), (line, idx)
+        assert S.size == sc.size // int(bw)
+        n += 1
+    assert n >= 8
+
+
+def test_block_topk_width_one_is_the_channel_topk(oracle_mod):
+    rng = np.random.default_rng(7)
+    sc = np.round(rng.exponential(size=500), 2)  # many exact ties
+    for k in (1, 17, 250, 500):
+        idx, _ = oracle_mod.block_topk(sc, 1, k)
+        assert np.array_equal(idx, oracle_mod.channel_topk(sc, k))
+
+
+def test_block_topk_keeps_whole_blocks_and_agrees_with_block_constant_channel_topk(oracle_mod):
+    """With every channel of a block carrying the same value v_e, the block
+    mask equals the channel top-(K bw): a channel ranking whose ties go to
+    the lower channel takes blocks whole, in order of v_e."""
+    rng = np.random.default_rng(8)
+    for bw, E in ((4, 64), (16, 37), (64, 20)):
+        v = rng.permutation(E).astype(np.float64) + 1.0  # distinct
+        sc = np.repeat(v, bw)
+        for K in (1, E // 3, E):
+            idx, S = oracle_mod.block_topk(sc, bw, K)
+            assert np.array_equal(S, v * bw)
+            assert idx.size == K * bw
+            assert np.array_equal(idx, oracle_mod.channel_topk(sc, K * bw))
+            blocks = idx.reshape(K, bw)
+            assert np.all(blocks == blocks[:, :1] + np.arange(bw))  # whole, contiguous
+
+
+def test_block_topk_follows_a_permutation_of_the_blocks(oracle_mod):
+    """Eq. (2) is stated for any permutation: relabelling the experts relabels
+    the kept set (distinct expert sums, so no tie decides)."""
+    rng = np.random.default_rng(9)
+    bw, E, K = 8, 50, 13
+    sc = rng.random(bw * E)
+    perm = rng.permutation(E)
+    sc_p = sc.reshape(E, bw)[perm].ravel()  # expert e of sc_p is expert perm[e] of sc
+    idx, _ = oracle_mod.block_topk(sc, bw, K)
+    idx_p, _ = oracle_mod.block_topk(sc_p, bw, K)
+    kept = set(idx.reshape(K, bw)[:, 0] // bw)
+    kept_p = set(idx_p.reshape(K, bw)[:, 0] // bw)
+    assert kept == {int(perm[e]) for e in kept_p}
+
+
+def test_block_topk_rejects_ragged_widths(oracle_mod):
+    with pytest.raises(Exception):
+        oracle_mod.block_topk(np.ones(10), 4, 1)  # 10 channels do not split into blocks of 4
+    with pytest.raises(Exception):
+        oracle_mod.block_topk(np.ones(8), 2, 5)   # only 4 blocks
