@@ -24,6 +24,7 @@ through the host-buffer entry point prox_ffn_host (x copied in and y copied
 out every step, inside the timed region); latency and GB/s at keep fractions
 0.5 / 0.3 / 0.1; the in-library dense GEMV and the speedup over it; the
 same step and dense GEMV on layers with int8 Stage-2 rows (prox_prepare_q8);
+the step with block-granular masks of 16 and 64 channels (prox_ffn_blocks);
 the 32-layer stack; and the CPU oracle timed on this host's cores (a
 reported baseline, not the target).
 
@@ -545,6 +546,33 @@ def run_gpu(args):
         if not args.no_q8:
             extras["int8_stage2"] = q8_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak,
                                              l2, ms_per_step, dus)
+
+        # ------------------------------------------------ block-granular masks
+        blocks = {}
+        for bw in (16, 64):
+            E = F // bw
+            kk = bw * keep_count(E, rho)
+            abb = algorithmic_bytes(d, F, kk, kx)["step"]
+
+            def bstep(i, bw=bw):
+                L, x, y = wl.slot(i)
+                prox.prox_ffn_blocks(L, x, bw, rho, y=y)
+
+            n = 4 * CHUNK
+            gs = graphs_for(bstep, n, stream)
+            with torch.cuda.stream(stream):
+                gs[0].replay()
+            torch.cuda.synchronize()
+            m, _, _ = timed_replays(gs, stream)
+            us = m * 1e3 / n
+            blocks[str(bw)] = {"blocks_kept": kk // bw, "of_blocks": E, "k": kk,
+                               "us_per_token": round(us, 3), "alg_bytes": abb,
+                               "gbs": round(abb / (us * 1e-6) / 1e9, 1),
+                               "frac_of_measured": round(abb / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+        for L in wl.layers:
+            if prox.prox_get_status(L) != 0:
+                raise SystemExit("device status set in the block-mask measurement")
+        extras["block_mask"] = blocks
 
         # ------------------------------------------------ 32-layer stack
         if not args.no_stack:

@@ -87,7 +87,7 @@ prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, fl
                      float* h_out, cudaStream_t stream, long long limit_ns, int inject,
                      cudaEvent_t const* ev = nullptr, uint64_t* ts = nullptr,
                      const void* x_prev = nullptr, const float* y_prev = nullptr,
-                     void* x_out = nullptr, float eps = 0.0f) {
+                     void* x_out = nullptr, float eps = 0.0f, int bw = 0) {
     prox::FusedLaunch f;
     f.codes = L->codes;
     f.scales = L->scales;
@@ -99,7 +99,9 @@ prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, fl
     f.x = static_cast<const uint16_t*>(x);
     f.y = y;
     f.kx = prox_keep_count(L->d_model, input_keep);
-    f.k = prox_keep_count(L->d_ff, keep_fraction);
+    f.k = bw > 0 ? bw * prox_keep_count(L->d_ff / bw, keep_fraction)  // whole blocks
+                 : prox_keep_count(L->d_ff, keep_fraction);
+    f.bw = bw;
     f.ws = &L->ws;
     f.kept_out = kept_out;
     f.scores_out = scores_out;
@@ -123,6 +125,18 @@ prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, fl
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
     const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
     return pa < pb + nb && pb < pa + na;
+}
+
+// A block width the fused kernel supports on this layer: a power of two in
+// [4, 256] dividing d_ff, at least one block per CTA, and every CTA's chunk
+// (whole blocks) within the kernel's chunk limit.
+prox_status check_blocks(const prox_layer* L, int bw) {
+    if (bw < 4 || bw > 256 || (bw & (bw - 1)) != 0) return PROX_ERR_INVALID_ARG;
+    if (L->d_ff % bw != 0) return PROX_ERR_UNSUPPORTED_SHAPE;
+    const int E = L->d_ff / bw, nb = L->num_blocks;
+    if (E < nb || bw * ((E + nb - 1) / nb) > prox::fused_max_chunk())
+        return PROX_ERR_UNSUPPORTED_SHAPE;
+    return PROX_OK;
 }
 
 prox_status check_call(const prox_layer* L, const void* x, const float* y) {
@@ -329,6 +343,34 @@ prox_status prox_ffn_debug(const prox_layer* layer, const void* x, float keep_fr
         if (p && !aligned16(p)) return PROX_ERR_MISALIGNED;
     return run_prox(layer, x, keep_fraction, input_keep, y, kept_inputs, scores, idx, h,
                     reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0);
+}
+
+prox_status prox_ffn_blocks(const prox_layer* layer, const void* x, int block_width,
+                            float keep_fraction, float* y, prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    if (!frac_ok(keep_fraction)) return PROX_ERR_INVALID_ARG;
+    st = check_blocks(layer, block_width);
+    if (st != PROX_OK) return st;
+    return run_prox(layer, x, keep_fraction, 0.5f, y, nullptr, nullptr, nullptr, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0, nullptr,
+                    nullptr, nullptr, nullptr, nullptr, 0.0f, block_width);
+}
+
+prox_status prox_ffn_blocks_debug(const prox_layer* layer, const void* x, int block_width,
+                                  float keep_fraction, float* y, float* scores, int32_t* idx,
+                                  float* h, prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    if (!frac_ok(keep_fraction)) return PROX_ERR_INVALID_ARG;
+    st = check_blocks(layer, block_width);
+    if (st != PROX_OK) return st;
+    const void* outs[] = {scores, idx, h};
+    for (const void* p : outs)
+        if (p && !aligned16(p)) return PROX_ERR_MISALIGNED;
+    return run_prox(layer, x, keep_fraction, 0.5f, y, nullptr, scores, idx, h,
+                    reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0, nullptr,
+                    nullptr, nullptr, nullptr, nullptr, 0.0f, block_width);
 }
 
 prox_status prox_residual_rmsnorm(int d_model, const void* x, const float* y, float eps,

@@ -122,6 +122,10 @@ struct FusedParams {
     const uint16_t* x;
     float* y;
     int kx, k;
+    // block-granular mask: channels per block (a power of two, 4..256; chunk
+    // starts are multiples of it) whose summed score ranks the whole block;
+    // 0: the per-channel mask
+    int bw;
     // optional stack glue in front of the step: x = bf16(RMSNorm(x_prev + y_prev))
     const uint16_t* x_prev;  // null: x is given
     const float* y_prev;
@@ -163,12 +167,15 @@ __host__ __device__ __forceinline__ int chunk_begin(int F, int b, int nb) {
 }
 
 // First channel of CTA b's chunk in the fused kernel: chunk starts are
-// multiples of 4 channels (so per-chunk arrays copy in 16-byte pieces); the
-// last chunk ends at F.
-__host__ __device__ __forceinline__ int chunk_lo(int F, int b, int nb) {
-    const int c = 4 * chunk_begin((F + 3) >> 2, b, nb);
+// multiples of al channels (al = 4, so per-chunk arrays copy in 16-byte
+// pieces, or the block width of a block-granular mask, so every chunk holds
+// whole blocks); the last chunk ends at F.
+__host__ __device__ __forceinline__ int chunk_lo(int F, int b, int nb, int al) {
+    const int c = al * chunk_begin((F + al - 1) / al, b, nb);
     return c < F ? c : F;
 }
+
+__host__ __device__ __forceinline__ int chunk_align(int bw) { return bw > 0 ? bw : 4; }
 
 // Speculative items of a chunk of nch channels: its expected share
 // k nch / F of the mask.
@@ -906,7 +913,8 @@ __device__ __forceinline__ int chunk_of(const int* pre, int n, int q) {
 
 // Speculative items of chunk c (the owner's rule).
 __device__ __forceinline__ int chunk_spec(const FusedParams& p, int c, int nb) {
-    return c == 0 ? 0 : spec_count(p.k, chunk_lo(p.F, c + 1, nb) - chunk_lo(p.F, c, nb), p.F);
+    const int al = chunk_align(p.bw);
+    return c == 0 ? 0 : spec_count(p.k, chunk_lo(p.F, c + 1, nb, al) - chunk_lo(p.F, c, nb, al), p.F);
 }
 
 // CTA 0, all threads: the exact channel top-k once every chunk is in (grid
@@ -943,7 +951,7 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
     uint32_t* cand = reinterpret_cast<uint32_t*>(upre + kMaxBlocks + 1);  // [kCandCap]
     for (int i = tid; i < kHistBins + 512; i += kNT) h2[i] = 0u;
     for (int t = tid; t <= nb; t += kNT) {
-        cbeg[t] = chunk_lo(F, t, nb);
+        cbeg[t] = chunk_lo(F, t, nb, chunk_align(p.bw));
         if (t < nb) cspc[t] = chunk_spec(p, t, nb);
     }
     // thread t < nb waits for chunk t's ready flag; then the histogram, all
@@ -1491,7 +1499,8 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     stamp(p.ts, 3);
 
     // ------------------------------------------------ P2: scores + histogram
-    const int cb0 = chunk_lo(F, b, nb), cb1 = chunk_lo(F, b + 1, nb);
+    const int cb0 = chunk_lo(F, b, nb, chunk_align(p.bw));
+    const int cb1 = chunk_lo(F, b + 1, nb, chunk_align(p.bw));
     const int nch = cb1 - cb0;  // <= kMaxChunk (checked by the host)
     const int m = b == 0 ? 0 : spec_count(p.k, nch, F);  // CTA 0 selects instead
     {
@@ -1515,6 +1524,31 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
             if (p.scores_out) p.scores_out[c] = sc;
             ctl.lsc[tid] = sc;
             key = __float_as_uint(sc);
+        }
+        if (p.bw > 0) {
+            // block-granular mask: every channel takes the sum of its block's
+            // scores (blocks are bw consecutive threads, bw | chunk start).
+            // Fixed order: a butterfly over min(bw, 32) lanes (every lane of a
+            // group ends with the same sum), then the warp sums of a wider
+            // block added in warp order.
+            const int bw = p.bw;
+            float sblk = act ? __uint_as_float(key) : 0.0f;
+            for (int o = 1; o < bw && o < 32; o <<= 1) sblk += __shfl_xor_sync(0xffffffffu, sblk, o);
+            if (bw > 32) {
+                if (lane == 0) ctl.warp_tot[wid] = __float_as_uint(sblk);
+                __syncthreads();
+                if (act) {  // tid < nch <= kMaxChunk: warps 0 .. kMaxChunk / 32 - 1
+                    const int w0 = (tid - tid % bw) >> 5;
+                    float t = 0.0f;
+                    for (int w = 0; w < (bw >> 5); ++w) t += __uint_as_float(ctl.warp_tot[w0 + w]);
+                    sblk = t;
+                }
+                __syncthreads();  // ctl.warp_tot is reused below
+            }
+            if (act) {
+                key = __float_as_uint(sblk);
+                ctl.lsc[tid] = sblk;
+            }
         }
         // one reduction per distinct bin in the warp
         const unsigned am = __ballot_sync(0xffffffffu, act);
@@ -1766,6 +1800,7 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     p.y = L.y;
     p.kx = L.kx;
     p.k = L.k;
+    p.bw = L.bw;
     p.x_prev = L.x_prev;
     p.y_prev = L.y_prev;
     p.x_out = L.x_out;

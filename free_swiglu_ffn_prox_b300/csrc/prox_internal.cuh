@@ -190,6 +190,7 @@ struct FusedLaunch {
     const uint16_t* x;
     float* y;
     int kx, k;
+    int bw = 0;          // block-granular mask: channels per block (0: per channel)
     // optional stack glue: x = bf16(RMSNorm(x_prev + y_prev)) computed in the
     // step itself (x unused, x_out receives it); x_prev null: plain step
     const uint16_t* x_prev = nullptr;

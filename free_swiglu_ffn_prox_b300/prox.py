@@ -67,6 +67,8 @@ def _load():
             "prox_ffn_traced": (i32, [vp, vp, f32, f32, vp, ctypes.POINTER(vp), i32, vp]),
             "prox_dense_ffn": (i32, [vp, vp, vp, vp]),
             "prox_ffn_debug": (i32, [vp, vp, f32, f32, vp, vp, vp, vp, vp, vp]),
+            "prox_ffn_blocks": (i32, [vp, vp, i32, f32, vp, vp]),
+            "prox_ffn_blocks_debug": (i32, [vp, vp, i32, f32, vp, vp, vp, vp, vp]),
             "prox_residual_rmsnorm": (i32, [i32, vp, vp, f32, vp, vp]),
             "prox_ffn_resnorm": (i32, [vp, vp, vp, f32, vp, f32, vp, vp]),
             "prox_get_status": (i32, [vp, vp]),
@@ -295,6 +297,36 @@ def prox_ffn_debug(layer: ProxLayer, x: torch.Tensor, keep_fraction: float,
                                   _stream(stream)), "prox_ffn_debug")
     return {"y": y, "kept": kept[:kx], "scores": scores, "idx": idx[:k], "h": h[:k],
             "kx": kx, "k": k}
+
+
+def prox_ffn_blocks(layer: ProxLayer, x: torch.Tensor, block_width: int, keep_fraction: float,
+                    y=None, stream=None):
+    """The step with a block-granular mask: the ceil(keep_fraction E) blocks
+    of block_width contiguous channels with the largest summed proxy score."""
+    y = _x_y(layer, x, y)
+    with torch.cuda.device(layer.device):
+        _check(_load().prox_ffn_blocks(layer.handle, _ptr(x), int(block_width),
+                                       float(keep_fraction), _ptr(y), _stream(stream)),
+               "prox_ffn_blocks")
+    return y
+
+
+def prox_ffn_blocks_debug(layer: ProxLayer, x: torch.Tensor, block_width: int,
+                          keep_fraction: float, stream=None) -> dict:
+    """prox_ffn_blocks plus per-channel scores, the channel list and h."""
+    y = _x_y(layer, x, None)
+    dev = x.device
+    E = layer.d_ff // int(block_width) if block_width > 0 else 0
+    k = int(block_width) * prox_keep_count(E, keep_fraction) if E > 0 else 0
+    scores = torch.empty(layer.d_ff, dtype=torch.float32, device=dev)
+    idx = torch.empty(max(k, 1), dtype=torch.int32, device=dev)
+    h = torch.empty(max(k, 1), dtype=torch.float32, device=dev)
+    with torch.cuda.device(layer.device):
+        _check(_load().prox_ffn_blocks_debug(layer.handle, _ptr(x), int(block_width),
+                                             float(keep_fraction), _ptr(y), _ptr(scores),
+                                             _ptr(idx), _ptr(h), _stream(stream)),
+               "prox_ffn_blocks_debug")
+    return {"y": y, "scores": scores, "idx": idx[:k], "h": h[:k], "k": k}
 
 
 def prox_residual_rmsnorm(x: torch.Tensor, y: torch.Tensor, eps: float = 1e-6, out=None,

@@ -220,6 +220,33 @@ PROX_API prox_status prox_ffn_phase_times(const prox_layer* layer, const void* x
                                  float keep_fraction, float* y, uint64_t* stamps, int dense,
                                  prox_stream_t stream);
 
+/*
+ * The decode step with a block-granular mask ("PrunePath", Sec. 2.2 Eq. (2):
+ * after a channel permutation, d_ff splits into E = d_ff / block_width
+ * contiguous experts; Sec. 3.1 runs a subset of them).  The weights given to
+ * prox_prepare are taken as already permuted.  Stage 1 is unchanged; the
+ * score of expert e is the sum of its channels' proxy scores (fp32, fixed
+ * order); the K = ceil(keep_fraction E) experts of largest score are kept
+ * (ties -> lower expert) and Stage 2 runs over all their channels
+ * (k = K block_width), so its rows are read in contiguous runs.
+ *   block_width  a power of two in [4, 256] (else PROX_ERR_INVALID_ARG)
+ *                dividing d_ff, with E >= the layer's CTA count and every
+ *                CTA's share of whole blocks <= 256 channels (else
+ *                PROX_ERR_UNSUPPORTED_SHAPE): e.g. 4..64 for d_ff 14336 on
+ *                148 SMs.
+ * x, y and the input keep (0.5) as in prox_ffn.
+ */
+PROX_API prox_status prox_ffn_blocks(const prox_layer* layer, const void* x, int block_width,
+                            float keep_fraction, float* y, prox_stream_t stream);
+
+/* prox_ffn_blocks plus, for parity checks, the per-channel proxy scores
+ * (fp32 [d_ff], before the block sums), the selected channels (int32 [k],
+ * ascending) and h (fp32 [k], idx order); each may be NULL. */
+PROX_API prox_status prox_ffn_blocks_debug(const prox_layer* layer, const void* x,
+                                  int block_width, float keep_fraction, float* y,
+                                  float* scores, int32_t* idx, float* h,
+                                  prox_stream_t stream);
+
 /* Dense SwiGLU FFN, Eq. (1) of the PrunePath page over all d_ff channels,
  * streaming the same gateup / down_t buffers (the in-library dense
  * baseline).  x bf16 [d_model], y fp32 [d_model], both device. */
