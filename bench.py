@@ -25,6 +25,7 @@ out every step, inside the timed region); latency and GB/s at keep fractions
 0.5 / 0.3 / 0.1; the in-library dense GEMV and the speedup over it; the
 same step and dense GEMV on layers with int8 Stage-2 rows (prox_prepare_q8);
 the step with block-granular masks of 16 and 64 channels (prox_ffn_blocks);
+a batch of 8 tokens with per-token masks (prox_ffn_batch);
 the 32-layer stack; and the CPU oracle timed on this host's cores (a
 reported baseline, not the target).
 
@@ -573,6 +574,26 @@ def run_gpu(args):
             if prox.prox_get_status(L) != 0:
                 raise SystemExit("device status set in the block-mask measurement")
         extras["block_mask"] = blocks
+
+        # ------------------------------------------------ batch of 8 tokens, per-token masks
+        Bt = 8
+        xb = torch.stack([wl.xs[i % N_X] for i in range(Bt)])
+        yb = torch.empty(Bt, d, dtype=torch.float32, device=dev)
+
+        def batch_step(i):
+            prox.prox_ffn_batch(wl.slot(i)[0], xb, rho, y=yb)
+
+        n = CHUNK // 2
+        gs = graphs_for(batch_step, n, stream)
+        with torch.cuda.stream(stream):
+            gs[0].replay()
+        torch.cuda.synchronize()
+        m, _, _ = timed_replays(gs, stream)
+        us = m * 1e3 / n
+        extras["batch8_per_token_masks"] = {
+            "us_per_call": round(us, 3), "us_per_token": round(us / Bt, 3),
+            "tokens_per_s": round(Bt * 1e6 / us, 1),
+            "note": "one persistent launch per token; the weights cycle through the layer copies"}
 
         # ------------------------------------------------ 32-layer stack
         if not args.no_stack:

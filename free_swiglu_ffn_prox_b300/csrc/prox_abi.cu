@@ -345,6 +345,25 @@ prox_status prox_ffn_debug(const prox_layer* layer, const void* x, float keep_fr
                     reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0);
 }
 
+prox_status prox_ffn_batch(const prox_layer* layer, const void* x, int batch,
+                           float keep_fraction, float* y, prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    if (batch < 1 || !frac_ok(keep_fraction)) return PROX_ERR_INVALID_ARG;
+    const size_t d = (size_t)layer->d_model;
+    if ((d * 2) % 16 != 0) return PROX_ERR_MISALIGNED;  // every token's x 16-byte aligned
+    const uint16_t* xs = static_cast<const uint16_t*>(x);
+    // token t's own mask: one step per token, in order on the stream (the
+    // layer's workspace is reused token after token)
+    for (int t = 0; t < batch; ++t) {
+        st = run_prox(layer, xs + (size_t)t * d, keep_fraction, 0.5f, y + (size_t)t * d, nullptr,
+                      nullptr, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream),
+                      prox::kWaitLimitNs, 0);
+        if (st != PROX_OK) return st;
+    }
+    return PROX_OK;
+}
+
 prox_status prox_ffn_blocks(const prox_layer* layer, const void* x, int block_width,
                             float keep_fraction, float* y, prox_stream_t stream) {
     prox_status st = check_call(layer, x, y);

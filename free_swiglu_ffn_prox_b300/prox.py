@@ -68,6 +68,7 @@ def _load():
             "prox_dense_ffn": (i32, [vp, vp, vp, vp]),
             "prox_ffn_debug": (i32, [vp, vp, f32, f32, vp, vp, vp, vp, vp, vp]),
             "prox_ffn_blocks": (i32, [vp, vp, i32, f32, vp, vp]),
+            "prox_ffn_batch": (i32, [vp, vp, i32, f32, vp, vp]),
             "prox_ffn_blocks_debug": (i32, [vp, vp, i32, f32, vp, vp, vp, vp, vp]),
             "prox_residual_rmsnorm": (i32, [i32, vp, vp, f32, vp, vp]),
             "prox_ffn_resnorm": (i32, [vp, vp, vp, f32, vp, f32, vp, vp]),
@@ -297,6 +298,22 @@ def prox_ffn_debug(layer: ProxLayer, x: torch.Tensor, keep_fraction: float,
                                   _stream(stream)), "prox_ffn_debug")
     return {"y": y, "kept": kept[:kx], "scores": scores, "idx": idx[:k], "h": h[:k],
             "kx": kx, "k": k}
+
+
+def prox_ffn_batch(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, y=None,
+                   stream=None):
+    """Per-token Prox steps over a batch: x bf16 [B, d_model] -> y fp32 [B, d_model]."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError("x must be a [batch, d_model] tensor")
+    B = x.shape[0]
+    _need(x, torch.bfloat16, (B, layer.d_model), "x")
+    if y is None:
+        y = torch.empty(B, layer.d_model, dtype=torch.float32, device=x.device)
+    _need(y, torch.float32, (B, layer.d_model), "y")
+    with torch.cuda.device(layer.device):
+        _check(_load().prox_ffn_batch(layer.handle, _ptr(x), int(B), float(keep_fraction),
+                                      _ptr(y), _stream(stream)), "prox_ffn_batch")
+    return y
 
 
 def prox_ffn_blocks(layer: ProxLayer, x: torch.Tensor, block_width: int, keep_fraction: float,

@@ -221,6 +221,17 @@ PROX_API prox_status prox_ffn_phase_times(const prox_layer* layer, const void* x
                                  prox_stream_t stream);
 
 /*
+ * Batch > 1 decode with per-token masks: for each of the `batch` tokens
+ * x[t] (bf16 [batch][d_model], rows contiguous, device) its own Prox step
+ * (Stage 1 mask of that token, Stage 2 on its selected channels) writes
+ * y[t] (fp32 [batch][d_model], device); keep fraction as in prox_ffn.  The
+ * steps run one after another on the stream (one persistent launch per
+ * token).  Identical to prox_ffn called per token.
+ */
+PROX_API prox_status prox_ffn_batch(const prox_layer* layer, const void* x, int batch,
+                           float keep_fraction, float* y, prox_stream_t stream);
+
+/*
  * The decode step with a block-granular mask ("PrunePath", Sec. 2.2 Eq. (2):
  * after a channel permutation, d_ff splits into E = d_ff / block_width
  * contiguous experts; Sec. 3.1 runs a subset of them).  The weights given to

@@ -130,6 +130,7 @@ def test_bad_arguments_are_rejected_before_any_device_work(lib):
     assert lib.prox_ffn_traced(None, good[0], ctypes.c_float(0.3), ctypes.c_float(0.5), good[1],
                                evs, 5, None) == 1
     assert lib.prox_ffn_blocks(None, good[0], 64, ctypes.c_float(0.3), good[1], None) == 1
+    assert lib.prox_ffn_batch(None, good[0], 4, ctypes.c_float(0.3), good[1], None) == 1
     assert lib.prox_ffn_blocks_debug(None, good[0], 64, ctypes.c_float(0.3), good[1], None, None,
                                      None, None) == 1
     assert lib.prox_get_status(None, None) == 1
