@@ -139,8 +139,8 @@ PROX_API prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, con
  * int8, which halves the Stage-2 bytes per channel): gateup_q8
  * and down_q8 (sizes from prox_query_sizes_q8) receive the int8 layouts
  * above; the proxy is the same.  Every step entry point (prox_ffn, _ex,
- * _host, _traced, _resnorm, _debug, _noalloc, prox_dense_ffn,
- * prox_ffn_phase_times) then runs Stage 2 on the int8 rows:
+ * _host, _traced, _resnorm, _debug, _noalloc, _batch, _blocks,
+ * prox_dense_ffn, prox_ffn_phase_times) then runs Stage 2 on the int8 rows:
  *   g_c = s_gate[c] sum_j q_gate[c][j] x_j,  u_c likewise,
  *   y   = sum_{c in mask} silu(g_c) u_c s_down[c] q_down[c][:]
  * in fp32 (each code-times-bf16 product is exact).  The channel mask is the

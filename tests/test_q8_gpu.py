@@ -181,3 +181,31 @@ def test_q8_full_size_llama3_8b(prox):
     q8 = _check_layouts(L8, bits)
     x = synth.hidden(shape, seed=1)
     _check_q8_step(prox, L8, L, q8, bits, x, 0.3)
+
+
+def test_q8_layer_with_block_mask_and_batch(prox):
+    """The int8 layer through the block-mask and batch entry points: the
+    block mask is the bf16 layer's (it depends on the proxy only), y matches
+    the oracle's int8 Stage 2 on it, and a batch equals per-token steps."""
+    d, F, bw, rho = 2048, 5000, 8, 0.3
+    (wg, wu, wd), bits = _weights(d, F, seed=41)
+    L8 = prox.prox_prepare_q8(wg.cuda(), wu.cuda(), wd.cuda())
+    L = prox.prox_prepare(wg.cuda(), wu.cuda(), wd.cuda())
+    torch.cuda.synchronize()
+    q8 = oracle.stage2_q8(*bits)
+    x = synth.make_x(d, 20, 20.0, 42)
+    r8 = prox.prox_ffn_blocks_debug(L8, x.cuda(), bw, rho)
+    r = prox.prox_ffn_blocks_debug(L, x.cuda(), bw, rho)
+    torch.cuda.synchronize()
+    assert prox.prox_get_status(L8) == 0 and prox.prox_get_status(L) == 0
+    idx = r8["idx"].cpu().numpy()
+    assert np.array_equal(idx, r["idx"].cpu().numpy())
+    _, y_or = oracle.sparse_ffn_q8(q8, host_bits(x), idx)
+    mx, rl = y_errors(r8["y"].cpu().numpy(), y_or)
+    assert mx <= 1e-3 * max(1.0, np.abs(y_or).max()) and rl <= RTOL_L2_Y, (mx, rl)
+    xs = torch.stack([synth.make_x(d, 20, 20.0, 43 + t) for t in range(3)]).cuda()
+    yb = prox.prox_ffn_batch(L8, xs, rho)
+    ys = [prox.prox_ffn(L8, xs[t], rho) for t in range(3)]
+    torch.cuda.synchronize()
+    for t in range(3):
+        assert torch.allclose(yb[t], ys[t], rtol=1e-5, atol=1e-6 * float(ys[t].abs().max()))
