@@ -1,6 +1,9 @@
 /*
- * prox.h -- C ABI of libprox: two-stage sparse SwiGLU FFN decode (batch 1)
- * on NVIDIA B300 (sm_103a).
+ * prox.h -- C ABI of libprox: two-stage sparse SwiGLU FFN decode (batch 1;
+ * prox_ffn_batch runs a batch token by token) on NVIDIA B300 (sm_103a).
+ * Variants of the same step: int8 Stage-2 rows (prox_prepare_q8), block-
+ * granular channel masks (prox_ffn_blocks), and the residual + RMSNorm glue
+ * of a layer stack fused in front of the step (prox_ffn_resnorm).
  *
  * The method: "Prox: Training-Free FFN Activation Sparsity via Approximate
  * Intermediate-Channel Salience in LLMs", Abstract.  Stage 1 builds one
