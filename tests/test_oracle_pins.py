@@ -394,6 +394,21 @@ def test_q8_quantizer_invariants(oracle_mod):
         assert np.all(err <= float(s[r]) * (0.5 + 127 * 2.0 ** -24))
 
 
+def test_q8_quantizer_hand_worked_row(oracle_mod):
+    """A row of multiples of 2^-7 whose largest magnitude is 127 * 2^-6: the
+    scale is exactly 2^-6, every quotient w / s is exact, and the codes below
+    are worked out by hand.  Half-way quotients go to the even integer
+    (2.5 -> 2, 3.5 -> 4, -2.5 -> -2, 0.5 -> 0, 1.5 -> 2), whole ones stay."""
+    u = 2.0 ** -6
+    row = np.array([127, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, -127, 0, 64, -0.5, 126.5]) * u
+    want = np.array([127, 2, 4, -2, -4, 0, 2, -127, 0, 64, 0, 126], dtype=np.int8)
+    bits = oracle_mod.double_to_bf16(row.reshape(1, -1))
+    assert np.array_equal(oracle_mod.bf16_bits_to_f64(bits).ravel(), row)  # exact in bf16
+    q, s = oracle_mod.quantize_rows_q8(bits)
+    assert s[0] == np.float32(u)
+    assert np.array_equal(q[0], want)
+
+
 def test_q8_stage2_reduces_to_bf16_stage2_on_exact_weights(oracle_mod):
     """Weights w = 2^-6 q_true with integer |q_true| <= 127 and every row (and
     W_down column) reaching 127 are exact in bf16 and quantize exactly (s =
