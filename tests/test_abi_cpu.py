@@ -141,3 +141,16 @@ def test_bad_arguments_are_rejected_before_any_device_work(lib):
     f = ctypes.c_float
     assert lib.prox_ffn_resnorm(None, good[0], good[1], f(1e-6), good[2], f(0.3), good[3], None) == 1
     lib.prox_destroy(None)  # accepted, no-op
+
+
+def test_no_alloc_scratch_limit_as_documented(lib):
+    """prox_ffn_noalloc's 4 MiB scratch holds the workspace of every d_ff up to
+    28480 at any supported d_model, and not that of the d_ff 28672 shapes."""
+    from free_swiglu_ffn_prox_b300 import prox
+
+    lim = 4 << 20
+    for d in (128, 4096, 8192, 10496):
+        assert prox.prox_query_sizes(d, 28480)["workspace"] <= lim
+        assert prox.prox_query_sizes(d, 28672)["workspace"] > lim
+    for d, F in ((4096, 11008), (4096, 14336)):
+        assert prox.prox_query_sizes(d, F)["workspace"] <= lim
