@@ -320,10 +320,10 @@ PROX_API prox_status prox_ffn_resnorm(const prox_layer* layer, const void* x_pre
  *   y  fp32 [d_model], device, overwritten as by prox_ffn.
  * Limits and rules:
  *   - the layer's workspace (prox_query_sizes().workspace) must fit in
- *     4 MiB: every d_ff up to 28480 at any supported d_model does (the
- *     Llama-2-7B and Llama-3-8B shapes do; the Llama-3-70B shape, d_ff
- *     28672, does not); larger layers return PROX_ERR_UNSUPPORTED_SHAPE and
- *     queue nothing;
+ *     4 MiB: every d_ff up to 28352 at any supported d_model does, so the
+ *     Llama-2-7B and Llama-3-8B shapes do; d_ff 28672 fits only with
+ *     d_model <= 3968, so the Llama-3-70B shape does not; larger layers
+ *     return PROX_ERR_UNSUPPORTED_SHAPE and queue nothing;
  *   - the layer's device must be the current device (else
  *     PROX_ERR_INVALID_ARG);
  *   - the first call on a device looks up the array's device address
