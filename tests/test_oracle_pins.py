@@ -361,6 +361,77 @@ def test_residual_rmsnorm_closed_forms(oracle_mod):
     assert np.all(np.sign(o1[np.abs(z) > 1e-3]) == np.sign(z[np.abs(z) > 1e-3]))
 
 
+def _rmsnorm_cases():
+    cases = []
+    for line in open(os.path.join(GOLDEN, "rmsnorm_cases.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        eps, xs, ys, want = (f.split() for f in line.split("|"))
+        cases.append((float(eps[0]), [float(v) for v in xs], [float(v) for v in ys],
+                      np.array([int(h, 16) for h in want], dtype=np.uint16)))
+    return cases
+
+
+def test_residual_rmsnorm_golden_cases(oracle_mod):
+    """The stack glue against hand-worked values (tests/golden/rmsnorm_cases.txt)."""
+    for eps, xs, ys, want in _rmsnorm_cases():
+        got = oracle_mod.residual_rmsnorm(_bf16_bits(np.array(xs)), np.array(ys), eps)
+        assert np.array_equal(got, want), (eps, xs, ys, [hex(v) for v in got])
+
+
+def _bf16_rne_py(v: float) -> int:
+    """bf16 bits of a double, round to nearest even (plain integer arithmetic)."""
+    if v == 0.0:
+        return 0
+    sign = 0x8000 if v < 0 else 0
+    e = math.floor(math.log2(abs(v)))
+    q = abs(v) / 2.0 ** e * 128.0
+    n = math.floor(q)
+    if q - n > 0.5 or (q - n == 0.5 and n % 2 == 1):
+        n += 1
+    if n == 256:
+        n, e = 128, e + 1
+    return sign | ((e + 127) << 7) | (n - 128)
+
+
+def test_residual_rmsnorm_golden_cases_reject_plausible_mistakes():
+    """Each plausible slip in the glue (mean over d - 1, eps outside the root
+    or dropped, the residual dropped, truncation instead of rounding, a
+    division by the mean square) disagrees with at least one golden case, so
+    the golden cases pin the definition and not just its shape."""
+    def glue(xs, ys, eps, mean_div=0, eps_out=False, no_eps=False, no_res=False,
+             trunc=False, no_sqrt=False):
+        z = [(0.0 if no_res else a) + b for a, b in zip(xs, ys)]
+        ms = sum(t * t for t in z) / (len(z) - mean_div)
+        if no_eps:
+            den = math.sqrt(ms)
+        elif eps_out:
+            den = math.sqrt(ms) + eps
+        elif no_sqrt:
+            den = ms + eps
+        else:
+            den = math.sqrt(ms + eps)
+        out = []
+        for t in z:
+            v = t / den if den > 0 else 0.0
+            if trunc:
+                b = int(np.float32(v).view(np.uint32)) >> 16
+            else:
+                b = _bf16_rne_py(v)
+            out.append(b)
+        return np.array(out, dtype=np.uint16)
+
+    cases = _rmsnorm_cases()
+    # the faithful restatement reproduces every case
+    for eps, xs, ys, want in cases:
+        assert np.array_equal(glue(xs, ys, eps), want)
+    for slip in ({"mean_div": 1}, {"eps_out": True}, {"no_eps": True}, {"no_res": True},
+                 {"trunc": True}, {"no_sqrt": True}):
+        assert any(not np.array_equal(glue(xs, ys, eps, **slip), want)
+                   for eps, xs, ys, want in cases), slip
+
+
 # ---------------------------------------------------------------- int8 Stage 2
 def _exact_bf16_bits(v):
     """bf16 bit patterns of float values that are exact in bf16."""
