@@ -17,7 +17,13 @@
 // must not pass `g_scratch` itself to a kernel (in host code the name is a
 // host-side stand-in, not a device address); the device address is looked up
 // once per device with cudaGetSymbolAddress, on the first call made on that
-// device, which should therefore come before any stream capture.
+// device, which should therefore come before any stream capture.  The address
+// is kept together with the CUDA context it belongs to: after a
+// cudaDeviceReset the device's next context loads the library's module again,
+// so a call that finds a different current context looks the address up anew
+// (again a set-up call, to be made outside any capture).
+#include <cuda.h>
+
 #include <mutex>
 
 #include "prox_internal.cuh"
@@ -32,15 +38,40 @@ static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
+CUcontext g_ctx[kMaxDevices] = {};  // the context each address belongs to
 
-// Device address of g_scratch on the current device (set up on first use).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// The current CUDA context (the driver's cuCtxGetCurrent, reached through
+// the runtime, so the library needs no link against the driver library).
+cudaError_t current_context(CUcontext* out) {
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e =
+            cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+            return e != cudaSuccess ? e : cudaErrorNotSupported;
+        fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    }
+    return fn(out) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of g_scratch on the current device: set up on the first
+// call in each context of the device, then reused.
 cudaError_t scratch_address(int dev, void** out) {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_addr[dev]) {
+    CUcontext ctx = nullptr;
+    cudaError_t e = current_context(&ctx);  // null if this thread has no context yet
+    if (e != cudaSuccess) return e;
+    if (!g_addr[dev] || !ctx || g_ctx[dev] != ctx) {
         void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+        e = cudaGetSymbolAddress(&p, g_scratch);  // makes the primary context current if needed
+        if (e == cudaSuccess) e = current_context(&ctx);
         if (e != cudaSuccess) return e;
         g_addr[dev] = p;
+        g_ctx[dev] = ctx;
     }
     *out = g_addr[dev];
     return cudaSuccess;
