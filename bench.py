@@ -361,22 +361,34 @@ def run_phases(args):
         prox.prox_ffn(L, x, args.keep_fraction, y=y)
     torch.cuda.synchronize()
     out = {"workload": f"{shape.name} keep_fraction {args.keep_fraction}", "unit": "us",
-           "phases": list(prox.PHASES), "steps": {}}
+           "phases": list(prox.PHASES),
+           "how": "per step: median (and max) over the CTAs that stamp a phase, us after the "
+                  "earliest CTA start; then the median over 8 steps", "steps": {}}
     for mode in ("prox", "dense"):
-        rows = []
+        rows, rows_max = [], []
         for i in range(8):
             L, x, _ = wl.slot(i)
             _, ts = prox.prox_ffn_phase_times(L, x, args.keep_fraction, dense=(mode == "dense"))
             torch.cuda.synchronize()
             t = ts.cpu().numpy().astype(np.int64)
             t0 = t[:, 0].min()
-            rows.append([float(np.median(t[:, j] - t0)) / 1e3 if (t[:, j] != 0).all() else None
-                         for j in range(prox.PROX_PHASE_STAMPS)])
-        med = []
-        for j in range(prox.PROX_PHASE_STAMPS):
-            v = [r[j] for r in rows if r[j] is not None]
-            med.append(round(float(np.median(v)), 2) if v else None)
-        out["steps"][mode] = dict(zip(prox.PHASES, med))
+            med_r, max_r = [], []
+            for j in range(prox.PROX_PHASE_STAMPS):
+                v = t[:, j][t[:, j] != 0] - t0
+                med_r.append(float(np.median(v)) / 1e3 if v.size else None)
+                max_r.append(float(v.max()) / 1e3 if v.size else None)
+            rows.append(med_r)
+            rows_max.append(max_r)
+
+        def agg(rs):
+            res = []
+            for j in range(prox.PROX_PHASE_STAMPS):
+                v = [r[j] for r in rs if r[j] is not None]
+                res.append(round(float(np.median(v)), 2) if v else None)
+            return dict(zip(prox.PHASES, res))
+
+        out["steps"][mode] = agg(rows)
+        out["steps"][mode + "_max_over_ctas"] = agg(rows_max)
     print(json.dumps(out), flush=True)
 
 
@@ -526,6 +538,22 @@ def run_gpu(args):
                               "frac_of_measured": round(abf / (us * 1e-6) / 1e9 / hbm_peak, 4)}
         extras["keep_fraction_sweep"] = sweep
 
+        # ------------------------------------------------ spread of the headline
+        reps = []
+        for _ in range(20):
+            m, _, _ = timed_replays(seq, stream)
+            reps.append(m * 1e3 / K)
+        q = statistics.quantiles(reps, n=10)
+        extras["headline_spread"] = {
+            "us_per_step_p10": round(q[0], 3), "us_per_step_median": round(statistics.median(reps), 3),
+            "us_per_step_p90": round(q[-1], 3), "replays": len(reps),
+            "note": "the timed K-step graph sequence replayed 20 more times, each timed alone"}
+
+        # ------------------------------------------------ the other layer shapes
+        if not args.no_shapes:
+            extras["shapes"] = {s.name: shape_sweep(prox, synth, s, dev, stream, hbm_peak, l2)
+                                for s in (synth.LLAMA2_7B, synth.LLAMA3_70B)}
+
         # ------------------------------------------------ dense GEMV baseline
         def dstep(i):
             L, x, y = wl.slot(i)
@@ -640,6 +668,11 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(synth, shape, rho, kappa, budget_s=args.cpu_budget)
+        try:
+            extras["cpu_baseline_all_cores"] = cpu_baseline_all_cores(
+                shape, rho, kappa, budget_s=args.cpu_budget)
+        except Exception as ex:  # reported, not fatal: the single-core figure stands
+            extras["cpu_baseline_all_cores"] = {"error": repr(ex)[:200]}
 
     if rank == 0:
         out = {
@@ -671,6 +704,77 @@ def run_gpu(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def shape_sweep(prox, synth, shape, dev, stream, hbm_peak, l2):
+    """Latency, tokens/s, GB/s and the fraction of measured HBM bandwidth of
+    the decode step at the shape's keep fractions, and of the dense GEMV, on
+    another layer shape; the steps cycle through enough prepared copies of
+    the layer that their selected bytes exceed 4 x L2 (the same rotation as
+    the headline)."""
+    import torch
+
+    d, F = shape.d_model, shape.d_ff
+    kx = keep_count(d, 0.5)
+    ab03 = algorithmic_bytes(d, F, keep_count(F, 0.3), kx)["step"]
+    R = 2
+    while R < 16 and R * ab03 < 4 * l2:
+        R *= 2
+    layers = []
+    for r in range(R):
+        wg, wu, wd = synth.layer(shape, seed=r, device=dev)
+        layers.append(prox.prox_prepare(wg, wu, wd))
+        del wg, wu, wd
+    xs = [synth.hidden(shape, seed=1 + i, device="cpu").to(dev) for i in range(N_X)]
+    ys = [torch.empty(d, dtype=torch.float32, device=dev) for _ in range(N_X)]
+    torch.cuda.synchronize()
+    out = {"workload": f"{shape.name} batch-1 decode, input_keep 0.5 (k_x={kx}), int4 g128 proxy",
+           "layer_copies": R, "keep_fraction": {}}
+    n = 2 * CHUNK
+    for fr in shape.keep_fractions:
+        k = keep_count(F, fr)
+        ab = algorithmic_bytes(d, F, k, kx)["step"]
+
+        def fn(i, fr=fr):
+            prox.prox_ffn(layers[i % R], xs[i % N_X], fr, y=ys[i % N_X])
+
+        with torch.cuda.stream(stream):
+            for i in range(4):
+                fn(i)
+        torch.cuda.synchronize()
+        gs = graphs_for(fn, n, stream)
+        with torch.cuda.stream(stream):
+            gs[0].replay()
+        torch.cuda.synchronize()
+        m, _, _ = timed_replays(gs, stream)
+        us = m * 1e3 / n
+        gbs = ab / (us * 1e-6) / 1e9
+        out["keep_fraction"][str(fr)] = {"k": k, "us_per_token": round(us, 3),
+                                         "tokens_per_s": round(1e6 / us, 1), "alg_bytes": ab,
+                                         "gbs": round(gbs, 1),
+                                         "frac_of_measured": round(gbs / hbm_peak, 4),
+                                         "frac_of_8tbs_spec": round(gbs / SPEC_HBM_GBS, 4)}
+
+    def dn(i):
+        prox.prox_dense_ffn(layers[i % R], xs[i % N_X], y=ys[i % N_X])
+
+    gs = graphs_for(dn, CHUNK, stream)
+    with torch.cuda.stream(stream):
+        gs[0].replay()
+    torch.cuda.synchronize()
+    m, _, _ = timed_replays(gs, stream)
+    dus = m * 1e3 / CHUNK
+    dab = algorithmic_bytes(d, F, F, kx)["dense"]
+    out["dense"] = {"us_per_token": round(dus, 3), "gbs": round(dab / (dus * 1e-6) / 1e9, 1),
+                    "frac_of_measured": round(dab / (dus * 1e-6) / 1e9 / hbm_peak, 4)}
+    for fr, v in out["keep_fraction"].items():
+        v["speedup_over_dense"] = round(dus / v["us_per_token"], 3)
+    for L in layers:
+        if prox.prox_get_status(L) != 0:
+            raise SystemExit(f"device status set in the {shape.name} sweep")
+    del layers
+    torch.cuda.empty_cache()
+    return out
 
 
 def q8_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak, l2, bf16_us_per_step,
@@ -809,6 +913,58 @@ def cpu_baseline(synth, shape, rho, kappa, budget_s=15.0, min_tokens=2):
             "host_cores_available": len(os.sched_getaffinity(0))}
 
 
+def _oracle_worker(args):
+    """One host core: the oracle on its own stream of tokens for `budget_s`
+    seconds of oracle time (the layer regenerated from its seed, the proxy
+    built untimed).  Runs in a spawned process."""
+    shape_name, rho, kappa, budget_s, worker = args
+    import sys as _sys
+
+    if ROOT not in _sys.path:
+        _sys.path.insert(0, ROOT)
+    import oracle
+    from free_swiglu_ffn_prox_b300 import synth
+
+    shape = synth.SHAPES[shape_name]
+    wg, wu, wd = synth.layer(shape, seed=0, device="cpu")
+    bits = [synth.bits(t) for t in (wg, wu, wd)]
+    del wg, wu, wd
+    px = oracle.Proxy(bits[0], bits[1])
+    n, spent = 0, 0.0
+    while spent < budget_s or n < 1:
+        xb = synth.bits(synth.hidden(shape, seed=1 + 1000 * worker + n))
+        t = time.perf_counter()
+        oracle.prox_ffn(*bits, xb, rho, kappa, proxy=px)
+        spent += time.perf_counter() - t
+        n += 1
+    return n, spent
+
+
+def cpu_baseline_all_cores(shape, rho, kappa, budget_s=10.0, max_workers=None):
+    """The oracle as it stands, one independent process per host core (each
+    on its own tokens): tokens/s of all of them together."""
+    import multiprocessing as mp
+
+    import oracle
+
+    oracle.build()  # compile once, before the workers load it
+    cores = len(os.sched_getaffinity(0))
+    nw = cores if max_workers is None else max(1, min(cores, max_workers))
+    ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
+    t0 = time.perf_counter()
+    with ctx.Pool(nw) as pool:
+        res = pool.map(_oracle_worker, [(shape.name, rho, kappa, budget_s, w) for w in range(nw)])
+    wall = time.perf_counter() - t0
+    # every worker ran about budget_s of oracle time at once: the aggregate rate
+    # is the sum of the per-worker rates
+    rate = sum(n / sp for n, sp in res)
+    tokens = sum(n for n, _ in res)
+    return {"value": round(rate, 4), "unit": UNIT, "cores": nw, "kind": "oracle",
+            "sample": f"{tokens} decode tokens through one {shape.name} layer at keep_fraction "
+                      f"{rho}, {nw} processes (one per host core) each timing ~{budget_s:.0f} s "
+                      f"of oracle work; wall {wall:.1f} s including set-up"}
+
+
 def run_reference(args):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -828,7 +984,8 @@ def run_reference(args):
     del wg, wu, wd
     px = oracle.Proxy(bits[0], bits[1])
     xs = [synth.bits(synth.hidden(shape, seed=1 + i)) for i in range(N_X)]
-    for i in range(min(max(3, args.warmup), 3)):
+    W = max(3, args.warmup)
+    for i in range(W):
         oracle.prox_ffn(*bits, xs[i % N_X], rho, kappa, proxy=px)
     t0 = time.perf_counter()
     n = 0
@@ -843,7 +1000,7 @@ def run_reference(args):
               f"through one {shape.name} layer, keep_fraction {rho}")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
-        "n_gpus": ws, "steps": n, "warmup": 3, "ms_per_step": round(el / n * 1e3, 3),
+        "n_gpus": ws, "steps": n, "warmup": W, "ms_per_step": round(el / n * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {
             "workload": f"llama3_8b_ffn_d{d}_f{F} batch-1 decode, keep_fraction {rho} (k={k}), "
@@ -872,6 +1029,8 @@ def main():
                     help="skip the 32-layer stack measurement in the extras")
     ap.add_argument("--no-q8", action="store_true",
                     help="skip the int8 Stage-2 measurement in the extras")
+    ap.add_argument("--no-shapes", action="store_true",
+                    help="skip the Llama-2-7B and Llama-3-70B sweeps in the extras")
     ap.add_argument("--phases", action="store_true",
                     help="print the per-phase timeline of the decode kernel instead")
     args = ap.parse_args()

@@ -72,7 +72,7 @@ constexpr int kHistBins = 2048;
 constexpr int kXGroups = 3;               // 8-element x groups per thread: d <= 8 * 3 * kNT
 static_assert(kHistBins <= kHistWords, "histogram words");
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr int kPhaseStamps = 10;
+constexpr int kPhaseStamps = 16;
 
 // Phase timestamp (tracing only): thread 0 of the CTA stores %globaltimer.
 __device__ __forceinline__ void stamp(uint64_t* ts, int i) {
@@ -1005,6 +1005,7 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
         return false;
     };
     if (!landed(&ctl.sel_ld)) return false;
+    if (tid == 0) stamp_here(p.ts, 14);
     auto broken = [&]() {
         if (tid == 0) {
             record_status(p.status, PROX_ERR_DEVICE_CHECK);
@@ -1059,6 +1060,7 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
     if (ctl.sel[0] == 0xffffffffu) return broken();
     const uint32_t T = (pre << 9) | ctl.sel[0];
     const int r = (int)ctl.sel[1];  // keys equal to T to keep, lowest channels first
+    if (tid == 0) stamp_here(p.ts, 15);
     // per chunk: keys above and equal to T (T lies in the digit-1 bin, so
     // every key before the chunk's candidates is above it)
     if (tid < nb) {
@@ -1288,6 +1290,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         mk = __reduce_max_sync(0xffffffffu, mk);
         if (lane == 0) atomicMax(&ctl.sel[3], mk);
         __syncthreads();
+        stamp(p.ts, 10);
         if (tid == 0) {  // power-of-two prescale: max|x| * 2^shift in [2^14, 2^15)
             const uint32_t mx = ctl.sel[3];
             int sh = 0;
@@ -1441,6 +1444,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
 #pragma unroll 1
             for (int q = q_beg; q < q_end; ++q) {
                 cp_async_wait_group<kRing - 1>();  // row q has landed
+                if (q == q_beg) stamp(p.ts, 11);
                 const uint4 w = my[(size_t)s * kNT];
                 const uint32_t kp = kept[q];
                 const int qn = q + kRing;
@@ -1461,6 +1465,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
             }
             cp_async_wait_group<0>();
             flush();
+            stamp(p.ts, 12);
         }
         // the scale copy must have landed before this shared memory is reused
         if (smem_scales && !scales_in)
@@ -1572,6 +1577,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         fence_mbar_init();
     }
     __syncthreads();
+    stamp(p.ts, 13);
     // local rank of each chunk channel (key descending, channel ascending: a
     // total order, so the ranks are a permutation), RT threads per channel
     // (consecutive lanes) each comparing a strided part of the chunk.  The

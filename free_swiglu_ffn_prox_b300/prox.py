@@ -24,9 +24,10 @@ PROX_ERR_CUDA = 4
 PROX_ERR_TIMEOUT = 5
 PROX_ERR_DEVICE_CHECK = 6
 PROX_TRACE_EVENTS = 2
-PROX_PHASE_STAMPS = 10
+PROX_PHASE_STAMPS = 16
 PHASES = ("start", "input_select", "proxy", "barrier1", "scores", "mask_known", "first_row",
-          "pass_a_done", "pass_b_done", "end")
+          "pass_a_done", "pass_b_done", "end", "input_hist", "proxy_first_row", "proxy_loop_done",
+          "scores_formed", "sel_staged", "sel_kth_found")
 
 _lock = threading.Lock()
 _lib = None

@@ -200,7 +200,7 @@ PROX_API prox_status prox_ffn_traced(const prox_layer* layer, const void* x, flo
                             prox_stream_t stream);
 
 /* Number of phase timestamps per CTA written by prox_ffn_phase_times. */
-#define PROX_PHASE_STAMPS 10
+#define PROX_PHASE_STAMPS 16
 
 /* Number of CTAs (one per SM) the layer's kernels launch.  Host only. */
 PROX_API int prox_layer_blocks(const prox_layer* layer);
@@ -215,7 +215,11 @@ PROX_API int prox_layer_blocks(const prox_layer* layer);
  *   3 past the grid barrier; 4 scores, histogram and local ranks done
  *   (Stage 2 starts on the speculative channels); 5 exact channel mask
  *   known (this CTA's item list final); 6 first gate|up row landed;
- *   7 gate|up dot products done; 8 W_down^T accumulation done; 9 end.
+ *   7 gate|up dot products done; 8 W_down^T accumulation done; 9 end;
+ *   10 input-magnitude histogram built; 11 first proxy row landed (thread
+ *   0); 12 proxy loop done (thread 0); 13 scores formed (before the local
+ *   ranking); 14 (CTA 0) every chunk in and the score histogram staged;
+ *   15 (CTA 0) exact k-th score found.
  * The dense step stamps 0 and 6..9 only.  Same results as prox_ffn /
  * prox_dense_ffn.
  */
