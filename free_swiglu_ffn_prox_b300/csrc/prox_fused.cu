@@ -8,35 +8,27 @@
 //   P1  proxy GEMV (Stage 1): CTA (tile, slice) streams the int4 proxy rows
 //       of its slice of the kept inputs, restricted to its channel tile, with
 //       128-bit loads, and writes per-slice partial (g~, u~) sums.
-//   --- grid barrier
+//   --- grid barrier 1
 //   P2  CTA b owns the channel chunk [cb0, cb1) (chunk starts on multiples of
 //       4 channels, ~F/n wide): sums the slices in a fixed order
 //       (deterministic scores), forms |silu(g~) u~|, adds the chunk to a
-//       global histogram of the scores' top 11 bits, ranks the chunk, publishes
-//       it sorted (score keys and chunk-local channel bytes) and raises its
-//       epoch-tagged ready flag.
-//   P3  Stage 2 (Eq. (1) of the PrunePath page restricted to the mask) and
-//       the exact channel top-k run side by side:
-//       - the items of CTA b > 0 start with the top m channels of its own
-//         chunk, m = the chunk's expected share k nch / F of the mask; most
-//         are in the mask, so their rows stream at once;
-//       - CTA 0 alone waits for every chunk's flag, stages the histogram and
-//         the sorted chunks in shared memory and finds the exact k-th score
-//         (three radix digits over the candidates, ties to the lower
-//         channel); per chunk it publishes how many channels are selected (a
-//         prefix of the chunk's sorted list) and writes the list of selected
-//         channels that no owner speculated on; one flag word carries the
-//         list length and the call epoch;
-//       - every CTA's selector warp then confirms its speculative items by
-//         rank and reads an even share of that list;
-//       - gate|up rows and W_down^T rows arrive by bulk copies (TMA) into two
-//         shared-memory rings (bytes in flight capped); pass-A warps form
-//         h = silu(W_gate x) (W_up x) per item (one warp per row), pass-B
-//         warps own slices of d_model and accumulate h * W_down^T,
-//         speculative items included before the mask is known (a dropped one
-//         is subtracted again at the end); one vector atomic per element adds
-//         the CTA's part of y at the end.
-//       A speculative item that the exact mask drops costs bandwidth only.
+//       global histogram of the scores' top 11 bits, ranks the chunk and
+//       publishes it sorted (score keys and chunk-local channel bytes).
+//   --- grid barrier 2
+//   P3a every CTA finds the exact k-th score itself (HBM is idle, so staging
+//       the histogram and every sorted chunk from L2 is fast): the digit-1
+//       bin from the histogram, that bin's candidates by a binary search per
+//       chunk, two more radix digits over the candidates, ties to the lower
+//       channel; the selected channels of each chunk are a prefix of its
+//       sorted list, and CTA b takes the positions [k b / n, k (b+1) / n) of
+//       the selected channels in chunk order as its Stage-2 items (an even
+//       split: every CTA moves the same bytes).
+//   P3b Stage 2 (Eq. (1) of the PrunePath page restricted to the mask):
+//       gate|up rows and W_down^T rows arrive by bulk copies (TMA) into two
+//       shared-memory rings (bytes in flight capped); pass-A warps form
+//       h = silu(W_gate x) (W_up x) per item (one warp per row), pass-B
+//       warps own slices of d_model and accumulate h * W_down^T; one vector
+//       atomic per element adds the CTA's part of y at the end.
 //   Stage-2 rows are bf16, or int8 with one fp32 scale per row (the kernels'
 //   Q8 instances): the codes are decoded exactly to fp32 and the scales are
 //   applied to g, u and h.
@@ -64,7 +56,7 @@ constexpr size_t kDRingBytes = 48 * 1024;     // W_down^T bytes in flight per SM
 constexpr int kMaxItems = 512;            // Stage-2 items per CTA
 constexpr int kMaxChunk = 256;            // channels per CTA chunk
 constexpr int kMaxBlocks = kMaxGrid;
-constexpr int kBarriers = 1;              // grid-barrier arrivals per CTA per call
+constexpr int kBarriers = 2;              // grid-barrier arrivals per CTA per call
 constexpr int kRing = 16;                 // proxy rows in flight per thread (cp.async ring)
 static_assert(kRing >= 8, "the running-total table reuses the ring (16 x 8 bytes per thread)");
 static_assert((kRing & (kRing - 1)) == 0, "ring depth must be a power of two");
@@ -90,17 +82,15 @@ struct Ctl {
     uint64_t sel_bar;                // completes when the item list is final
     uint64_t done_bar;               // every warp is through its Stage-2 role
     uint64_t ld_bar;                 // bulk load of the proxy scales (P1)
-    uint64_t sel_ld;                 // bulk load of the digit-1 histogram (CTA 0)
-    uint64_t key_ld;                 // bulk load of the sorted chunk keys (CTA 0)
-    uint64_t idx_ld;                 // bulk load of the chunk-local indices (CTA 0)
+    uint64_t sel_ld;                 // bulk load of the digit-1 histogram
+    uint64_t key_ld;                 // bulk load of every channel's score key
     int gu_last[kMaxStages], d_last[kMaxStages];
     float h[kMaxItems];              // h of each item
     int item[kMaxItems];             // channel of each item
     uint8_t conf[kMaxItems];         // item is in the mask (pass B adds it)
     uint8_t hready[kMaxItems];       // h[i] written by pass A
     float lsc[kMaxChunk];            // scores of this CTA's chunk
-    uint16_t lrank[kMaxChunk];       // rank of each chunk channel (score desc, channel asc)
-    uint32_t warp_tot[kNT / 32 + 1];
+    __align__(16) uint32_t warp_tot[(kNT / 32 + 4) / 4 * 4];  // per-warp totals, read as uint4
     uint32_t sel[4];
     unsigned epoch;
     int abort;
@@ -140,12 +130,7 @@ struct FusedParams {
     unsigned* epoch;     // number of completed calls on this workspace
     uint32_t* hist;      // [kHistWords]: digit-1, digit-2, digit-3 histograms
     float2* part;        // [slices][Fp]
-    uint32_t* skey;      // [Fp] per chunk at its first channel: its score bits, descending
-    uint8_t* sidx;       // [Fp] ... their chunk-local channel indices in that order (ties: lower first)
-    int* selc;           // [kMaxBlocks] per chunk: how many of its channels are selected
-    int* selpre;         // [kMaxBlocks] debug: prefix of selc
-    int* ulist;          // [Fp] the handed-out channels (selected, not speculated), chunk order
-    unsigned* ready;     // [kMaxBlocks] per chunk: epoch + 1 once its sorted list is out
+    uint32_t* skey;      // [Fp] every channel's score key (the fp32 score's bits), channel order
     int* idx_list;       // [Fp] debug: the selected channels, ascending
     float* hch;          // [Fp] debug: h per channel
     // debug outputs (may be null)
@@ -176,13 +161,6 @@ __host__ __device__ __forceinline__ int chunk_lo(int F, int b, int nb, int al) {
 }
 
 __host__ __device__ __forceinline__ int chunk_align(int bw) { return bw > 0 ? bw : 4; }
-
-// Speculative items of a chunk of nch channels: its expected share
-// k nch / F of the mask.
-__host__ __device__ __forceinline__ int spec_count(int k, int nch, int F) {
-    const unsigned m = (unsigned)k * (unsigned)nch / (unsigned)F;  // < 2^23
-    return (int)(m < (unsigned)nch ? m : (unsigned)nch);
-}
 
 // ----------------------------------------------------------------- helpers
 // ----------------------------------------------------------------- helpers
@@ -231,61 +209,6 @@ __device__ bool grid_barrier(unsigned* bar, unsigned target, int* status, long l
     return ctl.abort == 0;
 }
 
-// Given a histogram h[nbins] of digits (nbins a multiple of 128, at most
-// 2048) and krem >= 1 with sum(h) >= krem, warp 0 finds the digit b with
-// sum(h[b+1..]) < krem <= sum(h[b..]) and stores (b, krem - sum(h[b+1..]))
-// in sel[0..1].  Level 1: lane l sums the nbins/32 bins just below
-// nbins - l nbins/32 (independent vector loads) and a warp scan finds the
-// lane holding the k-th; level 2 spreads that lane's bins over the warp
-// (at most two per lane) and scans again.  No data-dependent loop.  Called
-// by warp 0 only; the caller synchronises.
-template <int NBINS>
-__device__ __forceinline__ void select_bin_warp(const uint32_t* h, uint32_t krem, uint32_t* sel) {
-    constexpr int PER = NBINS / 32, NQ = PER / 4, PER2 = PER > 32 ? 2 : 1;
-    static_assert(NBINS % 128 == 0 && NBINS <= 2048, "bins");
-    const int lane = threadIdx.x & 31;
-    const int lo = NBINS - (lane + 1) * PER;
-    const uint4* hv = reinterpret_cast<const uint4*>(h + lo);
-    uint4 w[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) w[q] = hv[q];  // all loads in flight at once
-    uint32_t sum = 0;
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) sum += (w[q].x + w[q].y) + (w[q].z + w[q].w);
-    uint32_t incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, incl - sum < krem && incl >= krem);
-    const int L = hit ? __ffs(hit) - 1 : 0;  // hit != 0 whenever sum(h) >= krem
-    const uint32_t above_l = __shfl_sync(0xffffffffu, incl - sum, L);
-    const int top = NBINS - L * PER - 1;  // lane L's highest bin
-    // level 2: lane l takes bins top - PER2 l and (PER2 = 2) top - 2 l - 1
-    const int b0 = top - lane * PER2;
-    uint32_t v0 = 0, v1 = 0;
-    if (lane * PER2 < PER) v0 = h[b0];
-    if (PER2 == 2 && lane * 2 + 1 < PER) v1 = h[b0 - 1];
-    const uint32_t s2 = v0 + v1;
-    uint32_t incl2 = s2;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl2, o);
-        if (lane >= o) incl2 += t;
-    }
-    const uint32_t above2 = above_l + incl2 - s2;
-    if (above2 < krem && above2 + s2 >= krem) {
-        if (above2 + v0 >= krem) {
-            sel[0] = (uint32_t)b0;
-            sel[1] = krem - above2;
-        } else {
-            sel[0] = (uint32_t)(b0 - 1);
-            sel[1] = krem - above2 - v0;
-        }
-    }
-}
-
 // Exclusive scan of one value per thread over the block (warp shuffles, one
 // barrier); also returns the block total.  Uses ctl.warp_tot.
 // Barrier over the first NT threads: __syncthreads for the whole block,
@@ -307,90 +230,26 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Ctl& ctl, uint32
     }
     if (lane == 31) ctl.warp_tot[wid] = s;
     group_sync<NT>();
+    // all warp totals at once (independent 16-byte loads), then sums in registers
+    constexpr int NV = (NT / 32 + 3) / 4;
+    uint4 wt[NV];
+#pragma unroll
+    for (int q = 0; q < NV; ++q) wt[q] = reinterpret_cast<const uint4*>(ctl.warp_tot)[q];
     uint32_t wp = 0, tt = 0;
 #pragma unroll
-    for (int w = 0; w < NT / 32; ++w) {
-        const uint32_t x = ctl.warp_tot[w];
-        wp += w < wid ? x : 0u;
-        tt += x;
+    for (int q = 0; q < NV; ++q) {
+        const uint32_t x4[4] = {wt[q].x, wt[q].y, wt[q].z, wt[q].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int w = 4 * q + e;
+            if (w < NT / 32) {
+                wp += w < wid ? x4[e] : 0u;
+                tt += x4[e];
+            }
+        }
     }
     total = tt;
     return wp + s - v;
-}
-
-// Exact top-k over n keys in shared memory (thread t owns the contiguous
-// keys [t kpt, (t+1) kpt), kpt <= 64), ties to the lower index, in three
-// radix digits: d1 = key >> s1 from a histogram h1 already built, then the
-// next digits over the thread's own candidates only (the keys in the
-// selected d1 bin, tracked in a bit mask), so only the first pass touches
-// every key.  Produces T (the k-th key) and r (ties at T to keep) in
-// ctl.sel[0..1], and for this thread: the number of selected keys before
-// its range (in ascending index order) and a candidate mask.
-struct TopkPlan {
-    int s1, n1;        // digit-1 shift and histogram size (h1)
-    int s2, n2;        // digit-2 shift and bins (h2), digit 3 = key & (n3 - 1)
-    int n3;
-};
-
-template <int NT, typename KeyFn>
-__device__ __forceinline__ void topk_digits(const TopkPlan& pl, int n, int kpt, uint32_t k,
-                                            KeyFn key, uint32_t* h1, uint32_t* h2, uint32_t* h3,
-                                            Ctl& ctl, uint32_t& T, uint32_t& r, uint32_t& pos0,
-                                            uint32_t& ties_before, uint32_t& nsel) {
-    const int wid = threadIdx.x >> 5;
-    const int i0 = threadIdx.x * kpt;
-    // digit 1 from h1
-    if (wid == 0) {
-        if (pl.n1 == 2048) select_bin_warp<2048>(h1, k, ctl.sel);
-        else select_bin_warp<256>(h1, k, ctl.sel);
-    }
-    group_sync<NT>();
-    const uint32_t b1 = ctl.sel[0], k1 = ctl.sel[1];
-    uint32_t gt1 = 0;
-    uint64_t cmask = 0;
-    for (int e = 0; e < kpt; ++e) {
-        const int i = i0 + e;
-        if (i < n) {
-            const uint32_t d1 = key(i) >> pl.s1;
-            gt1 += d1 > b1;
-            cmask |= (uint64_t)(d1 == b1) << e;
-        }
-    }
-    for (uint64_t m = cmask; m; m &= m - 1)
-        atomicAdd(&h2[(key(i0 + __ffsll((long long)m) - 1) >> pl.s2) & (pl.n2 - 1)], 1u);
-    group_sync<NT>();
-    if (wid == 0) {
-        if (pl.n2 == 2048) select_bin_warp<2048>(h2, k1, ctl.sel);
-        else select_bin_warp<128>(h2, k1, ctl.sel);
-    }
-    group_sync<NT>();
-    const uint32_t b12 = (b1 << (pl.s1 - pl.s2)) | ctl.sel[0], k2 = ctl.sel[1];
-    if (pl.n3 > 1) {
-        for (uint64_t m = cmask; m; m &= m - 1) {
-            const uint32_t kk = key(i0 + __ffsll((long long)m) - 1);
-            if ((kk >> pl.s2) == b12) atomicAdd(&h3[kk & (pl.n3 - 1)], 1u);
-        }
-        group_sync<NT>();
-        if (wid == 0) select_bin_warp<512>(h3, k2, ctl.sel);
-        group_sync<NT>();
-        T = (b12 << pl.s2) | ctl.sel[0];
-        r = ctl.sel[1];
-    } else {
-        T = b12;
-        r = k2;
-    }
-    // per-thread counts from the sure keys and the thread's own candidates
-    uint32_t gt = gt1, eq = 0;
-    for (uint64_t m = cmask; m; m &= m - 1) {
-        const uint32_t kk = key(i0 + __ffsll((long long)m) - 1);
-        gt += kk > T;
-        eq += kk == T;
-    }
-    uint32_t tot;
-    const uint32_t ex = block_excl_scan<NT>(gt | (eq << 16), ctl, tot);
-    ties_before = ex >> 16;
-    pos0 = (ex & 0xffffu) + min(ties_before, r);  // selected keys before this range
-    nsel = gt + (ties_before < r ? min(eq, r - ties_before) : 0u);
 }
 
 // fp16 bits of x * 2^shift for a bf16 x (exact whenever the result is a
@@ -407,21 +266,9 @@ __device__ __forceinline__ uint16_t scaled_fp16(uint16_t xb, int shift) {
 }
 
 // --------------------------------------------------------------- proxy math
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
-    __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-    return *reinterpret_cast<uint32_t*>(&r);
-}
-
-__device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t c) {
-    __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
-                        *reinterpret_cast<__half2*>(&c));
-    return *reinterpret_cast<uint32_t*>(&r);
+// acc += a * x  (fp16 x fp16 -> fp32, one rounding)
+__device__ __forceinline__ void fma_f32_f16(float& acc, uint16_t a, uint16_t x) {
+    asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(x));
 }
 
 // acc0 += q.lo * x, acc1 += q.hi * x  (fp16 x fp16 -> fp32, one rounding each)
@@ -435,22 +282,20 @@ __device__ __forceinline__ void fma_f32_f16x2(float& acc0, float& acc1, uint32_t
 }
 
 // One 32-bit word of proxy codes = 4 channels (byte = gate | up << 4, each
-// nibble offset-binary q + 8).  The nibbles become exact fp16 integers with
-// one LOP3 and one packed HSUB2/HFMA2 per two channels.
+// nibble offset-binary n = q + 8).  A single AND per two channels leaves each
+// nibble in the mantissa of an fp16 half with a zero exponent field: the
+// exact subnormal n 2^-24 (gate nibbles, bits 0-3 and 16-19) or 16 n 2^-24 =
+// n 2^-20 (up nibbles, bits 4-7 and 20-23); the word shifted by 8 gives the
+// other two channels.  The fp16 x fp16 -> fp32 products are exact, the group
+// sums are sum n x scaled by 2^-24 / 2^-20, and the flush removes the offset
+// with sum q x = sum n x - 8 sum x (one FMA per channel, exact whenever the
+// sums fit in fp32).
 __device__ __forceinline__ void proxy_mac_word(uint32_t w, uint16_t xh, float* ag, float* au) {
-    constexpr uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kMagic = 0x64006400u;
-    constexpr uint32_t kBias = 0x64086408u;      // (1032, 1032)
-    constexpr uint32_t kSixteenth = 0x2C002C00u; // (1/16, 1/16)
-    constexpr uint32_t kHiBias = 0xD480D480u;    // (-72, -72)
     const uint32_t w8 = w >> 8;
-    const uint32_t g02 = hsub2_bits(lop3_and_or(w, kLo, kMagic), kBias);
-    const uint32_t g13 = hsub2_bits(lop3_and_or(w8, kLo, kMagic), kBias);
-    const uint32_t u02 = hfma2_bits(lop3_and_or(w, kHi, kMagic), kSixteenth, kHiBias);
-    const uint32_t u13 = hfma2_bits(lop3_and_or(w8, kHi, kMagic), kSixteenth, kHiBias);
-    fma_f32_f16x2(ag[0], ag[2], g02, xh);
-    fma_f32_f16x2(ag[1], ag[3], g13, xh);
-    fma_f32_f16x2(au[0], au[2], u02, xh);
-    fma_f32_f16x2(au[1], au[3], u13, xh);
+    fma_f32_f16x2(ag[0], ag[2], w & 0x000F000Fu, xh);
+    fma_f32_f16x2(ag[1], ag[3], w8 & 0x000F000Fu, xh);
+    fma_f32_f16x2(au[0], au[2], w & 0x00F000F0u, xh);
+    fma_f32_f16x2(au[1], au[3], w8 & 0x00F000F0u, xh);
 }
 
 // 16-byte global -> shared copy that bypasses L1 (cp.async), L2 policy hint.
@@ -807,16 +652,12 @@ __device__ __forceinline__ void stage2_join(const Stage2Args& a, Ctl& ctl) {
             mbar_wait_bounded(&ctl.d_full[s], (ctl.d_last[s] / a.n_d) & 1, a.limit_ns, nullptr);
 }
 
+// ------------------------------------------------------------ the selection
+constexpr int kPrefetchItems = 8;  // sure items per CTA prefetched into L2 during the selection
+
 // Bulk prefetch of global memory into L2 (no shared-memory destination).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// ------------------------------------------------------------ the selection
-constexpr int kCandCap = 2048;  // digit-1 candidates kept in shared memory
-
-__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Block-wide digit select, called by every thread: threads t < NB/4 read
@@ -844,152 +685,80 @@ __device__ __forceinline__ void block_select(const uint32_t* h, uint32_t krem, C
     __syncthreads();
     if (tid < NQ) {
         uint32_t above = suf - s;
-        for (int w = wid + 1; w < NW; ++w) above += ctl.warp_tot[w];
+        if constexpr (NW > 1) {  // the higher warps' totals: independent 16-byte loads
+            constexpr int NV = (NW + 3) / 4;
+            uint4 wt[NV];
+#pragma unroll
+            for (int q = 0; q < NV; ++q) wt[q] = reinterpret_cast<const uint4*>(ctl.warp_tot)[q];
+#pragma unroll
+            for (int q = 0; q < NV; ++q) {
+                const uint32_t x4[4] = {wt[q].x, wt[q].y, wt[q].z, wt[q].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * q + e < NW && 4 * q + e > wid) above += x4[e];
+            }
+        }
         if (above < krem && above + s >= krem) {
-            const uint32_t bj[4] = {v.x, v.y, v.z, v.w};
-            uint32_t a = above;
-            int j = 3;
-            while (j > 0 && a + bj[j] < krem) a += bj[j--];
-            ctl.sel[0] = (uint32_t)(4 * tid + j);
+            // the bin within this thread's four, top bin first (no indexed array)
+            uint32_t j = 3, a = above;
+            if (a + v.w < krem) {
+                a += v.w;
+                j = 2;
+                if (a + v.z < krem) {
+                    a += v.z;
+                    j = 1;
+                    if (a + v.y < krem) {
+                        a += v.y;
+                        j = 0;
+                    }
+                }
+            }
+            ctl.sel[0] = 4u * (uint32_t)tid + j;
             ctl.sel[1] = krem - a;
         }
     }
     __syncthreads();
 }
 
-// Number of leading entries of the descending keys s[0..n) with pred true
-// (pred holds for a prefix).
-template <typename Pred>
-__device__ __forceinline__ int count_leading(const uint32_t* s, int n, Pred pred) {
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (pred(s[mid])) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
-}
-
-// Warp-wide exclusive prefix over per-chunk values v(t), t < nb (<= 256):
-// out[t] for t < nb, the total in out[nb].  Called by one whole warp.
-template <typename V>
-__device__ __forceinline__ void warp_chunk_scan(int nb, V v, int* out) {
-    const int lane = threadIdx.x & 31;
-    const int per = (nb + 31) >> 5, t0 = lane * per;  // per <= kMaxBlocks / 32
-    int val[kMaxBlocks / 32];
-    int run = 0;
-#pragma unroll
-    for (int j = 0; j < kMaxBlocks / 32; ++j) {
-        val[j] = (j < per && t0 + j < nb) ? v(t0 + j) : 0;
-        run += val[j];
-    }
-    int incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    int base = incl - run;
-#pragma unroll
-    for (int j = 0; j < kMaxBlocks / 32; ++j)
-        if (j < per && t0 + j < nb) {
-            out[t0 + j] = base;
-            base += val[j];
-        }
-    if (lane == 31) out[nb] = incl;
-    __syncwarp();
-}
-
-// Largest c in [0, n) with pre[c] <= q (pre non-decreasing, pre[0] = 0 <= q).
-__device__ __forceinline__ int chunk_of(const int* pre, int n, int q) {
-    int lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pre[mid] <= q) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
-// Speculative items of chunk c (the owner's rule).
-__device__ __forceinline__ int chunk_spec(const FusedParams& p, int c, int nb) {
-    const int al = chunk_align(p.bw);
-    return c == 0 ? 0 : spec_count(p.k, chunk_lo(p.F, c + 1, nb, al) - chunk_lo(p.F, c, nb, al), p.F);
-}
-
-// CTA 0, all threads: the exact channel top-k once every chunk is in (grid
-// barrier 2).  Every chunk has published its keys sorted descending (ties:
-// lower channel first), so the selected channels of a chunk are a prefix of
-// its sorted list, and so are its speculative items.  CTA 0 stages the
-// digit-1 histogram and all sorted keys in shared memory; the digit-1 bin
-// (bits 30..20 of the score bits) of the k-th key comes from the histogram;
-// a binary search per chunk finds that bin's candidates, which are gathered
-// and reduced to the exact k-th key T by two more digits (bits 19..9 and
-// 8..0); ties at T are kept in channel order.  Per chunk it publishes
-// selc = how many of its channels are selected and the prefix over chunks of
-// max(0, selc - its speculative count), then the result flag (epoch + 1).
-// Returns false on a timeout or a broken invariant.
-__device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, int nb,
-                               unsigned ep) {
+// Every CTA, all threads, once every channel's score key is published
+// (grid barrier 2): the exact channel top-k and this CTA's share of it.
+// The CTA stages the digit-1 histogram and all F score keys (channel order)
+// in shared memory; HBM is idle at this point, so the copies are L2 hits at
+// low latency.  Thread t owns the contiguous keys [t kpt, (t+1) kpt):
+//   digit 1 (bits 30..20 of the score bits) of the k-th key from the
+//   histogram every chunk added to; digit 2 (bits 19..9) and digit 3
+//   (bits 8..0) from shared histograms over the keys that match so far;
+//   then T (the k-th key) and r (keys equal to T to keep, lowest channels
+//   first).  One block scan of (keys above T, keys equal to T) per thread
+//   gives each thread the position of its first selected channel in the
+//   ascending list of selected channels; CTA b takes the positions
+//   [k b / n, k (b+1) / n) of that list as its Stage-2 items (an even split:
+//   every CTA moves the same bytes; every CTA computes the same T and
+//   prefixes, so the shares partition the mask).
+// As soon as digit 1 is known (and the staging copies are in), the lowest
+// channels of the CTA's own chunk above the digit-1 bin are certain: the
+// rows of the first kPrefetchItems of them are prefetched into L2, so HBM
+// streams while the selection finishes (whichever CTA's share holds them
+// finds them in L2).  Returns false on a timeout or a broken invariant
+// (ctl.abort set).
+__device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int nb, int b,
+                             int cb0, int nch) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int F = p.F, Fp = p.Fp;
     uint32_t* h1 = reinterpret_cast<uint32_t*>(area + (size_t)2 * p.d);
     uint32_t* h2 = h1 + kHistBins;
     uint32_t* h3 = h2 + kHistBins;
-    uint32_t* sk = h3 + 512;                               // [Fp] sorted keys per chunk
-    uint8_t* sidx = reinterpret_cast<uint8_t*>(sk + Fp);   // [Fp] their chunk-local channels
-    int* clo = reinterpret_cast<int*>(sidx + Fp);          // [kMaxBlocks] first candidate
-    int* ccn = clo + kMaxBlocks;                           // candidates
-    int* coff = ccn + kMaxBlocks;                          // [kMaxBlocks + 1]
-    int* cgt = coff + kMaxBlocks + 1;                      // keys above T
-    int* ceq = cgt + kMaxBlocks;                           // keys equal to T
-    int* epre = ceq + kMaxBlocks;                          // [kMaxBlocks + 1]
-    int* csel = epre + kMaxBlocks + 1;                     // selected
-    int* cbeg = csel + kMaxBlocks;                         // [kMaxBlocks + 1] chunk starts
-    int* cspc = cbeg + kMaxBlocks + 1;                     // speculative items per chunk
-    int* upre = cspc + kMaxBlocks;                         // [kMaxBlocks + 1]
-    uint32_t* cand = reinterpret_cast<uint32_t*>(upre + kMaxBlocks + 1);  // [kCandCap]
-    for (int i = tid; i < kHistBins + 512; i += kNT) h2[i] = 0u;
-    for (int t = tid; t <= nb; t += kNT) {
-        cbeg[t] = chunk_lo(F, t, nb, chunk_align(p.bw));
-        if (t < nb) cspc[t] = chunk_spec(p, t, nb);
-    }
-    // thread t < nb waits for chunk t's ready flag; then the histogram, all
-    // sorted keys and the chunk-local indices arrive by three bulk copies
-    // (the histogram on its own barrier, so digit 1 runs while the rest lands)
-    if (tid < nb) {
-        bool ok = true;
-        uint64_t t0 = 0;
-        for (uint32_t it = 1;; ++it) {
-            if (ld_acquire_gpu(p.ready + tid) == ep + 1u) break;
-            if ((it & 15u) == 0) {
-                const uint64_t now = global_timer_ns();
-                if (t0 == 0) t0 = now;
-                else if ((long long)(now - t0) > p.limit_ns) {
-                    ok = false;
-                    break;
-                }
-            }
-        }
-        if (!ok) {
-            record_status(p.status, PROX_ERR_TIMEOUT);
-            ctl.abort = 1;
-        }
-    }
-    __syncthreads();
-    if (ctl.abort) return false;
+    uint32_t* sk = h3 + 512;  // [Fp] score keys, channel order
     if (tid == 0) {
-        *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;  // every CTA has read it
         asm volatile("fence.proxy.async.global;" ::: "memory");
         const uint64_t pol = policy_evict_first();
         mbar_arrive_expect_tx(&ctl.sel_ld, (uint32_t)(kHistBins * 4));
         bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.sel_ld, pol);
         mbar_arrive_expect_tx(&ctl.key_ld, (uint32_t)(Fp * 4));
         bulk_g2s(sk, p.skey, (uint32_t)(Fp * 4), &ctl.key_ld, pol);
-        mbar_arrive_expect_tx(&ctl.idx_ld, (uint32_t)Fp);
-        bulk_g2s(sidx, p.sidx, (uint32_t)Fp, &ctl.idx_ld, pol);
     }
-    // waits for one of the three staging copies; after a timeout lets all land
+    for (int i = tid; i < kHistBins + 512; i += kNT) h2[i] = 0u;
+    // waits for one of the staging copies; after a timeout lets both land
     auto landed = [&](uint64_t* bar) {
         if (!mbar_wait_bounded(bar, 0, p.limit_ns, &ctl.abort) && lane == 0) {
             ctl.abort = 1;
@@ -1000,188 +769,99 @@ __device__ bool central_select(const FusedParams& p, Ctl& ctl, uint8_t* area, in
         if (tid == 0) {
             mbar_wait_bounded(&ctl.sel_ld, 0, p.limit_ns, nullptr);
             mbar_wait_bounded(&ctl.key_ld, 0, p.limit_ns, nullptr);
-            mbar_wait_bounded(&ctl.idx_ld, 0, p.limit_ns, nullptr);
         }
         return false;
     };
-    if (!landed(&ctl.sel_ld)) return false;
-    if (tid == 0) stamp_here(p.ts, 14);
     auto broken = [&]() {
         if (tid == 0) {
             record_status(p.status, PROX_ERR_DEVICE_CHECK);
             ctl.abort = 1;
+            mbar_wait_bounded(&ctl.key_ld, 0, p.limit_ns, nullptr);  // before the area is reused
         }
+        __syncthreads();
         return false;
     };
-    // digit 1 from the histogram of every chunk (the sorted keys still landing)
+    if (!landed(&ctl.sel_ld)) return false;
+    stamp(p.ts, 14);
+    // digit 1 from the histogram of every chunk (the keys still landing)
     block_select<2048>(h1, (uint32_t)p.k, ctl);
     if (ctl.sel[0] == 0xffffffffu) return broken();
     const uint32_t b1 = ctl.sel[0], k1 = ctl.sel[1];
-    if (!landed(&ctl.key_ld)) return false;
-    // per chunk: its digit-1 candidates are the sorted positions [lo, hi)
-    if (tid < nb) {
-        const int c0 = cbeg[tid], n = cbeg[tid + 1] - c0;
-        const int lo = count_leading(sk + c0, n, [&](uint32_t kk) { return (kk >> 20) > b1; });
-        const int hi = count_leading(sk + c0, n, [&](uint32_t kk) { return (kk >> 20) >= b1; });
-        clo[tid] = lo;
-        ccn[tid] = hi - lo;
-    }
-    __syncthreads();
-    if (wid == 0) warp_chunk_scan(nb, [&](int t) { return ccn[t]; }, coff);
-    __syncthreads();
-    const int n_c = coff[nb];
-    const bool compact = n_c <= kCandCap;
-    if (compact && tid < nb) {
-        const uint32_t* src = sk + cbeg[tid] + clo[tid];
-        for (int i = 0; i < ccn[tid]; ++i) cand[coff[tid] + i] = src[i];
-    }
-    __syncthreads();
-    // the candidates (or, if there are too many, every key filtered on digit 1)
-    auto each_cand = [&](auto&& fn) {
-        if (compact) {
-            for (int i = tid; i < n_c; i += kNT) fn(cand[i]);
-        } else {
-            for (int i = tid; i < F; i += kNT) {
-                const uint32_t kk = sk[i];
-                if ((kk >> 20) == b1) fn(kk);
-            }
+    // own channels above the digit-1 bin are certain: rank them in channel order
+    const bool sure = tid < nch && (__float_as_uint(ctl.lsc[tid]) >> 20) > b1;
+    const unsigned sb = __ballot_sync(0xffffffffu, sure);
+    if (lane == 0) ctl.warp_tot[wid] = __popc(sb);
+    if (!landed(&ctl.key_ld)) return false;  // (its barrier also publishes warp_tot)
+    if (sure) {
+        // every staging copy has landed, so the rest of the selection reads
+        // shared memory only: start HBM on the first certain rows now
+        int rank = __popc(sb & ((1u << lane) - 1u));
+        for (int w = 0; w < wid; ++w) rank += (int)ctl.warp_tot[w];  // nch <= 256: <= 7 warps
+        if (rank < kPrefetchItems) {
+            const int c = cb0 + tid;
+            const size_t gb = gu_row_bytes(p.d, p.q8), db = down_row_bytes(p.d, p.q8);
+            prefetch_l2(p.gateup + (size_t)c * gb, (uint32_t)gb);
+            prefetch_l2(p.down_t + (size_t)c * db, (uint32_t)db);
         }
-    };
-    each_cand([&](uint32_t kk) { atomicAdd(&h2[(kk >> 9) & 2047u], 1u); });
+    }
+    // this thread's keys: [i0, i1)
+    const int kpt = (F + kNT - 1) / kNT;
+    const int i0 = min(F, tid * kpt), i1 = min(F, i0 + kpt);
+    // digit 2 over the keys in the digit-1 bin
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t kk = sk[i];
+        if ((kk >> 20) == b1) atomicAdd(&h2[(kk >> 9) & 2047u], 1u);
+    }
     __syncthreads();
     block_select<2048>(h2, k1, ctl);
     if (ctl.sel[0] == 0xffffffffu) return broken();
     const uint32_t pre = (b1 << 11) | ctl.sel[0], k2 = ctl.sel[1];
-    each_cand([&](uint32_t kk) {
+    // digit 3 over the keys matching both digits
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t kk = sk[i];
         if ((kk >> 9) == pre) atomicAdd(&h3[kk & 511u], 1u);
-    });
+    }
     __syncthreads();
     block_select<512>(h3, k2, ctl);
     if (ctl.sel[0] == 0xffffffffu) return broken();
     const uint32_t T = (pre << 9) | ctl.sel[0];
-    const int r = (int)ctl.sel[1];  // keys equal to T to keep, lowest channels first
-    if (tid == 0) stamp_here(p.ts, 15);
-    // per chunk: keys above and equal to T (T lies in the digit-1 bin, so
-    // every key before the chunk's candidates is above it)
-    if (tid < nb) {
-        int gt = clo[tid], eq = 0;
-        if (compact) {
-            const uint32_t* cs = cand + coff[tid];
-            for (int i = 0; i < ccn[tid]; ++i) {
-                gt += cs[i] > T;
-                eq += cs[i] == T;
+    const uint32_t r = ctl.sel[1];  // keys equal to T to keep, lowest channels first
+    stamp(p.ts, 15);
+    // this thread's keys above and equal to T; one scan gives the selected
+    // channels and the ties before it (gt <= F <= 32768 < 2^16: no carry)
+    uint32_t gt = 0, eq = 0;
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t kk = sk[i];
+        gt += kk > T;
+        eq += kk == T;
+    }
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan<kNT>(gt | (eq << 16), ctl, tot);
+    uint32_t ties = ex >> 16;
+    uint32_t pos = (ex & 0xffffu) + min(ties, r);  // selected channels before this thread's
+    if ((tot & 0xffffu) + min(tot >> 16, r) != (uint32_t)p.k) return broken();
+    const int q0 = chunk_begin(p.k, b, nb), q1 = chunk_begin(p.k, b + 1, nb);
+    if (q1 - q0 > kMaxItems) return broken();
+    if ((int)pos < q1 && (int)(pos + gt + eq) >= q0) {  // this thread may hold some of the share
+        for (int i = i0; i < i1 && (int)pos < q1; ++i) {
+            const uint32_t kk = sk[i];
+            bool sel = kk > T;
+            if (kk == T) sel = ties++ < r;
+            if (sel) {
+                if ((int)pos >= q0) {
+                    ctl.item[pos - q0] = i;
+                    ctl.conf[pos - q0] = 1;
+                }
+                ++pos;
             }
-        } else {
-            const int c0 = cbeg[tid], n = cbeg[tid + 1] - c0;
-            gt = count_leading(sk + c0, n, [&](uint32_t kk) { return kk > T; });
-            eq = count_leading(sk + c0, n, [&](uint32_t kk) { return kk >= T; }) - gt;
         }
-        cgt[tid] = gt;
-        ceq[tid] = eq;
     }
+    if (tid == 0) ctl.n_items = q1 - q0;
     __syncthreads();
-    if (wid == 0) {
-        warp_chunk_scan(nb, [&](int t) { return ceq[t]; }, epre);
-        for (int t = lane; t < nb; t += 32) {
-            const int sel = cgt[t] + min(max(r - epre[t], 0), ceq[t]);
-            csel[t] = sel;
-            p.selc[t] = sel;
-        }
-        __syncwarp();
-        warp_chunk_scan(nb, [&](int t) { return max(csel[t] - cspc[t], 0); }, upre);
-        if (p.debug) warp_chunk_scan(nb, [&](int t) { return csel[t]; }, p.selpre);
-    }
-    __syncthreads();
-    // the handed-out list: per chunk, in chunk order, its selected channels of
-    // rank >= its speculative count
-    if (!landed(&ctl.idx_ld)) return false;
-    const int U = upre[nb];
-    for (int q = tid; q < U; q += kNT) {
-        const int c = chunk_of(upre, nb, q);
-        p.ulist[q] = cbeg[c] + sidx[cbeg[c] + cspc[c] + (q - upre[c])];
-    }
-    __syncthreads();  // the per-chunk results and the list are out
-    if (tid == 0) {
-        // the flag carries the list length: (U << 16) | (epoch + 1) mod 2^16
-        st_release_gpu(p.bar + 2, ((unsigned)U << 16) | ((ep + 1u) & 0xffffu));
-        stamp_here(p.ts, 5);
-    }
+    // debug: the whole mask, ascending (every CTA writes its share)
+    if (p.debug)
+        for (int i = tid; i < q1 - q0; i += kNT) p.idx_list[q0 + i] = ctl.item[i];
     return true;
-}
-
-// The selector warp of every CTA: waits for CTA 0's result flag, confirms
-// its speculative items ctl.item[0..m) (those of rank < selc[b]; they are the
-// chunk's top m), appends its share [U b / n, U (b+1) / n) of the handed-out
-// channels (in chunk order, the selected channels of rank >= the chunk's
-// speculative count) and completes ctl.sel_bar.  With the debug outputs it
-// also writes the chunk's selected channels, ascending, into idx_list.
-__device__ void await_selection(const FusedParams& p, Ctl& ctl, int b, int nb, int cb0, int nch,
-                                int m, unsigned ep) {
-    const int lane = threadIdx.x & 31;
-    const unsigned below = (1u << lane) - 1u;
-    bool ok = true;
-    unsigned flag = 0;
-    if (lane == 0) {
-        uint64_t t0 = 0;
-        for (uint32_t it = 1;; ++it) {
-            flag = ld_acquire_gpu(p.bar + 2);
-            if ((flag & 0xffffu) == ((ep + 1u) & 0xffffu)) break;
-            if ((it & 15u) == 0) {
-                if (*reinterpret_cast<volatile int*>(&ctl.abort)) {
-                    ok = false;
-                    break;
-                }
-                const uint64_t now = global_timer_ns();
-                if (t0 == 0) t0 = now;
-                else if ((long long)(now - t0) > p.limit_ns) {
-                    ok = false;
-                    record_status(p.status, PROX_ERR_TIMEOUT);
-                    ctl.abort = 1;
-                    break;
-                }
-            }
-        }
-    }
-    __syncwarp();
-    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-    const int U = (int)(__shfl_sync(0xffffffffu, flag, 0) >> 16);
-    const int q0 = chunk_begin(U, b, nb), q1 = chunk_begin(U, b + 1, nb);
-    if (m + (q1 - q0) > kMaxItems) {
-        if (lane == 0) {
-            record_status(p.status, PROX_ERR_DEVICE_CHECK);
-            ctl.abort = 1;
-        }
-        return;
-    }
-    const int selb = __ldcg(p.selc + b);
-    for (int q = q0 + lane; q < q1; q += 32) {
-        ctl.item[m + q - q0] = __ldcg(p.ulist + q);
-        ctl.conf[m + q - q0] = 1;
-    }
-    for (int j = lane; j < m; j += 32) {
-        ctl.conf[j] = j < selb ? 1 : 0;
-        // a dropped speculative item may already be in y: pass B will read its
-        // W_down^T row again to take it out, so bring the row into L2 now
-        if (j >= selb)
-            prefetch_l2(p.down_t + (size_t)ctl.item[j] * down_row_bytes(p.d, p.q8),
-                        (uint32_t)down_row_bytes(p.d, p.q8));
-    }
-    if (p.debug) {
-        int pos = __ldcg(p.selpre + b);
-        for (int i0 = 0; i0 < nch; i0 += 32) {
-            const int i = i0 + lane;
-            const bool sel = i < nch && (int)ctl.lrank[i] < selb;
-            const unsigned bs = __ballot_sync(0xffffffffu, sel);
-            if (sel) p.idx_list[pos + __popc(bs & below)] = cb0 + i;
-            pos += __popc(bs);
-        }
-    }
-    if (lane == 0) {
-        ctl.n_items = m + (q1 - q0);
-        stamp_here(p.ts, 5);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl.sel_bar);
 }
 
 // ------------------------------------------------------------ fused kernel
@@ -1387,8 +1067,10 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                 bulk_g2s(ssc + (size_t)g * W, p.scales + (size_t)(g_lo + g) * Fp + c0,
                          (uint32_t)(width * 4), &ctl.ld_bar, pol);
         }
-        // this group's sums (ag, au) and the scaled running totals (tg, tu)
+        // this group's sums (ag, au: sum n x in units of 2^-24 / 2^-20), the
+        // group's sum of x (cx) and the scaled running totals (tg, tu)
         float ag[16], au[16], tg[16], tu[16];
+        float cx = 0.0f;
 #pragma unroll
         for (int t = 0; t < 16; ++t) ag[t] = au[t] = tg[t] = tu[t] = 0.0f;
         int cur_g = -1;
@@ -1408,6 +1090,8 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
             } else {
                 src = reinterpret_cast<const uint4*>(p.scales + (size_t)cur_g * Fp + c0 + cu * 16);
             }
+            const float m8c = -8.0f * cx;  // the offset: sum q x = sum n x - 8 sum x
+            cx = 0.0f;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
                 const uint4 s4 = src[v];
@@ -1416,8 +1100,8 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                 for (int e = 0; e < 4; ++e) {
                     const int t = 4 * v + e;
                     const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&sv[e]));
-                    tg[t] = fmaf(s2.x, ag[t], tg[t]);
-                    tu[t] = fmaf(s2.y, au[t], tu[t]);
+                    tg[t] = fmaf(s2.x, fmaf(ag[t], 16777216.0f, m8c), tg[t]);
+                    tu[t] = fmaf(s2.y, fmaf(au[t], 1048576.0f, m8c), tu[t]);
                     ag[t] = 0.0f;
                     au[t] = 0.0f;
                 }
@@ -1458,6 +1142,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                     cur_g = g;
                 }
                 const uint16_t xh = (uint16_t)(kp & 0xffffu);
+                fma_f32_f16(cx, (uint16_t)0x3C00u, xh);
                 proxy_mac_word(w.x, xh, &ag[0], &au[0]);
                 proxy_mac_word(w.y, xh, &ag[4], &au[4]);
                 proxy_mac_word(w.z, xh, &ag[8], &au[8]);
@@ -1507,7 +1192,6 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     const int cb0 = chunk_lo(F, b, nb, chunk_align(p.bw));
     const int cb1 = chunk_lo(F, b + 1, nb, chunk_align(p.bw));
     const int nch = cb1 - cb0;  // <= kMaxChunk (checked by the host)
-    const int m = b == 0 ? 0 : spec_count(p.k, nch, F);  // CTA 0 selects instead
     {
         const bool act = tid < nch;
         uint32_t key = 0;
@@ -1555,7 +1239,9 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                 ctl.lsc[tid] = sblk;
             }
         }
-        // one reduction per distinct bin in the warp
+        // the key, in channel order, for the selection; one histogram
+        // reduction per distinct bin in the warp
+        if (act) p.skey[cb0 + tid] = key;
         const unsigned am = __ballot_sync(0xffffffffu, act);
         if (act) {
             const unsigned peers = __match_any_sync(am, key >> 20);
@@ -1573,43 +1259,26 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         stage2_init(ctl, p.n_gu, p.n_d);
         mbar_init(&ctl.sel_ld, 1);
         mbar_init(&ctl.key_ld, 1);
-        mbar_init(&ctl.idx_ld, 1);
         fence_mbar_init();
     }
-    __syncthreads();
     stamp(p.ts, 13);
-    // local rank of each chunk channel (key descending, channel ascending: a
-    // total order, so the ranks are a permutation), RT threads per channel
-    // (consecutive lanes) each comparing a strided part of the chunk.  The
-    // chunk goes out sorted (keys and channels at its first channel); the
-    // top m are the speculative items, most likely first.
-    {
-        int RT = 8;
-        while (RT > 1 && RT * nch > kNT) RT >>= 1;
-        const int i = tid / RT, part = tid % RT;
-        const uint32_t mine = i < nch ? __float_as_uint(ctl.lsc[i]) : 0u;
-        int rank = 0;
-        if (i < nch)
-            for (int j = part; j < nch; j += RT) {
-                const uint32_t o = __float_as_uint(ctl.lsc[j]);
-                rank += (o > mine) || (o == mine && j < i);
-            }
-        for (int o = RT >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-        if (i < nch && part == 0) {
-            ctl.lrank[i] = (uint16_t)rank;
-            p.skey[cb0 + rank] = mine;
-            p.sidx[cb0 + rank] = (uint8_t)i;
-            if (rank < m) ctl.item[rank] = cb0 + i;
-        }
+    stamp(p.ts, 4);
+    // grid barrier 2: every chunk's keys and histogram counts are out (its
+    // __syncthreads also orders the shared-memory initialisation above)
+    if (!grid_barrier(p.bar, (unsigned)nb * (kBarriers * ep + 2u), p.status, p.limit_ns, ctl,
+                      false))
+        return;
+    // every CTA has read the call epoch (at its start): the next call's
+    if (b == 0 && tid == 0) *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;
+
+    // ------------------------------------------------ P3: selection, then stage 2
+    if (!select_items(p, ctl, area, nb, b, cb0, nch)) return;
+    const int m = ctl.n_items;  // every item is known before Stage 2 starts
+    if (tid == 0) {
+        mbar_arrive(&ctl.sel_bar);
+        stamp_here(p.ts, 5);
     }
     __syncthreads();
-    // this chunk's histogram counts and sorted list are out (CTA 0 waits for
-    // every chunk's flag); the test hook makes the last CTA withhold its flag
-    if (tid == 0 && !(p.inject == 1 && b == nb - 1)) st_release_gpu(p.ready + b, ep + 1u);
-    stamp(p.ts, 4);
-
-    // ------------------------------------------------ P3: selection + stage 2
-    if (b == 0) central_select(p, ctl, area, nb, ep);
     Stage2Args a;
     a.gateup = p.gateup;
     a.down_t = p.down_t;
@@ -1623,11 +1292,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     a.n_a = p.n_a;
     a.limit_ns = p.limit_ns;
     a.ts = p.ts;
-    if (wid == kSelectorWarp) {
-        if (!ctl.abort) await_selection(p, ctl, b, nb, cb0, nch, m, ep);
-    } else {
-        stage2_roles<CPT, Q8>(a, ctl, area, m);
-    }
+    if (wid != kSelectorWarp) stage2_roles<CPT, Q8>(a, ctl, area, m);
     stage2_join(a, ctl);
 }
 
@@ -1770,14 +1435,11 @@ int fused_max_blocks() { return kMaxBlocks; }
 bool fused_fits(int d, int F) {
     // P0: x (2 d) + kept list (4 d) + histograms; P1 adds the cp.async ring
     // (the running-total table reuses it); P3: the Stage-2 rings.
-    (void)F;
     const size_t p01 = (size_t)6 * d + 4096 + (size_t)16 * kRing * kNT;
     const Ring r = ring_for(d, 0);  // the bf16 rings are the larger
-    // the channel selection (CTA 0): x, three digit histograms, the sorted
-    // keys and chunk-local indices of every chunk, per-chunk tables, candidates
-    const size_t sel = (size_t)2 * d + (size_t)4 * (2 * kHistBins + 512) +
-                       (size_t)5 * padded_ff(F) + (size_t)4 * (11 * kMaxBlocks + 4) +
-                       (size_t)4 * kCandCap;
+    // the channel selection (every CTA): x, three digit histograms and
+    // every channel's score key
+    const size_t sel = (size_t)2 * d + (size_t)4 * (2 * kHistBins + 512) + (size_t)4 * padded_ff(F);
     return p01 <= area_budget() && ring_bytes(d, 0, r) <= area_budget() &&
            ring_bytes(d, 1, ring_for(d, 1)) <= area_budget() && sel <= area_budget() &&
            r.n_gu >= 1 && r.n_d >= 1 && d / 8 <= kXGroups * kNT;
@@ -1821,11 +1483,6 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     p.hist = L.ws->hist;
     p.part = L.ws->part;
     p.skey = L.ws->skey;
-    p.sidx = L.ws->sidx;
-    p.selc = L.ws->selc;
-    p.selpre = L.ws->selpre;
-    p.ulist = L.ws->ulist;
-    p.ready = L.ws->ready;
     p.idx_list = L.ws->idx_list;
     p.hch = L.ws->hch;
     p.kept_out = L.kept_out;

@@ -59,3 +59,47 @@ def y_errors(y_gpu, y_ref):
     err = np.abs(y_gpu - y_ref)
     rel = np.linalg.norm(y_gpu - y_ref) / max(np.linalg.norm(y_ref), 1e-30)
     return float(err.max()), float(rel)
+
+
+def check_step(prox, L, w, x, rho, kappa=0.5, px=None):
+    """One decode step through prox_ffn_debug against the oracle: the kept
+    inputs bit-exact, every score within half the tie band, the mask exact
+    outside the band, y and h within the bars on the GPU's own mask.  Returns
+    the debug outputs."""
+    wg, wu, wd = w
+    xb = host_bits(x)
+    r = prox.prox_ffn_debug(L, x.cuda(), rho, kappa)
+    torch.cuda.synchronize()
+    assert prox.prox_get_status(L) == 0
+    kx, k = oracle.keep_count(L.d_model, kappa), oracle.keep_count(L.d_ff, rho)
+    assert (r["kx"], r["k"]) == (kx, k)
+    # input sparsity: bit-exact
+    kept_or = oracle.input_topk(xb, kx)
+    assert np.array_equal(r["kept"].cpu().numpy(), kept_or)
+    # proxy scores and the mask
+    if px is None:
+        px = oracle.Proxy(wg, wu)
+    g, u, sc = oracle.proxy_scores(px.q_gate, px.s_gate, px.q_up, px.s_up, xb, kept_or)
+    sc_gpu = r["scores"].cpu().numpy().astype(np.float64)
+    # fp32 proxy vs fp64 oracle, measured on the ranking scale: the k-th score
+    # (or the median score, when k is so large that the k-th is near zero).
+    # The bound is half the tie band: with every score within band/2 of the
+    # oracle's, no two channels whose oracle scores lie outside the band around
+    # the k-th can change order, so the band covers all fp32 rounding.  (An fp32
+    # sum of k_x products that cancel to ~1/sqrt(k_x) of their magnitude sum
+    # carries ~sqrt(k_x) * 2^-24 relative error: about 1e-5 at k_x = 4096.)
+    kth = np.sort(sc)[::-1][k - 1]
+    scale = max(kth, float(np.median(sc)), 1e-30)
+    rel = np.abs(sc_gpu - sc) / np.maximum(np.abs(sc), scale)
+    assert rel.max() < TIE_BAND / 2, rel.max()
+    idx = r["idx"].cpu().numpy()
+    bad, in_band = tie_band_mask_check(idx, sc, k)
+    assert bad == 0, f"{bad} channels outside the tie band disagree ({in_band} in band)"
+    # Stage 2 on the GPU's mask
+    h_or, y_or = oracle.sparse_ffn(wg, wu, wd, xb, idx)
+    mx, rl = y_errors(r["y"].cpu().numpy(), y_or)
+    assert mx <= ATOL_Y and rl <= RTOL_L2_Y, (mx, rl)
+    assert mx <= 1e-3 * max(1.0, np.abs(y_or).max())  # fp32 path: far inside the bar
+    hh = r["h"].cpu().numpy().astype(np.float64)
+    assert np.allclose(hh, h_or, rtol=1e-4, atol=1e-4 * np.abs(h_or).max())
+    return r

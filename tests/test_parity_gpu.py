@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from free_swiglu_ffn_prox_b300 import synth
-from parity_util import (ATOL_Y, RTOL_L2_Y, TIE_BAND, decode_proxy, host_bits,
+from parity_util import (ATOL_Y, RTOL_L2_Y, TIE_BAND, check_step, decode_proxy, host_bits,
                          tie_band_mask_check, y_errors)
 
 pytestmark = pytest.mark.gpu
@@ -39,43 +39,7 @@ def _x(d, n_out, seed):
 
 
 def _check_step(prox, L, w, x, rho, kappa=0.5, px=None):
-    wg, wu, wd = w
-    xb = host_bits(x)
-    r = prox.prox_ffn_debug(L, x.cuda(), rho, kappa)
-    torch.cuda.synchronize()
-    assert prox.prox_get_status(L) == 0
-    kx, k = oracle.keep_count(L.d_model, kappa), oracle.keep_count(L.d_ff, rho)
-    assert (r["kx"], r["k"]) == (kx, k)
-    # input sparsity: bit-exact
-    kept_or = oracle.input_topk(xb, kx)
-    assert np.array_equal(r["kept"].cpu().numpy(), kept_or)
-    # proxy scores and the mask
-    if px is None:
-        px = oracle.Proxy(wg, wu)
-    g, u, sc = oracle.proxy_scores(px.q_gate, px.s_gate, px.q_up, px.s_up, xb, kept_or)
-    sc_gpu = r["scores"].cpu().numpy().astype(np.float64)
-    # fp32 proxy vs fp64 oracle, measured on the ranking scale: the k-th score
-    # (or the median score, when k is so large that the k-th is near zero).
-    # The bound is half the tie band: with every score within band/2 of the
-    # oracle's, no two channels whose oracle scores lie outside the band around
-    # the k-th can change order, so the band covers all fp32 rounding.  (An fp32
-    # sum of k_x products that cancel to ~1/sqrt(k_x) of their magnitude sum
-    # carries ~sqrt(k_x) * 2^-24 relative error: about 1e-5 at k_x = 4096.)
-    kth = np.sort(sc)[::-1][k - 1]
-    scale = max(kth, float(np.median(sc)), 1e-30)
-    rel = np.abs(sc_gpu - sc) / np.maximum(np.abs(sc), scale)
-    assert rel.max() < TIE_BAND / 2, rel.max()
-    idx = r["idx"].cpu().numpy()
-    bad, in_band = tie_band_mask_check(idx, sc, k)
-    assert bad == 0, f"{bad} channels outside the tie band disagree ({in_band} in band)"
-    # Stage 2 on the GPU's mask
-    h_or, y_or = oracle.sparse_ffn(wg, wu, wd, xb, idx)
-    mx, rl = y_errors(r["y"].cpu().numpy(), y_or)
-    assert mx <= ATOL_Y and rl <= RTOL_L2_Y, (mx, rl)
-    assert mx <= 1e-3 * max(1.0, np.abs(y_or).max())  # fp32 path: far inside the bar
-    hh = r["h"].cpu().numpy().astype(np.float64)
-    assert np.allclose(hh, h_or, rtol=1e-4, atol=1e-4 * np.abs(h_or).max())
-    return r
+    return check_step(prox, L, w, x, rho, kappa, px)
 
 
 @pytest.mark.parametrize("d,F", [(256, 688), (128, 64), (384, 1000), (1024, 77), (512, 3000)])
