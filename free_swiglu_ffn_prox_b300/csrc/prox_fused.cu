@@ -82,7 +82,6 @@ struct Ctl {
     uint64_t sel_bar;                // completes when the item list is final
     uint64_t done_bar;               // every warp is through its Stage-2 role
     uint64_t ld_bar;                 // bulk load of the proxy scales (P1)
-    uint64_t sel_ld;                 // bulk load of the digit-1 histogram
     uint64_t key_ld;                 // bulk load of every channel's score key
     int gu_last[kMaxStages], d_last[kMaxStages];
     float h[kMaxItems];              // h of each item
@@ -653,12 +652,13 @@ __device__ __forceinline__ void stage2_join(const Stage2Args& a, Ctl& ctl) {
 }
 
 // ------------------------------------------------------------ the selection
-constexpr int kPrefetchItems = 8;  // sure items per CTA prefetched into L2 during the selection
+constexpr int kPrefetchItems = 16;  // certain rows per CTA prefetched into L2 during the selection
 
 // Bulk prefetch of global memory into L2 (no shared-memory destination).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
+
 
 // Block-wide digit select, called by every thread: threads t < NB/4 read
 // bins 4t..4t+3 with one 16-byte load (consecutive threads, consecutive
@@ -667,12 +667,15 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 // ctl.sel[0..1].  If the bins hold fewer than krem counts ctl.sel[0] stays
 // 0xffffffff.
 template <int NB>
-__device__ __forceinline__ void block_select(const uint32_t* h, uint32_t krem, Ctl& ctl) {
+__device__ __forceinline__ void block_select(const uint32_t* h, uint32_t krem, Ctl& ctl,
+                                             const uint32_t* hg = nullptr) {
     constexpr int NQ = NB / 4, NW = NQ / 32;
     static_assert(NQ % 32 == 0 && NQ <= kNT, "bins");
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (tid < NQ) v = reinterpret_cast<const uint4*>(h)[tid];
+    // the bins from shared memory, or (hg given) from global memory through L2
+    if (tid < NQ) v = hg ? __ldcg(reinterpret_cast<const uint4*>(hg) + tid)
+                         : reinterpret_cast<const uint4*>(h)[tid];
     const uint32_t s = (v.x + v.y) + (v.z + v.w);
     uint32_t suf = s;  // sum over this and the higher lanes of the warp
 #pragma unroll
@@ -722,52 +725,52 @@ __device__ __forceinline__ void block_select(const uint32_t* h, uint32_t krem, C
 
 // Every CTA, all threads, once every channel's score key is published
 // (grid barrier 2): the exact channel top-k and this CTA's share of it.
-// The CTA stages the digit-1 histogram and all F score keys (channel order)
-// in shared memory; HBM is idle at this point, so the copies are L2 hits at
-// low latency.  Thread t owns the contiguous keys [t kpt, (t+1) kpt):
+// HBM is idle at this point, so the reads below are L2 hits at low latency:
+// the digit-1 histogram (every chunk added to it) straight into the threads
+// that select on it, and all F score keys (channel order) into shared
+// memory by one bulk copy, which lands while digit 1 is being selected.
 //   digit 1 (bits 30..20 of the score bits) of the k-th key from the
-//   histogram every chunk added to; digit 2 (bits 19..9) and digit 3
-//   (bits 8..0) from shared histograms over the keys that match so far;
+//   global histogram; digit 2 (bits 19..9) and digit 3 (bits 8..0) from
+//   shared histograms over the keys in the digit-1 bin (the candidates);
 //   then T (the k-th key) and r (keys equal to T to keep, lowest channels
-//   first).  One block scan of (keys above T, keys equal to T) per thread
-//   gives each thread the position of its first selected channel in the
-//   ascending list of selected channels; CTA b takes the positions
-//   [k b / n, k (b+1) / n) of that list as its Stage-2 items (an even split:
-//   every CTA moves the same bytes; every CTA computes the same T and
-//   prefixes, so the shares partition the mask).
-// As soon as digit 1 is known (and the staging copies are in), the lowest
-// channels of the CTA's own chunk above the digit-1 bin are certain: the
-// rows of the first kPrefetchItems of them are prefetched into L2, so HBM
-// streams while the selection finishes (whichever CTA's share holds them
-// finds them in L2).  Returns false on a timeout or a broken invariant
-// (ctl.abort set).
+//   first).  Thread t owns the keys [t kpt, (t+1) kpt); one block scan of
+//   (keys above T, keys equal to T) per thread gives each thread the
+//   position of its first selected channel in the ascending list of
+//   selected channels; CTA b takes the positions [k b / n, k (b+1) / n) of
+//   that list as its Stage-2 items (an even split: every CTA moves the same
+//   bytes; every CTA computes the same T and prefixes, so the shares
+//   partition the mask).
+// Costs measured on this part drove the layout: a block-wide select or scan
+// costs ~1000 cycles, a pass over all keys ~1500, and a shared store or
+// atomic inside a loop that loads from shared memory serialises each step,
+// so every pass over keys is loads-only and builds bit masks.  While it
+// runs, the first certain rows of the CTA's own chunk stream into L2.
+// Returns false on a timeout or a broken invariant (ctl.abort set).
 __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int nb, int b,
                              int cb0, int nch) {
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int tid = threadIdx.x;
     const int F = p.F, Fp = p.Fp;
-    uint32_t* h1 = reinterpret_cast<uint32_t*>(area + (size_t)2 * p.d);
-    uint32_t* h2 = h1 + kHistBins;
+    uint32_t* h2 = reinterpret_cast<uint32_t*>(area + (size_t)2 * p.d);
     uint32_t* h3 = h2 + kHistBins;
     uint32_t* sk = h3 + 512;  // [Fp] score keys, channel order
     if (tid == 0) {
         asm volatile("fence.proxy.async.global;" ::: "memory");
         const uint64_t pol = policy_evict_first();
-        mbar_arrive_expect_tx(&ctl.sel_ld, (uint32_t)(kHistBins * 4));
-        bulk_g2s(h1, p.hist, kHistBins * 4, &ctl.sel_ld, pol);
         mbar_arrive_expect_tx(&ctl.key_ld, (uint32_t)(Fp * 4));
         bulk_g2s(sk, p.skey, (uint32_t)(Fp * 4), &ctl.key_ld, pol);
     }
     for (int i = tid; i < kHistBins + 512; i += kNT) h2[i] = 0u;
     // waits for one of the staging copies; after a timeout lets both land
+    // (one thread polls the barrier; the block barrier then orders the data
+    // for every thread: 608 threads polling one mbarrier cost ~600 cycles)
     auto landed = [&](uint64_t* bar) {
-        if (!mbar_wait_bounded(bar, 0, p.limit_ns, &ctl.abort) && lane == 0) {
+        if (tid == 0 && !mbar_wait_bounded(bar, 0, p.limit_ns, &ctl.abort)) {
             ctl.abort = 1;
             record_status(p.status, PROX_ERR_TIMEOUT);
         }
         __syncthreads();
         if (!ctl.abort) return true;
         if (tid == 0) {
-            mbar_wait_bounded(&ctl.sel_ld, 0, p.limit_ns, nullptr);
             mbar_wait_bounded(&ctl.key_ld, 0, p.limit_ns, nullptr);
         }
         return false;
@@ -781,22 +784,26 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
         __syncthreads();
         return false;
     };
-    if (!landed(&ctl.sel_ld)) return false;
+    // digit 1 from the histogram of every chunk, read from L2 straight into
+    // the selecting threads (the keys still landing)
+    block_select<2048>(nullptr, (uint32_t)p.k, ctl, p.hist);
     stamp(p.ts, 14);
-    // digit 1 from the histogram of every chunk (the keys still landing)
-    block_select<2048>(h1, (uint32_t)p.k, ctl);
     if (ctl.sel[0] == 0xffffffffu) return broken();
     const uint32_t b1 = ctl.sel[0], k1 = ctl.sel[1];
-    // own channels above the digit-1 bin are certain: rank them in channel order
+    // own channels above the digit-1 bin are certain members of the mask:
+    // rank them in channel order (the barrier inside landed publishes the
+    // warp counts); once the keys are in (no more staging traffic to delay),
+    // the first kPrefetchItems of them start streaming into L2, each by its
+    // own thread, while the rest of the selection runs; the CTA whose share
+    // holds them finds them in L2 (shares follow channel order, so mostly
+    // this CTA or a neighbour)
     const bool sure = tid < nch && (__float_as_uint(ctl.lsc[tid]) >> 20) > b1;
     const unsigned sb = __ballot_sync(0xffffffffu, sure);
-    if (lane == 0) ctl.warp_tot[wid] = __popc(sb);
-    if (!landed(&ctl.key_ld)) return false;  // (its barrier also publishes warp_tot)
+    if ((tid & 31) == 0) ctl.warp_tot[tid >> 5] = __popc(sb);
+    if (!landed(&ctl.key_ld)) return false;
     if (sure) {
-        // every staging copy has landed, so the rest of the selection reads
-        // shared memory only: start HBM on the first certain rows now
-        int rank = __popc(sb & ((1u << lane) - 1u));
-        for (int w = 0; w < wid; ++w) rank += (int)ctl.warp_tot[w];  // nch <= 256: <= 7 warps
+        int rank = __popc(sb & ((1u << (tid & 31)) - 1u));
+        for (int w = 0; w < (tid >> 5); ++w) rank += (int)ctl.warp_tot[w];  // nch <= 256: <= 7 warps
         if (rank < kPrefetchItems) {
             const int c = cb0 + tid;
             const size_t gb = gu_row_bytes(p.d, p.q8), db = down_row_bytes(p.d, p.q8);
@@ -804,21 +811,34 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
             prefetch_l2(p.down_t + (size_t)c * db, (uint32_t)db);
         }
     }
-    // this thread's keys: [i0, i1)
-    const int kpt = (F + kNT - 1) / kNT;
-    const int i0 = min(F, tid * kpt), i1 = min(F, i0 + kpt);
-    // digit 2 over the keys in the digit-1 bin
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t kk = sk[i];
-        if ((kk >> 20) == b1) atomicAdd(&h2[(kk >> 9) & 2047u], 1u);
+    // Thread t owns the keys [i0, i1) = [t kpt, (t+1) kpt) (channel order).
+    // kpt is odd, so the threads of a warp stepping through their keys
+    // together hit 32 different shared-memory banks (an even stride such as
+    // 24 puts 8 of them on each bank).  Every loop over keys is loads-only:
+    // on this part a shared store or atomic inside a loop that also loads
+    // from shared memory serialises each step (~200 cycles instead of ~20),
+    // so the passes build per-thread bit masks (kpt <= 55 < 64) and the
+    // stores come afterwards, over the few set bits.
+    const int kpt = ((F + kNT - 1) / kNT) | 1;
+    const int i0 = min(F, tid * kpt), n = min(F, i0 + kpt) - i0;
+    const uint32_t* mk = sk + i0;
+    uint64_t above = 0, cmask = 0;  // keys above the digit-1 bin / in it (candidates)
+    for (int e = 0; e < n; ++e) {
+        const uint32_t d1 = mk[e] >> 20;
+        above |= (uint64_t)(d1 > b1) << e;
+        cmask |= (uint64_t)(d1 == b1) << e;
+    }
+    for (uint64_t m = cmask; m; m &= m - 1) {
+        const uint32_t kk = mk[__ffsll((long long)m) - 1];
+        atomicAdd(&h2[(kk >> 9) & 2047u], 1u);
     }
     __syncthreads();
     block_select<2048>(h2, k1, ctl);
     if (ctl.sel[0] == 0xffffffffu) return broken();
     const uint32_t pre = (b1 << 11) | ctl.sel[0], k2 = ctl.sel[1];
-    // digit 3 over the keys matching both digits
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t kk = sk[i];
+    // digit 3 over the candidates matching both digits
+    for (uint64_t m = cmask; m; m &= m - 1) {
+        const uint32_t kk = mk[__ffsll((long long)m) - 1];
         if ((kk >> 9) == pre) atomicAdd(&h3[kk & 511u], 1u);
     }
     __syncthreads();
@@ -827,40 +847,43 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
     const uint32_t T = (pre << 9) | ctl.sel[0];
     const uint32_t r = ctl.sel[1];  // keys equal to T to keep, lowest channels first
     stamp(p.ts, 15);
-    // this thread's keys above and equal to T; one scan gives the selected
-    // channels and the ties before it (gt <= F <= 32768 < 2^16: no carry)
-    uint32_t gt = 0, eq = 0;
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t kk = sk[i];
-        gt += kk > T;
-        eq += kk == T;
+    // this thread's keys above T and equal to T (T lies in the digit-1 bin,
+    // so only the candidates need a look); one scan gives the selected
+    // channels and the ties before this thread (counts <= F <= 32768 < 2^16)
+    uint64_t gtm = above, eqm = 0;
+    for (uint64_t m = cmask; m; m &= m - 1) {
+        const int e = __ffsll((long long)m) - 1;
+        const uint32_t kk = mk[e];
+        if (kk > T) gtm |= 1ull << e;
+        else if (kk == T) eqm |= 1ull << e;
     }
+    const uint32_t gt = (uint32_t)__popcll(gtm), eq = (uint32_t)__popcll(eqm);
     uint32_t tot;
     const uint32_t ex = block_excl_scan<kNT>(gt | (eq << 16), ctl, tot);
-    uint32_t ties = ex >> 16;
-    uint32_t pos = (ex & 0xffffu) + min(ties, r);  // selected channels before this thread's
+    const uint32_t ties = ex >> 16;
+    const uint32_t pos = (ex & 0xffffu) + min(ties, r);  // selected channels before this thread's
     if ((tot & 0xffffu) + min(tot >> 16, r) != (uint32_t)p.k) return broken();
     const int q0 = chunk_begin(p.k, b, nb), q1 = chunk_begin(p.k, b + 1, nb);
     if (q1 - q0 > kMaxItems) return broken();
-    if ((int)pos < q1 && (int)(pos + gt + eq) >= q0) {  // this thread may hold some of the share
-        for (int i = i0; i < i1 && (int)pos < q1; ++i) {
-            const uint32_t kk = sk[i];
-            bool sel = kk > T;
-            if (kk == T) sel = ties++ < r;
-            if (sel) {
-                if ((int)pos >= q0) {
-                    ctl.item[pos - q0] = i;
-                    ctl.conf[pos - q0] = 1;
-                }
-                ++pos;
-            }
-        }
+    // the ties this thread keeps: its lowest min(eq, r - ties) tie bits
+    uint32_t keep = ties < r ? min(eq, r - ties) : 0u;
+    uint64_t sel = gtm;
+    for (uint64_t m = eqm; m && keep; m &= m - 1, --keep) sel |= m & (~m + 1);
+    // a thread whose selected channels meet [q0, q1) writes those items; in
+    // debug mode CTA 0 writes the whole mask
+    const int nsel = __popcll(sel);
+    if ((int)pos < q1 && (int)pos + nsel > q0) {
+        int at = (int)pos;
+        for (uint64_t m = sel; m && at < q1; m &= m - 1, ++at)
+            if (at >= q0) ctl.item[at - q0] = i0 + __ffsll((long long)m) - 1;
     }
+    if (p.debug && b == 0) {
+        int at = (int)pos;
+        for (uint64_t m = sel; m; m &= m - 1, ++at) p.idx_list[at] = i0 + __ffsll((long long)m) - 1;
+    }
+    for (int i = tid; i < q1 - q0; i += kNT) ctl.conf[i] = 1;
     if (tid == 0) ctl.n_items = q1 - q0;
     __syncthreads();
-    // debug: the whole mask, ascending (every CTA writes its share)
-    if (p.debug)
-        for (int i = tid; i < q1 - q0; i += kNT) p.idx_list[q0 + i] = ctl.item[i];
     return true;
 }
 
@@ -879,6 +902,16 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         ctl.epoch = *reinterpret_cast<volatile unsigned*>(p.epoch);
         mbar_init(&ctl.ld_bar, 1);
         fence_mbar_init();
+    } else if (tid == kNT - 32) {
+        // the barriers of the selection and of Stage 2 (this warp has no x
+        // group at the common sizes, so the set-up costs the input phase nothing)
+        stage2_init(ctl, p.n_gu, p.n_d);
+        mbar_init(&ctl.key_ld, 1);
+        fence_mbar_init();
+    }
+    for (int i = tid; i < kMaxItems; i += kNT) {
+        ctl.conf[i] = 0;
+        ctl.hready[i] = 0;
     }
 
     // ------------------------------------------------ P0: input sparsity
@@ -1251,16 +1284,6 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                              : "memory");
         }
     }
-    for (int i = tid; i < kMaxItems; i += kNT) {
-        ctl.conf[i] = 0;
-        ctl.hready[i] = 0;
-    }
-    if (tid == 0) {
-        stage2_init(ctl, p.n_gu, p.n_d);
-        mbar_init(&ctl.sel_ld, 1);
-        mbar_init(&ctl.key_ld, 1);
-        fence_mbar_init();
-    }
     stamp(p.ts, 13);
     stamp(p.ts, 4);
     // grid barrier 2: every chunk's keys and histogram counts are out (its
@@ -1439,7 +1462,7 @@ bool fused_fits(int d, int F) {
     const Ring r = ring_for(d, 0);  // the bf16 rings are the larger
     // the channel selection (every CTA): x, three digit histograms and
     // every channel's score key
-    const size_t sel = (size_t)2 * d + (size_t)4 * (2 * kHistBins + 512) + (size_t)4 * padded_ff(F);
+    const size_t sel = (size_t)2 * d + (size_t)4 * (kHistBins + 512) + (size_t)4 * padded_ff(F);
     return p01 <= area_budget() && ring_bytes(d, 0, r) <= area_budget() &&
            ring_bytes(d, 1, ring_for(d, 1)) <= area_budget() && sel <= area_budget() &&
            r.n_gu >= 1 && r.n_d >= 1 && d / 8 <= kXGroups * kNT;

@@ -77,10 +77,11 @@ def _load():
             lib.oracle_quantize_rows_q8.argtypes = [_i32, _i32, _ptr, _ptr, _ptr]
             lib.oracle_sparse_ffn_q8.argtypes = [_i32, _i32] + [_ptr] * 7 + [_i32, _ptr, _ptr, _ptr]
             lib.oracle_block_topk.argtypes = [_i32, _ptr, _i32, _i32, _ptr, _ptr]
+            lib.oracle_contrib_scores.argtypes = [_i32, _i32, _ptr, _ptr, _ptr]
             for name in ("oracle_quantize", "oracle_input_topk", "oracle_proxy_scores",
                          "oracle_channel_topk", "oracle_sparse_ffn", "oracle_dense_ffn",
                          "oracle_prox_ffn", "oracle_residual_rmsnorm", "oracle_quantize_rows_q8",
-                         "oracle_sparse_ffn_q8", "oracle_block_topk"):
+                         "oracle_sparse_ffn_q8", "oracle_block_topk", "oracle_contrib_scores"):
                 getattr(lib, name).restype = _i32
             _lib = lib
     return _lib
@@ -174,6 +175,21 @@ def proxy_scores(q_gate, s_gate, q_up, s_up, x_bits, kept):
     _check(lib.oracle_proxy_scores(F, d, _p(qg), _p(sg), _p(qu), _p(su), _p(x), kept.size,
                                    _p(kept), _p(g), _p(u), _p(sc)), "proxy_scores")
     return g, u, sc
+
+
+def contrib_scores(state_score, w_down_bits) -> np.ndarray:
+    """Second selection signal (COUNTDOWN reading): |h~_c| * ||W_down[:, c]||_2,
+    the magnitude of channel c's term of the down projection's linear
+    combination, from the proxy state score |h~_c| (fp64)."""
+    lib = _load()
+    sc = _c(state_score, np.float64).ravel()
+    wd = _c(w_down_bits, np.uint16)
+    d, F = wd.shape
+    if sc.size != F:
+        raise ValueError("state_score must have d_ff entries")
+    out = np.empty(F)
+    _check(lib.oracle_contrib_scores(F, d, _p(wd), _p(sc), _p(out)), "contrib_scores")
+    return out
 
 
 def channel_topk(score: np.ndarray, k: int) -> np.ndarray:

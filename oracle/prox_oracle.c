@@ -251,6 +251,29 @@ int oracle_proxy_scores(int F, int d,
 /* a3: the shared channel mask ([Prox] Abstract: mask from the magnitude
  * ranking).  Reading: the k channels with the largest score (ties -> lower
  * channel), emitted in ascending channel order. */
+/* Second selection signal, COUNTDOWN style ("COUNTDOWN", Abstract: the
+ * FFN output is a linear combination of the down projection's columns,
+ * y = sum_c h_c W_down[:, c], whose coefficients carry the sparsity;
+ * M-COUNTDOWN ranks by indirect, predictor-free coefficients).  Reading: the
+ * proxy's approximate coefficient magnitude |h~_c| = state_score[c] weighted
+ * by the norm of the column it scales, i.e. the magnitude of that term of
+ * the linear combination:  out[c] = state_score[c] * ||W_down[:, c]||_2,
+ * with the norm in fp64 over the bf16 column.  (D-COUNTDOWN's trained
+ * predictor of the direct coefficients is out of scope.) */
+int oracle_contrib_scores(int F, int d, const uint16_t* w_down, const double* state_score,
+                          double* out) {
+    if (F <= 0 || d <= 0 || !w_down || !state_score || !out) return ORACLE_BAD_ARG;
+    for (int c = 0; c < F; ++c) {
+        double ss = 0.0;
+        for (int i = 0; i < d; ++i) {
+            double w = oracle_bf16_to_double(w_down[(size_t)i * F + c]);
+            ss += w * w;
+        }
+        out[c] = state_score[c] * sqrt(ss);
+    }
+    return ORACLE_OK;
+}
+
 int oracle_channel_topk(int F, const double* score, int k, int32_t* idx) {
     if (!score || !idx) return ORACLE_BAD_ARG;
     return topk_ascending(F, score, k, idx);

@@ -432,6 +432,52 @@ def test_residual_rmsnorm_golden_cases_reject_plausible_mistakes():
                    for eps, xs, ys, want in cases), slip
 
 
+def _contrib_cases():
+    for line in open(os.path.join(GOLDEN, "contrib_cases.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        wd, st, k, want, idx = (f.strip() for f in line.split("|"))
+        rows = [[float(v) for v in r.split()] for r in wd.split(";")]
+        yield (np.array(rows), np.array([float(v) for v in st.split()]), int(k),
+               np.array([float(v) for v in want.split()]), np.array([int(v) for v in idx.split()]))
+
+
+def test_contrib_scores_golden_cases(oracle_mod):
+    """The COUNTDOWN-style signal |h~_c| ||W_down[:, c]|| against hand-worked
+    values (tests/golden/contrib_cases.txt), and the mask it keeps."""
+    for wd, st, k, want, idx in _contrib_cases():
+        got = oracle_mod.contrib_scores(st, _bf16_bits(wd))
+        assert np.allclose(got, want, rtol=1e-15, atol=0), (got, want)
+        assert np.array_equal(oracle_mod.channel_topk(got, k), idx)
+
+
+def test_contrib_scores_invariants(oracle_mod):
+    """Scaling one column of W_down by a power of two scales that channel's
+    score by the same factor and no other; with every column of one norm the
+    signal keeps the same channels as the state score; permuting the channels
+    of the state scores and of W_down permutes the scores."""
+    rng = np.random.default_rng(31)
+    d, F = 64, 40
+    wd = rng.standard_normal((d, F)) * 0.02
+    st = np.abs(rng.standard_normal(F))
+    base = oracle_mod.contrib_scores(st, _bf16_bits(wd))
+    wd2 = oracle_mod.bf16_bits_to_f64(_bf16_bits(wd)).copy()
+    wd2[:, 7] *= 4.0
+    sc2 = oracle_mod.contrib_scores(st, _bf16_bits(wd2))
+    assert sc2[7] == 4.0 * base[7]
+    assert np.array_equal(np.delete(sc2, 7), np.delete(base, 7))
+    # one column norm: a signed permutation of one column in every channel
+    col = rng.standard_normal(d) * 0.02
+    wd_eq = np.stack([rng.permutation(col) * rng.choice([-1.0, 1.0], size=d) for _ in range(F)], axis=1)
+    sc_eq = oracle_mod.contrib_scores(st, _bf16_bits(wd_eq))
+    for k in (1, 7, 20, 40):
+        assert np.array_equal(oracle_mod.channel_topk(sc_eq, k), oracle_mod.channel_topk(st, k))
+    perm = rng.permutation(F)
+    sc_p = oracle_mod.contrib_scores(st[perm], _bf16_bits(wd)[:, perm])
+    assert np.array_equal(sc_p, base[perm])
+
+
 # ---------------------------------------------------------------- int8 Stage 2
 def _exact_bf16_bits(v):
     """bf16 bit patterns of float values that are exact in bf16."""
