@@ -16,8 +16,8 @@ static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 size_t workspace_bytes(int d, int F) {
     const size_t Fp = (size_t)padded_ff(F);
     return kControlBytes + align256((size_t)kHistWords * 4) +
-           align256((size_t)kMaxSlices * Fp * 8) + 2 * align256((size_t)(kMaxGrid + 1) * 4) +
-           4 * align256(Fp * 4) + align256(Fp) + align256((size_t)d * 2) + align256((size_t)d * 4);
+           align256((size_t)kMaxSlices * Fp * 8) + 4 * align256(Fp * 4) +
+           align256((size_t)d * 2) + align256((size_t)d * 4);
 }
 
 Workspace carve_workspace(void* base, int d, int F) {
@@ -26,26 +26,19 @@ Workspace carve_workspace(void* base, int d, int F) {
     Workspace w;
     w.status = reinterpret_cast<int*>(p);
     w.bar = reinterpret_cast<unsigned*>(p + 128);
-    w.ready = reinterpret_cast<unsigned*>(p + 1024);
     p += kControlBytes;
     w.hist = reinterpret_cast<uint32_t*>(p);
     p += align256((size_t)kHistWords * 4);
     w.part = reinterpret_cast<float2*>(p);
     p += align256((size_t)kMaxSlices * Fp * 8);
-    w.selc = reinterpret_cast<int*>(p);
-    p += align256((size_t)(kMaxGrid + 1) * 4);
-    w.selpre = reinterpret_cast<int*>(p);
-    p += align256((size_t)(kMaxGrid + 1) * 4);
     w.skey = reinterpret_cast<uint32_t*>(p);
-    p += align256(Fp * 4);
-    w.ulist = reinterpret_cast<int*>(p);
     p += align256(Fp * 4);
     w.idx_list = reinterpret_cast<int*>(p);
     p += align256(Fp * 4);
     w.hch = reinterpret_cast<float*>(p);
     p += align256(Fp * 4);
-    w.sidx = p;
-    p += align256(Fp);
+    w.dnorm = reinterpret_cast<float*>(p);
+    p += align256(Fp * 4);
     w.x_stage = reinterpret_cast<uint16_t*>(p);
     p += align256((size_t)d * 2);
     w.y_stage = reinterpret_cast<float*>(p);
@@ -87,7 +80,8 @@ prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, fl
                      float* h_out, cudaStream_t stream, long long limit_ns, int inject,
                      cudaEvent_t const* ev = nullptr, uint64_t* ts = nullptr,
                      const void* x_prev = nullptr, const float* y_prev = nullptr,
-                     void* x_out = nullptr, float eps = 0.0f, int bw = 0) {
+                     void* x_out = nullptr, float eps = 0.0f, int bw = 0,
+                     bool contrib = false) {
     prox::FusedLaunch f;
     f.codes = L->codes;
     f.scales = L->scales;
@@ -102,6 +96,7 @@ prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, fl
     f.k = bw > 0 ? bw * prox_keep_count(L->d_ff / bw, keep_fraction)  // whole blocks
                  : prox_keep_count(L->d_ff, keep_fraction);
     f.bw = bw;
+    f.dnorm = contrib ? L->ws.dnorm : nullptr;
     f.ws = &L->ws;
     f.kept_out = kept_out;
     f.scores_out = scores_out;
@@ -182,7 +177,8 @@ prox_status prepare(int d_model, int d_ff, const void* w_gate, const void* w_up,
                                  static_cast<const __nv_bfloat16*>(w_down),
                                  static_cast<uint8_t*>(proxy_codes),
                                  static_cast<__half2*>(proxy_scales),
-                                 gateup, down_t, q8, s);
+                                 gateup, down_t, q8,
+                                 prox::carve_workspace(workspace, d_model, d_ff).dnorm, s);
     if (e != cudaSuccess) return PROX_ERR_CUDA;
     // one persistent CTA per SM; every CTA holds its chunk of the channels
     // in shared memory
@@ -318,6 +314,60 @@ prox_status prox_ffn_resnorm(const prox_layer* layer, const void* x_prev, const 
                     nullptr, x_prev, y_prev, x_out, eps);
 }
 
+prox_status prox_stack_ffn(const prox_layer* const* layers, int n_layers, const void* x0,
+                           float keep_fraction, float eps, void* xs, float* ys,
+                           prox_stream_t stream) {
+    if (!layers || !x0 || !xs || !ys || n_layers < 1) return PROX_ERR_INVALID_ARG;
+    if (n_layers > prox::kMaxStack) return PROX_ERR_UNSUPPORTED_SHAPE;
+    if (!frac_ok(keep_fraction) || !(eps >= 0.0f) || !isfinite(eps)) return PROX_ERR_INVALID_ARG;
+    const prox_layer* L0 = layers[0];
+    if (!L0) return PROX_ERR_INVALID_ARG;
+    if (!aligned16(x0) || !aligned16(xs) || !aligned16(ys)) return PROX_ERR_MISALIGNED;
+    const size_t d = (size_t)L0->d_model, n = (size_t)n_layers;
+    if (overlap(x0, 2 * d, xs, 2 * d * n) || overlap(x0, 2 * d, ys, 4 * d * n) ||
+        overlap(xs, 2 * d * n, ys, 4 * d * n))
+        return PROX_ERR_INVALID_ARG;
+    prox::StackLayers sl;
+    sl.n = n_layers;
+    sl.x0 = static_cast<const uint16_t*>(x0);
+    sl.xs = static_cast<uint16_t*>(xs);
+    sl.ys = ys;
+    for (int l = 0; l < n_layers; ++l) {
+        const prox_layer* L = layers[l];
+        if (!L) return PROX_ERR_INVALID_ARG;
+        if (L->d_model != L0->d_model || L->d_ff != L0->d_ff || L->q8 != L0->q8 ||
+            L->device != L0->device || L->num_blocks != L0->num_blocks)
+            return PROX_ERR_INVALID_ARG;
+        sl.layer[l].codes = L->codes;
+        sl.layer[l].scales = L->scales;
+        sl.layer[l].gateup = static_cast<const uint8_t*>(L->gateup);
+        sl.layer[l].down_t = static_cast<const uint8_t*>(L->down_t);
+    }
+    prox::FusedLaunch f;
+    f.codes = L0->codes;
+    f.scales = L0->scales;
+    f.gateup = L0->gateup;
+    f.down_t = L0->down_t;
+    f.q8 = L0->q8;
+    f.d = L0->d_model;
+    f.F = L0->d_ff;
+    f.x = sl.x0;
+    f.y = ys;
+    f.kx = prox_keep_count(L0->d_model, 0.5f);
+    f.k = prox_keep_count(L0->d_ff, keep_fraction);
+    f.eps = eps;
+    f.ws = &L0->ws;  // the first layer's workspace serves the whole launch
+    f.kept_out = nullptr;
+    f.scores_out = nullptr;
+    f.idx_out = nullptr;
+    f.h_out = nullptr;
+    f.num_blocks = L0->num_blocks;
+    f.limit_ns = prox::kWaitLimitNs;
+    f.inject = 0;
+    f.ts = nullptr;
+    return cuda_status(prox::launch_stack(f, sl, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 prox_status prox_dense_ffn(const prox_layer* layer, const void* x, float* y,
                            prox_stream_t stream) {
     prox_status st = check_call(layer, x, y);
@@ -390,6 +440,30 @@ prox_status prox_ffn_blocks_debug(const prox_layer* layer, const void* x, int bl
     return run_prox(layer, x, keep_fraction, 0.5f, y, nullptr, scores, idx, h,
                     reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0, nullptr,
                     nullptr, nullptr, nullptr, nullptr, 0.0f, block_width);
+}
+
+prox_status prox_ffn_contrib(const prox_layer* layer, const void* x, float keep_fraction, float* y,
+                             prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    if (!frac_ok(keep_fraction)) return PROX_ERR_INVALID_ARG;
+    return run_prox(layer, x, keep_fraction, 0.5f, y, nullptr, nullptr, nullptr, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0, nullptr,
+                    nullptr, nullptr, nullptr, nullptr, 0.0f, 0, true);
+}
+
+prox_status prox_ffn_contrib_debug(const prox_layer* layer, const void* x, float keep_fraction,
+                                   float* y, float* scores, int32_t* idx, float* h,
+                                   prox_stream_t stream) {
+    prox_status st = check_call(layer, x, y);
+    if (st != PROX_OK) return st;
+    if (!frac_ok(keep_fraction)) return PROX_ERR_INVALID_ARG;
+    const void* outs[] = {scores, idx, h};
+    for (const void* p : outs)
+        if (p && !aligned16(p)) return PROX_ERR_MISALIGNED;
+    return run_prox(layer, x, keep_fraction, 0.5f, y, nullptr, scores, idx, h,
+                    reinterpret_cast<cudaStream_t>(stream), prox::kWaitLimitNs, 0, nullptr,
+                    nullptr, nullptr, nullptr, nullptr, 0.0f, 0, true);
 }
 
 prox_status prox_residual_rmsnorm(int d_model, const void* x, const float* y, float eps,

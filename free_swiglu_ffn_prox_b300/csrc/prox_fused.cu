@@ -76,29 +76,6 @@ __device__ __forceinline__ void stamp_here(uint64_t* ts, int i) {
     if (ts) ts[(size_t)blockIdx.x * kPhaseStamps + i] = global_timer_ns();
 }
 
-struct Ctl {
-    uint64_t gu_full[kMaxStages], gu_empty[kMaxStages];
-    uint64_t d_full[kMaxStages], d_empty[kMaxStages];
-    uint64_t sel_bar;                // completes when the item list is final
-    uint64_t done_bar;               // every warp is through its Stage-2 role
-    uint64_t ld_bar;                 // bulk load of the proxy scales (P1)
-    uint64_t key_ld;                 // bulk load of every channel's score key
-    int gu_last[kMaxStages], d_last[kMaxStages];
-    float h[kMaxItems];              // h of each item
-    int item[kMaxItems];             // channel of each item
-    uint8_t conf[kMaxItems];         // item is in the mask (pass B adds it)
-    uint8_t hready[kMaxItems];       // h[i] written by pass A
-    float lsc[kMaxChunk];            // scores of this CTA's chunk
-    __align__(16) uint32_t warp_tot[(kNT / 32 + 4) / 4 * 4];  // per-warp totals, read as uint4
-    uint32_t sel[4];
-    unsigned epoch;
-    int abort;
-    int n_items;
-};
-
-constexpr size_t ctl_bytes() { return (sizeof(Ctl) + 127) / 128 * 128; }
-__host__ __device__ constexpr size_t area_budget_dev() { return kSmemLimit - ctl_bytes(); }
-
 struct FusedParams {
     // layer
     const uint8_t* codes;
@@ -115,6 +92,7 @@ struct FusedParams {
     // starts are multiples of it) whose summed score ranks the whole block;
     // 0: the per-channel mask
     int bw;
+    const float* dnorm;      // contribution-ranked selection: ||W_down[:, c]|| (null: |h~_c|)
     // optional stack glue in front of the step: x = bf16(RMSNorm(x_prev + y_prev))
     const uint16_t* x_prev;  // null: x is given
     const float* y_prev;
@@ -143,6 +121,31 @@ struct FusedParams {
     int inject;          // 1: the last CTA withholds its grid-barrier arrival (test hook)
     uint64_t* ts;        // [gridDim][kPhaseStamps] %globaltimer stamps, or null
 };
+
+struct Ctl {
+    uint64_t gu_full[kMaxStages], gu_empty[kMaxStages];
+    uint64_t d_full[kMaxStages], d_empty[kMaxStages];
+    uint64_t sel_bar;                // completes when the item list is final
+    uint64_t done_bar;               // every warp is through its Stage-2 role
+    uint64_t ld_bar;                 // bulk load of the proxy scales (P1)
+    uint64_t key_ld;                 // bulk load of every channel's score key
+    int gu_last[kMaxStages], d_last[kMaxStages];
+    float h[kMaxItems];              // h of each item
+    int item[kMaxItems];             // channel of each item
+    uint8_t conf[kMaxItems];         // item is in the mask (pass B adds it)
+    uint8_t hready[kMaxItems];       // h[i] written by pass A
+    float lsc[kMaxChunk];            // scores of this CTA's chunk
+    __align__(16) uint32_t warp_tot[(kNT / 32 + 4) / 4 * 4];  // per-warp totals, read as uint4
+    uint32_t sel[4];
+    unsigned epoch;
+    int abort;
+    int n_items;
+    FusedParams sp;                  // the current layer's parameters (stack launch)
+};
+
+constexpr size_t ctl_bytes() { return (sizeof(Ctl) + 127) / 128 * 128; }
+__host__ __device__ constexpr size_t area_budget_dev() { return kSmemLimit - ctl_bytes(); }
+
 
 // First channel of chunk b (F <= 32768 and b <= 256, so F b fits 32 bits;
 // a 64-bit division costs hundreds of instructions on the GPU).
@@ -615,8 +618,22 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
     }
 }
 
-// Initialises the Stage-2 ring barriers (thread 0; the caller synchronises).
-__device__ __forceinline__ void stage2_init(Ctl& ctl, int n_gu, int n_d) {
+// Initialises the Stage-2 ring barriers (one thread; the caller
+// synchronises).  reinit: an earlier step of this launch initialised them
+// (same ring geometry), so they are invalidated first.
+__device__ __forceinline__ void stage2_init(Ctl& ctl, int n_gu, int n_d, bool reinit = false) {
+    if (reinit) {
+        for (int s = 0; s < n_gu; ++s) {
+            mbar_inval(&ctl.gu_full[s]);
+            mbar_inval(&ctl.gu_empty[s]);
+        }
+        for (int s = 0; s < n_d; ++s) {
+            mbar_inval(&ctl.d_full[s]);
+            mbar_inval(&ctl.d_empty[s]);
+        }
+        mbar_inval(&ctl.sel_bar);
+        mbar_inval(&ctl.done_bar);
+    }
     for (int s = 0; s < n_gu; ++s) {
         mbar_init(&ctl.gu_full[s], 1);
         mbar_init(&ctl.gu_empty[s], 1);
@@ -888,24 +905,34 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
 }
 
 // ------------------------------------------------------------ fused kernel
+// One decode step (one layer) inside a persistent launch.  The grid
+// barrier word counts arrivals and is never reset between launches: gen is
+// the number of grid barriers completed before this launch (read at its
+// start), and this step's two barriers are number gen + bi + 1 and
+// gen + bi + 2 (barrier j completes when the word reaches n j); bi > 0
+// marks a later step of a stacked launch (its mbarriers are re-used).  The last
+// step of a launch publishes gen + bi + 2 for the next launch (every CTA
+// has read gen by then).  Returns false when the CTA must leave (a wait ran
+// out or a check failed; the status word says which).
 template <int CPT, bool Q8>
-__global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
-    uint8_t* area = smem_raw + ctl_bytes();  // phase-dependent union
+__device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8_t* area,
+                                           unsigned gen, unsigned bi, bool last) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nb = gridDim.x, b = blockIdx.x;
     const int d = p.d, F = p.F, Fp = p.Fp;
     stamp(p.ts, 0);
+    // a later step of a stacked launch finds the barriers of the step before
+    // it still valid in shared memory: invalidate, then initialise
+    const bool reinit = bi > 0;
     if (tid == 0) {
-        ctl.abort = 0;
-        ctl.epoch = *reinterpret_cast<volatile unsigned*>(p.epoch);
+        if (reinit) mbar_inval(&ctl.ld_bar);
         mbar_init(&ctl.ld_bar, 1);
         fence_mbar_init();
     } else if (tid == kNT - 32) {
         // the barriers of the selection and of Stage 2 (this warp has no x
         // group at the common sizes, so the set-up costs the input phase nothing)
-        stage2_init(ctl, p.n_gu, p.n_d);
+        stage2_init(ctl, p.n_gu, p.n_d, reinit);
+        if (reinit) mbar_inval(&ctl.key_ld);
         mbar_init(&ctl.key_ld, 1);
         fence_mbar_init();
     }
@@ -943,9 +970,10 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                 uint4 xb = make_uint4(0u, 0u, 0u, 0u);
                 float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
                 if (valid(q)) {
-                    xb = __ldg(reinterpret_cast<const uint4*>(p.x_prev) + g0 + q);
-                    y0 = __ldg(reinterpret_cast<const float4*>(p.y_prev) + 2 * (g0 + q));
-                    y1 = __ldg(reinterpret_cast<const float4*>(p.y_prev) + 2 * (g0 + q) + 1);
+                    // through L2: a stacked launch wrote them in an earlier layer
+                    xb = __ldcg(reinterpret_cast<const uint4*>(p.x_prev) + g0 + q);
+                    y0 = __ldcg(reinterpret_cast<const float4*>(p.y_prev) + 2 * (g0 + q));
+                    y1 = __ldcg(reinterpret_cast<const float4*>(p.y_prev) + 2 * (g0 + q) + 1);
                 }
                 const uint32_t w[4] = {xb.x, xb.y, xb.z, xb.w};
                 const float yy[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
@@ -1215,10 +1243,9 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         }
     }
     stamp(p.ts, 2);
-    const unsigned ep = ctl.epoch;
-    if (!grid_barrier(p.bar, (unsigned)nb * (kBarriers * ep + 1u), p.status, p.limit_ns, ctl,
+    if (!grid_barrier(p.bar, (unsigned)nb * (gen + bi + 1u), p.status, p.limit_ns, ctl,
                       p.inject == 1 && b == nb - 1))
-        return;
+        return false;
     stamp(p.ts, 3);
 
     // ------------------------------------------------ P2: scores + histogram
@@ -1241,8 +1268,10 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
                     g += v[sl].x;
                     u += v[sl].y;
                 }
-            // |silu(g~) * u~|, silu(z) = z / (1 + e^-z)
-            const float sc = fabsf(g / (1.0f + expf(-g)) * u);
+            // |silu(g~) * u~|, silu(z) = z / (1 + e^-z); the contribution
+            // signal weights it by the norm of the W_down column it scales
+            float sc = fabsf(g / (1.0f + expf(-g)) * u);
+            if (p.dnorm) sc *= __ldg(p.dnorm + c);
             if (p.scores_out) p.scores_out[c] = sc;
             ctl.lsc[tid] = sc;
             key = __float_as_uint(sc);
@@ -1288,14 +1317,13 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     stamp(p.ts, 4);
     // grid barrier 2: every chunk's keys and histogram counts are out (its
     // __syncthreads also orders the shared-memory initialisation above)
-    if (!grid_barrier(p.bar, (unsigned)nb * (kBarriers * ep + 2u), p.status, p.limit_ns, ctl,
-                      false))
-        return;
-    // every CTA has read the call epoch (at its start): the next call's
-    if (b == 0 && tid == 0) *reinterpret_cast<volatile unsigned*>(p.epoch) = ep + 1u;
+    if (!grid_barrier(p.bar, (unsigned)nb * (gen + bi + 2u), p.status, p.limit_ns, ctl, false))
+        return false;
+    // every CTA has read gen (at the launch start): the next launch's
+    if (last && b == 0 && tid == 0) *reinterpret_cast<volatile unsigned*>(p.epoch) = gen + bi + 2u;
 
     // ------------------------------------------------ P3: selection, then stage 2
-    if (!select_items(p, ctl, area, nb, b, cb0, nch)) return;
+    if (!select_items(p, ctl, area, nb, b, cb0, nch)) return false;
     const int m = ctl.n_items;  // every item is known before Stage 2 starts
     if (tid == 0) {
         mbar_arrive(&ctl.sel_bar);
@@ -1317,6 +1345,69 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     a.ts = p.ts;
     if (wid != kSelectorWarp) stage2_roles<CPT, Q8>(a, ctl, area, m);
     stage2_join(a, ctl);
+    return !*reinterpret_cast<volatile int*>(&ctl.abort);
+}
+
+// The decode step: one layer per launch.
+template <int CPT, bool Q8>
+__global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
+    uint8_t* area = smem_raw + ctl_bytes();  // phase-dependent union
+    if (threadIdx.x == 0) {
+        ctl.abort = 0;
+        ctl.epoch = *reinterpret_cast<volatile unsigned*>(p.epoch);
+    }
+    __syncthreads();
+    fused_step<CPT, Q8>(p, ctl, area, ctl.epoch, 0u, true);
+}
+
+// A stack of layers in one launch: layer l takes x_l = bf16(RMSNorm(x_{l-1}
+// + y_{l-1})) (l > 0; computed inside its own step) and writes y_l; a grid
+// barrier between layers makes y_{l-1} complete before layer l reads it.
+// Each layer's parameters are the base parameters with that layer's
+// weights and buffers, copied into shared memory for its step.  Layer l's
+// step barriers are number gen + 3l + 1 and + 2; the barrier in front of
+// layer l > 0 is number gen + 3l.
+template <int CPT, bool Q8>
+__global__ void __launch_bounds__(kNT, 1) k_prox_stack(const FusedParams base, const StackLayers sl) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
+    uint8_t* area = smem_raw + ctl_bytes();
+    const int tid = threadIdx.x, nb = gridDim.x;
+    if (tid == 0) {
+        ctl.abort = 0;
+        ctl.epoch = *reinterpret_cast<volatile unsigned*>(base.epoch);
+    }
+    __syncthreads();
+    const unsigned gen = ctl.epoch;
+    for (int l = 0; l < sl.n; ++l) {
+        const unsigned bi = 3u * (unsigned)l;
+        if (l > 0 && !grid_barrier(base.bar, (unsigned)nb * (gen + bi), base.status, base.limit_ns,
+                                   ctl, false))
+            return;
+        if (tid == 0) {
+            FusedParams q = base;
+            const StackLayer& ly = sl.layer[l];
+            q.codes = ly.codes;
+            q.scales = ly.scales;
+            q.gateup = ly.gateup;
+            q.down_t = ly.down_t;
+            q.y = sl.ys + (size_t)l * base.d;
+            if (l == 0) {
+                q.x = sl.x0;
+                q.x_prev = nullptr;
+            } else {
+                q.x = nullptr;
+                q.x_prev = l == 1 ? sl.x0 : sl.xs + (size_t)(l - 1) * base.d;
+                q.y_prev = sl.ys + (size_t)(l - 1) * base.d;
+                q.x_out = sl.xs + (size_t)l * base.d;
+            }
+            ctl.sp = q;
+        }
+        __syncthreads();
+        if (!fused_step<CPT, Q8>(ctl.sp, ctl, area, gen, bi, l + 1 == sl.n)) return;
+    }
 }
 
 // Dense baseline: Stage 2 over every channel, CTA i taking [F i/n, F (i+1)/n)
@@ -1436,6 +1527,14 @@ cudaError_t fused_configure() {
     if (e == cudaSuccess) e = set_smem(k_prox_fused<2, true>);
     if (e == cudaSuccess) e = set_smem(k_prox_fused<4, true>);
     if (e == cudaSuccess) e = set_smem(k_prox_fused<8, true>);
+    if (e == cudaSuccess) e = set_smem(k_prox_stack<1, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_stack<2, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_stack<4, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_stack<8, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_stack<1, true>);
+    if (e == cudaSuccess) e = set_smem(k_prox_stack<2, true>);
+    if (e == cudaSuccess) e = set_smem(k_prox_stack<4, true>);
+    if (e == cudaSuccess) e = set_smem(k_prox_stack<8, true>);
     if (e == cudaSuccess) e = set_smem(k_dense<1, false>);
     if (e == cudaSuccess) e = set_smem(k_dense<2, false>);
     if (e == cudaSuccess) e = set_smem(k_dense<4, false>);
@@ -1476,8 +1575,8 @@ cudaError_t launch_fused_t(const cudaLaunchConfig_t& cfg, const FusedParams& p) 
 }
 }  // namespace
 
-cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
-    if (L.num_blocks < 1 || L.num_blocks > kMaxBlocks) return cudaErrorInvalidValue;
+namespace {
+FusedParams make_params(const FusedLaunch& L) {
     FusedParams p;
     p.codes = L.codes;
     p.scales = L.scales;
@@ -1492,6 +1591,7 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     p.kx = L.kx;
     p.k = L.k;
     p.bw = L.bw;
+    p.dnorm = L.dnorm;
     p.x_prev = L.x_prev;
     p.y_prev = L.y_prev;
     p.x_out = L.x_out;
@@ -1518,16 +1618,34 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     p.limit_ns = L.limit_ns;
     p.inject = L.inject;
     p.ts = L.ts;
+    return p;
+}
+
+cudaLaunchConfig_t coop_config(int blocks, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(L.num_blocks);
+    cfg.gridDim = dim3(blocks);
     cfg.blockDim = dim3(kNT);
     cfg.dynamicSmemBytes = kSmemLimit;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int CPT>
+cudaError_t launch_stack_t(const cudaLaunchConfig_t& cfg, const FusedParams& p, const StackLayers& sl) {
+    return p.q8 ? cudaLaunchKernelEx(&cfg, k_prox_stack<CPT, true>, p, sl)
+                : cudaLaunchKernelEx(&cfg, k_prox_stack<CPT, false>, p, sl);
+}
+}  // namespace
+
+cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
+    if (L.num_blocks < 1 || L.num_blocks > kMaxBlocks) return cudaErrorInvalidValue;
+    const FusedParams p = make_params(L);
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = coop_config(L.num_blocks, stream, attr);
     const int nchunk = L.d / 8;
     cudaError_t e;
     if (nchunk <= kPassB) e = launch_fused_t<1>(cfg, p);
@@ -1540,6 +1658,23 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
         e = cudaGetLastError();
     }
     return e;
+}
+
+cudaError_t launch_stack(const FusedLaunch& L, const StackLayers& sl, cudaStream_t stream) {
+    if (L.num_blocks < 1 || L.num_blocks > kMaxBlocks || sl.n < 1 || sl.n > kMaxStack)
+        return cudaErrorInvalidValue;
+    FusedParams p = make_params(L);
+    p.debug = 0;
+    p.kept_out = nullptr;
+    p.scores_out = nullptr;
+    p.ts = nullptr;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = coop_config(L.num_blocks, stream, attr);
+    const int nchunk = L.d / 8;
+    if (nchunk <= kPassB) return launch_stack_t<1>(cfg, p, sl);
+    if (nchunk <= 2 * kPassB) return launch_stack_t<2>(cfg, p, sl);
+    if (nchunk <= 4 * kPassB) return launch_stack_t<4>(cfg, p, sl);
+    return launch_stack_t<8>(cfg, p, sl);
 }
 
 cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const uint16_t* x, int d,

@@ -27,21 +27,16 @@ constexpr size_t kControlBytes = 2048;
 
 // Workspace carve-out (offsets in bytes, each 256-aligned).  The first
 // kControlBytes are the control block: status word, then (at +128) the grid
-// barrier count, the call epoch and the channel-selection result flag, then
-// (at +1024) the per-chunk ready flags; a fault clears the whole block.
+// barrier count and the call epoch; a fault clears the whole block.
 struct Workspace {
     int* status;        // [0] device status word (0 = ok)
-    unsigned* bar;      // grid barrier count; bar[1] call epoch; bar[2..5] selection result
+    unsigned* bar;      // grid barrier count; bar[1] call epoch
     uint32_t* hist;     // [kHistWords] score histogram, zeroed by each call
     float2* part;       // [kMaxSlices][Fp] per-slice proxy partials (g~, u~)
-    uint32_t* skey;     // [Fp] per chunk: its score bits sorted descending
-    uint8_t* sidx;      // [Fp] per chunk: the chunk-local channel indices in that order
-    int* selc;          // [kMaxGrid] per chunk: selected channels
-    int* selpre;        // [kMaxGrid] debug: prefix of selc
-    int* ulist;         // [Fp] the channels handed out by the selection
-    unsigned* ready;    // [kMaxGrid] per-chunk ready flags (in the control block)
+    uint32_t* skey;     // [Fp] every channel's score key (fp32 score bits)
     int* idx_list;      // [Fp] debug: selected channels, ascending
     float* hch;         // [Fp] debug: h per channel
+    float* dnorm;       // [Fp] ||W_down[:, c]||_2 per channel, written by prepare (persistent)
     uint16_t* x_stage;  // [d] bf16 input staged from host memory (prox_ffn_host)
     float* y_stage;     // [d] fp32 output staged for host memory (prox_ffn_host)
 };
@@ -63,6 +58,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");
+}
+
+// Invalidates an initialised mbarrier.  A step that reuses the shared
+// memory of an earlier step in the same launch must invalidate each of its
+// mbarriers before initialising it again: re-initialising a valid mbarrier
+// is undefined (PTX ISA, mbarrier.init), and on this part such a barrier's
+// first phase was never seen to complete by a parity-0 wait.
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Makes mbarrier initialisation visible to the async (bulk-copy) proxy.
@@ -167,7 +171,8 @@ __device__ __forceinline__ void record_status(int* status, int code) {
 // bytes), see prox_prepare_q8.
 cudaError_t launch_prepare(int d, int F, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
                            const __nv_bfloat16* w_down, uint8_t* codes, __half2* scales,
-                           void* gateup, void* down_t, int q8, cudaStream_t stream);
+                           void* gateup, void* down_t, int q8, float* down_norms,
+                           cudaStream_t stream);
 
 // Bytes of one Stage-2 gate|up row and one W_down^T row in device memory.
 constexpr size_t gu_row_bytes(int d, int q8) { return q8 ? (size_t)2 * d + 16 : (size_t)4 * d; }
@@ -191,6 +196,9 @@ struct FusedLaunch {
     float* y;
     int kx, k;
     int bw = 0;          // block-granular mask: channels per block (0: per channel)
+    // second selection signal: rank by |h~_c| ||W_down[:, c]|| (the
+    // contribution of channel c) instead of |h~_c|; null: the state signal
+    const float* dnorm = nullptr;
     // optional stack glue: x = bf16(RMSNorm(x_prev + y_prev)) computed in the
     // step itself (x unused, x_out receives it); x_prev null: plain step
     const uint16_t* x_prev = nullptr;
@@ -208,6 +216,23 @@ struct FusedLaunch {
     uint64_t* ts;        // phase stamps [num_blocks][PROX_PHASE_STAMPS] or null
 };
 
+// A stack of layers run in one persistent launch (launch_stack): per layer
+// its weights; the layers share shape, workspace and grid.
+constexpr int kMaxStack = 64;
+struct StackLayer {
+    const uint8_t* codes;
+    const __half2* scales;
+    const uint8_t* gateup;
+    const uint8_t* down_t;
+};
+struct StackLayers {
+    int n;
+    const uint16_t* x0;  // bf16 [d]: layer 0's input
+    uint16_t* xs;        // bf16 [n][d]: x_l for l >= 1 (row 0 unused)
+    float* ys;           // fp32 [n][d]: y_l
+    StackLayer layer[kMaxStack];
+};
+
 cudaError_t fused_configure();
 bool fused_fits(int d, int F);
 int fused_threads();
@@ -215,6 +240,9 @@ int fused_max_chunk();
 int fused_max_blocks();
 size_t fused_smem_bytes();
 cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream);
+// The stack launch: layers[l] of the same shape (L.q8 for all), first
+// layer on x0, layer l > 0 on x_l = bf16(RMSNorm(x_{l-1} + y_{l-1}) / eps).
+cudaError_t launch_stack(const FusedLaunch& L, const StackLayers& sl, cudaStream_t stream);
 cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const uint16_t* x, int d,
                          int F, float* y, int* status, int num_blocks, long long limit_ns,
                          uint64_t* ts, cudaStream_t stream);

@@ -104,6 +104,7 @@ extern "C" PROX_API prox_status prox_ffn_noalloc(const prox_layer* layer, const 
     if (cudaMemsetAsync(base, 0, prox::kControlBytes, s) != cudaSuccess) return PROX_ERR_CUDA;
     prox::Workspace ws = prox::carve_workspace(base, layer->d_model, layer->d_ff);
     ws.status = layer->ws.status;  // faults stay visible to prox_get_status(layer)
+    ws.dnorm = layer->ws.dnorm;    // per-layer data written by prepare
     prox::FusedLaunch f;
     f.codes = layer->codes;
     f.scales = layer->scales;

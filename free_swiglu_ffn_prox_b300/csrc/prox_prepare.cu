@@ -160,11 +160,30 @@ k_q8_down(const __nv_bfloat16* __restrict__ w_down, int8_t* __restrict__ down_q8
 
 }  // namespace
 
+// ||W_down[:, c]||_2 of every channel c in fp32 (the weight of channel c's
+// term in the down projection's linear combination y = sum_c h_c W_down[:, c],
+// used by the contribution-ranked selection).  Thread c walks column c of the
+// bf16 W_down [d][F]; consecutive threads read consecutive elements.
+__global__ void __launch_bounds__(256)
+    k_col_norms(const __nv_bfloat16* __restrict__ w_down, float* __restrict__ norms, int d, int F, int Fp) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= Fp) return;
+    float ss = 0.0f;
+    if (c < F)
+        for (int i = 0; i < d; ++i) {
+            const float w = __bfloat162float(w_down[(size_t)i * F + c]);
+            ss = fmaf(w, w, ss);
+        }
+    norms[c] = sqrtf(ss);
+}
+
 cudaError_t launch_prepare(int d, int F, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
                            const __nv_bfloat16* w_down, uint8_t* codes, __half2* scales,
-                           void* gateup, void* down_t, int q8, cudaStream_t stream) {
+                           void* gateup, void* down_t, int q8, float* down_norms,
+                           cudaStream_t stream) {
     const int Fp = padded_ff(F);
     const int G = d / kGroup;
+    k_col_norms<<<(Fp + 255) / 256, 256, 0, stream>>>(w_down, down_norms, d, F, Fp);
     dim3 qgrid((Fp + 127) / 128, G);
     k_quantize_pack<<<qgrid, 128, 0, stream>>>(w_gate, w_up, codes, scales, d, F, Fp);
     cudaError_t e = cudaGetLastError();

@@ -71,6 +71,9 @@ def _load():
             "prox_ffn_blocks": (i32, [vp, vp, i32, f32, vp, vp]),
             "prox_ffn_batch": (i32, [vp, vp, i32, f32, vp, vp]),
             "prox_ffn_blocks_debug": (i32, [vp, vp, i32, f32, vp, vp, vp, vp, vp]),
+            "prox_ffn_contrib": (i32, [vp, vp, f32, vp, vp]),
+            "prox_stack_ffn": (i32, [ctypes.POINTER(vp), i32, vp, f32, f32, vp, vp, vp]),
+            "prox_ffn_contrib_debug": (i32, [vp, vp, f32, vp, vp, vp, vp, vp]),
             "prox_residual_rmsnorm": (i32, [i32, vp, vp, f32, vp, vp]),
             "prox_ffn_resnorm": (i32, [vp, vp, vp, f32, vp, f32, vp, vp]),
             "prox_get_status": (i32, [vp, vp]),
@@ -274,6 +277,53 @@ def prox_ffn_noalloc(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, y=
     _check(fn(layer.handle, _ptr(x), float(keep_fraction), _ptr(y), _stream(stream)),
            "prox_ffn_noalloc")
     return y
+
+
+def prox_ffn_contrib(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, y=None,
+                     stream=None):
+    """The decode step ranking channels by |h~_c| ||W_down[:, c]|| (the
+    COUNTDOWN-style contribution signal) instead of |h~_c|."""
+    y = _x_y(layer, x, y)
+    _check(_load().prox_ffn_contrib(layer.handle, _ptr(x), float(keep_fraction), _ptr(y),
+                                    _stream(stream)), "prox_ffn_contrib")
+    return y
+
+
+def prox_ffn_contrib_debug(layer: ProxLayer, x: torch.Tensor, keep_fraction: float,
+                           stream=None) -> dict:
+    """prox_ffn_contrib plus its scores, channel list and h (device tensors)."""
+    y = _x_y(layer, x, None)
+    dev = x.device
+    k = prox_keep_count(layer.d_ff, keep_fraction)
+    scores = torch.empty(layer.d_ff, dtype=torch.float32, device=dev)
+    idx = torch.empty(max(k, 1), dtype=torch.int32, device=dev)
+    h = torch.empty(max(k, 1), dtype=torch.float32, device=dev)
+    _check(_load().prox_ffn_contrib_debug(layer.handle, _ptr(x), float(keep_fraction), _ptr(y),
+                                          _ptr(scores), _ptr(idx), _ptr(h), _stream(stream)),
+           "prox_ffn_contrib_debug")
+    return {"y": y, "scores": scores, "idx": idx[:k], "h": h[:k], "k": k}
+
+
+def prox_stack_ffn(layers, x0: torch.Tensor, keep_fraction: float, eps: float = 1e-6,
+                   xs=None, ys=None, stream=None):
+    """n layers in one persistent launch: layer 0 on x0, layer l > 0 on
+    x_l = bf16(RMSNorm(x_{l-1} + y_{l-1})).  Returns (xs bf16 [n][d] with row l
+    = x_l for l >= 1, ys fp32 [n][d] with row l = y_l)."""
+    n = len(layers)
+    d = layers[0].d_model
+    _need(x0, torch.bfloat16, (d,), "x0")
+    if xs is None:
+        xs = torch.zeros(n, d, dtype=torch.bfloat16, device=x0.device)
+    if ys is None:
+        ys = torch.empty(n, d, dtype=torch.float32, device=x0.device)
+    _need(xs, torch.bfloat16, (n, d), "xs")
+    _need(ys, torch.float32, (n, d), "ys")
+    handles = (ctypes.c_void_p * n)(*[L.handle.value if isinstance(L.handle, ctypes.c_void_p)
+                                      else L.handle for L in layers])
+    _check(_load().prox_stack_ffn(ctypes.cast(handles, ctypes.POINTER(ctypes.c_void_p)), n,
+                                  _ptr(x0), float(keep_fraction), float(eps), _ptr(xs), _ptr(ys),
+                                  _stream(stream)), "prox_stack_ffn")
+    return xs, ys
 
 
 def prox_dense_ffn(layer: ProxLayer, x: torch.Tensor, y=None, stream=None):

@@ -43,7 +43,7 @@
  *   - Calls that share one prox_layer use its workspace and must be ordered
  *     with respect to each other (one stream, or events); calls on
  *     different layers are independent.
- *   - Shapes: d_model a multiple of 128 in [128, 10496] (the step's
+ *   - Shapes: d_model a multiple of 128 in [128, 10880] (the step's
  *     shared-memory tables must fit one SM); d_ff in [1, 32768]
  *     (prox_prepare also needs ceil(d_ff / #SMs) <= 256 and at most 256 SMs).
  *   - Inputs must be finite (no NaN or Inf in x or the weights).
@@ -265,6 +265,53 @@ PROX_API prox_status prox_ffn_blocks_debug(const prox_layer* layer, const void* 
                                   float* scores, int32_t* idx, float* h,
                                   prox_stream_t stream);
 
+/*
+ * The decode step with a second selection signal, after the COUNTDOWN page
+ * ("COUNTDOWN", Abstract): the FFN output is a linear combination of the
+ * down projection's columns, y = sum_c h_c W_down[:, c], and its
+ * predictor-free variant ranks channels by indirect coefficients.  Here
+ * channel c is ranked by the magnitude of its term of that combination,
+ *   score_c = |silu(g~_c) u~_c| * ||W_down[:, c]||_2,
+ * with g~, u~ the Prox proxy state (Stage 1 as in prox_ffn) and the column
+ * norms computed in fp32 by prox_prepare (kept in the layer's workspace);
+ * the k = ceil(rho d_ff) largest are kept (ties to the lower channel) and
+ * Stage 2 is prox_ffn's.  x bf16 [d_model], y fp32 [d_model], both device;
+ * input keep 0.5.  Same status and ordering rules as prox_ffn.
+ */
+PROX_API prox_status prox_ffn_contrib(const prox_layer* layer, const void* x, float keep_fraction,
+                                      float* y, prox_stream_t stream);
+
+/* prox_ffn_contrib plus the contribution scores (fp32 [d_ff]), the channel
+ * list (int32 [k], ascending) and h (fp32 [k], in list order); any of the
+ * three may be NULL; non-NULL ones 16-byte aligned (parity checks). */
+PROX_API prox_status prox_ffn_contrib_debug(const prox_layer* layer, const void* x,
+                                            float keep_fraction, float* y, float* scores,
+                                            int32_t* idx, float* h, prox_stream_t stream);
+
+/*
+ * A stack of n_layers decode steps in ONE persistent launch (the stacked
+ * residual-stream workload: x_{l+1} = RMSNorm(x_l + y_l), no learned gain):
+ *   layer 0 runs prox_ffn on x0; layer l > 0 runs it on
+ *   x_l = bf16_rne((x_{l-1} + y_{l-1}) / sqrt(mean((x_{l-1} + y_{l-1})^2) + eps)),
+ *   computed inside layer l's own step; a grid barrier between layers makes
+ *   y_{l-1} complete before layer l reads it, so no launch separates them.
+ *   layers   host array of n_layers handles of one shape (d_model, d_ff, the
+ *            same Stage-2 format and device); 1 <= n_layers <= 64
+ *            (PROX_ERR_UNSUPPORTED_SHAPE beyond); the launch uses
+ *            layers[0]'s workspace and status word (prox_get_status(layers[0]))
+ *   x0       bf16 [d_model], device: layer 0's input
+ *   xs       bf16 [n_layers][d_model], device: row l receives x_l (l >= 1;
+ *            row 0 is left as it is)
+ *   ys       fp32 [n_layers][d_model], device: row l receives y_l
+ * keep_fraction in (0, 1] for every layer, input keep 0.5, eps >= 0.  x0, xs
+ * and ys must not overlap (PROX_ERR_INVALID_ARG); all 16-byte aligned.
+ * The layers' workspaces other than the first are not touched; calls that
+ * share layers[0] must be ordered as for prox_ffn.
+ */
+PROX_API prox_status prox_stack_ffn(const prox_layer* const* layers, int n_layers, const void* x0,
+                                    float keep_fraction, float eps, void* xs, float* ys,
+                                    prox_stream_t stream);
+
 /* Dense SwiGLU FFN, Eq. (1) of the PrunePath page over all d_ff channels,
  * streaming the same gateup / down_t buffers (the in-library dense
  * baseline).  x bf16 [d_model], y fp32 [d_model], both device. */
@@ -324,9 +371,9 @@ PROX_API prox_status prox_ffn_resnorm(const prox_layer* layer, const void* x_pre
  *   y  fp32 [d_model], device, overwritten as by prox_ffn.
  * Limits and rules:
  *   - the layer's workspace (prox_query_sizes().workspace) must fit in
- *     4 MiB: every d_ff up to 28352 at any supported d_model does, so the
- *     Llama-2-7B and Llama-3-8B shapes do; d_ff 28672 fits only with
- *     d_model <= 3968, so the Llama-3-70B shape does not; larger layers
+ *     4 MiB: every d_ff up to 28544 at any supported d_model does, so the
+ *     Llama-2-7B and Llama-3-8B shapes do; d_ff 28672 fits up to d_model
+ *     9216, so the Llama-3-70B shape (d_model 8192) does too; larger layers
  *     return PROX_ERR_UNSUPPORTED_SHAPE and queue nothing;
  *   - the layer's device must be the current device (else
  *     PROX_ERR_INVALID_ARG);

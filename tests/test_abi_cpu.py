@@ -145,14 +145,17 @@ def test_bad_arguments_are_rejected_before_any_device_work(lib):
 
 def test_no_alloc_scratch_limit_as_documented(lib):
     """prox_ffn_noalloc's 4 MiB scratch holds the workspace of every d_ff up to
-    28352 at any supported d_model; d_ff 28672 only up to d_model 3968."""
+    28544 at any supported d_model (up to 10880); d_ff 28672 up to d_model
+    9216, which includes the Llama-3-70B shape; the bounds are exact."""
     from free_swiglu_ffn_prox_b300 import prox
 
     lim = 4 << 20
-    for d in (128, 4096, 8192, 10496):
-        assert prox.prox_query_sizes(d, 28352)["workspace"] <= lim
-    assert prox.prox_query_sizes(3968, 28672)["workspace"] <= lim
-    for d in (4096, 8192):
-        assert prox.prox_query_sizes(d, 28672)["workspace"] > lim
+    for d in (128, 4096, 8192, 10880):
+        assert prox.prox_query_sizes(d, 28544)["workspace"] <= lim
+    assert prox.prox_query_sizes(10880, 28608)["workspace"] > lim
+    assert prox.prox_query_sizes(9216, 28672)["workspace"] <= lim
+    assert prox.prox_query_sizes(9344, 28672)["workspace"] > lim
+    with pytest.raises(prox.ProxError):
+        prox.prox_query_sizes(11008, 64)  # beyond the supported d_model
     for d, F in ((4096, 11008), (4096, 14336)):
         assert prox.prox_query_sizes(d, F)["workspace"] <= lim

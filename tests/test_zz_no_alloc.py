@@ -79,14 +79,15 @@ def _oracle_y_on_gpu_mask(prox, L, w_host, x, rho):
     return y_or
 
 
-@pytest.mark.parametrize("d,F", [(1024, 3000), (10752, 28352)])
+@pytest.mark.parametrize("d,F", [(1024, 3000), (10880, 28544), (8192, 28672)])
 def test_no_alloc_matches_the_oracle_and_allocates_nothing(prox, d, F):
-    """y against the oracle on the GPU's mask, on a small layer and on one at
-    the documented limit (d_ff 28352 at the largest supported d_model, whose
-    workspace fills all but ~6 KB of the 4 MiB array, so its last buffers sit
-    at the end of the array); free device memory is the same before and after
-    repeated calls (the first call, which may load the library's module and
-    look up the array, comes before the measurement)."""
+    """y against the oracle on the GPU's mask, on a small layer, on one at the
+    documented limit (d_ff 28544 at the largest supported d_model, whose
+    workspace fills all but ~8 KB of the 4 MiB array, so its last buffers sit
+    at the end of the array) and on the Llama-3-70B shape; free device memory
+    is the same before and after repeated calls (the first call, which may
+    load the library's module and look up the array, comes before the
+    measurement)."""
     oracle.build()
     wg, wu, wd = synth.make_weights(d, F, 0.02, 61, device="cuda")
     sizes = prox.prox_query_sizes(d, F)
