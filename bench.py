@@ -514,10 +514,12 @@ def run_gpu(args):
                     if peak_kind == "measured" else "fallback 6.4 TB/s",
                     "timing": how}
         step_gbs = ab["step"] / (ms_per_step * 1e-3) / 1e9
+        extras["peak"] = {"hbm_gbs": hbm_peak, "source": roofline["peak_source"],
+                          "note": "every frac_of_peak below divides by this"}
         extras["kernels"] = kern
         extras["step_roofline"] = {
             "alg_bytes": ab["step"], "achieved_gbs": round(step_gbs, 1),
-            "frac_of_measured": round(step_gbs / hbm_peak, 4),
+            "frac_of_peak": round(step_gbs / hbm_peak, 4),
             "frac_of_8tbs_spec": round(step_gbs / SPEC_HBM_GBS, 4)}
 
         # ------------------------------------------------ keep-fraction sweep
@@ -535,7 +537,7 @@ def run_gpu(args):
             sweep[str(fr)] = {"k": kk, "us_per_token": round(us, 3),
                               "tokens_per_s": round(1e6 / us, 1), "alg_bytes": abf,
                               "gbs": round(abf / (us * 1e-6) / 1e9, 1),
-                              "frac_of_measured": round(abf / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+                              "frac_of_peak": round(abf / (us * 1e-6) / 1e9 / hbm_peak, 4)}
         extras["keep_fraction_sweep"] = sweep
 
         # ------------------------------------------------ spread of the headline
@@ -568,7 +570,7 @@ def run_gpu(args):
         dus = m * 1e3 / n
         extras["dense"] = {"us_per_token": round(dus, 3),
                            "gbs": round(ab["dense"] / (dus * 1e-6) / 1e9, 1),
-                           "frac_of_measured": round(ab["dense"] / (dus * 1e-6) / 1e9 / hbm_peak, 4),
+                           "frac_of_peak": round(ab["dense"] / (dus * 1e-6) / 1e9 / hbm_peak, 4),
                            "speedup_prox_over_dense": round(dus / (ms_per_step * 1e3), 3)}
 
         # ------------------------------------------------ int8 Stage-2 rows
@@ -597,7 +599,7 @@ def run_gpu(args):
             blocks[str(bw)] = {"blocks_kept": kk // bw, "of_blocks": E, "k": kk,
                                "us_per_token": round(us, 3), "alg_bytes": abb,
                                "gbs": round(abb / (us * 1e-6) / 1e9, 1),
-                               "frac_of_measured": round(abb / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+                               "frac_of_peak": round(abb / (us * 1e-6) / 1e9 / hbm_peak, 4)}
         for L in wl.layers:
             if prox.prox_get_status(L) != 0:
                 raise SystemExit("device status set in the block-mask measurement")
@@ -618,7 +620,7 @@ def run_gpu(args):
         extras["contrib_signal"] = {
             "us_per_token": round(us, 3), "tokens_per_s": round(1e6 / us, 1),
             "gbs": round(ab["step"] / (us * 1e-6) / 1e9, 1),
-            "frac_of_measured": round(ab["step"] / (us * 1e-6) / 1e9 / hbm_peak, 4),
+            "frac_of_peak": round(ab["step"] / (us * 1e-6) / 1e9 / hbm_peak, 4),
             "signal": "|silu(g~) u~| * ||W_down[:, c]|| (prox_ffn_contrib), keep_fraction 0.3"}
 
         # ------------------------------------------------ batch of 8 tokens, per-token masks
@@ -770,7 +772,7 @@ def shape_sweep(prox, synth, shape, dev, stream, hbm_peak, l2):
         out["keep_fraction"][str(fr)] = {"k": k, "us_per_token": round(us, 3),
                                          "tokens_per_s": round(1e6 / us, 1), "alg_bytes": ab,
                                          "gbs": round(gbs, 1),
-                                         "frac_of_measured": round(gbs / hbm_peak, 4),
+                                         "frac_of_peak": round(gbs / hbm_peak, 4),
                                          "frac_of_8tbs_spec": round(gbs / SPEC_HBM_GBS, 4)}
 
     def dn(i):
@@ -784,7 +786,7 @@ def shape_sweep(prox, synth, shape, dev, stream, hbm_peak, l2):
     dus = m * 1e3 / CHUNK
     dab = algorithmic_bytes(d, F, F, kx)["dense"]
     out["dense"] = {"us_per_token": round(dus, 3), "gbs": round(dab / (dus * 1e-6) / 1e9, 1),
-                    "frac_of_measured": round(dab / (dus * 1e-6) / 1e9 / hbm_peak, 4)}
+                    "frac_of_peak": round(dab / (dus * 1e-6) / 1e9 / hbm_peak, 4)}
     for fr, v in out["keep_fraction"].items():
         v["speedup_over_dense"] = round(dus / v["us_per_token"], 3)
     for L in layers:
@@ -837,7 +839,7 @@ def q8_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak, l2, bf16_us_per
         us = m * 1e3 / n
         gbs = ab[mode] / (us * 1e-6) / 1e9
         out[mode] = {"us_per_token": round(us, 3), "alg_bytes": ab[mode], "gbs": round(gbs, 1),
-                     "frac_of_measured": round(gbs / hbm_peak, 4)}
+                     "frac_of_peak": round(gbs / hbm_peak, 4)}
     for L in layers:
         if prox.prox_get_status(L) != 0:
             raise SystemExit("device status set in the int8 Stage-2 measurement")
@@ -903,14 +905,14 @@ def stack_extra(prox, synth, dev, stream, rho, hbm_peak, tokens_per_graph=8, rep
         us = ms * 1e3 / n
         res[name] = {"us_per_token": round(us, 2), "us_per_layer": round(us / shape.layers, 3),
                      "tokens_per_s": round(1e6 / us, 1), "gbs": round(ab / (us * 1e-6) / 1e9, 1),
-                     "frac_of_measured": round(ab / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+                     "frac_of_peak": round(ab / (us * 1e-6) / 1e9 / hbm_peak, 4)}
         del g
     finite = bool(torch.isfinite(ys_st[-1]).all()) and bool(torch.isfinite(ys[-1]).all())
     one = res["one_launch"]
     out = {"layers": shape.layers, "keep_fraction": rho, "tokens": n,
            "us_per_token": one["us_per_token"], "us_per_layer": one["us_per_layer"],
            "tokens_per_s": one["tokens_per_s"], "alg_bytes_per_token": ab,
-           "gbs": one["gbs"], "frac_of_measured": one["frac_of_measured"],
+           "gbs": one["gbs"], "frac_of_peak": one["frac_of_peak"],
            "launches_per_token": 1, "final_hidden_finite": finite,
            "launch_per_layer": res["launch_per_layer"],
            "glue": "residual + RMSNorm fused into each later layer's step; the headline "
