@@ -56,7 +56,6 @@ constexpr size_t kDRingBytes = 48 * 1024;     // W_down^T bytes in flight per SM
 constexpr int kMaxItems = 512;            // Stage-2 items per CTA
 constexpr int kMaxChunk = 256;            // channels per CTA chunk
 constexpr int kMaxBlocks = kMaxGrid;
-constexpr int kBarriers = 2;              // grid-barrier arrivals per CTA per call
 constexpr int kRing = 16;                 // proxy rows in flight per thread (cp.async ring)
 static_assert(kRing >= 8, "the running-total table reuses the ring (16 x 8 bytes per thread)");
 static_assert((kRing & (kRing - 1)) == 0, "ring depth must be a power of two");
@@ -531,12 +530,13 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
     }
 
     // ---------------------------------------------------- pass B: y += h W_down^T
-    // Items [0, m) are the chunk's speculative items.  Until a warp sees the
-    // item list final it adds them tentatively (nearly all are in the mask);
-    // afterwards it skips the items the mask dropped, and at the end it takes
-    // out again the dropped items it had already added (their W_down^T rows
-    // read once more from global memory).  Each warp decides for itself, and
-    // only for its own slices of y.
+    // Items [0, m) are known when the roles start.  Both callers pass the
+    // whole list (the decode step resolves the exact mask first; the dense
+    // pass takes every channel), so every item is confirmed.  Were m shorter,
+    // a warp would add the first m tentatively until it sees the list final,
+    // then skip the items dropped from it and take out again those it had
+    // already added (their W_down^T rows read once more from global memory),
+    // each warp for its own slices of y.
     const int t = threadIdx.x - kPassBWarp0 * 32;
     float yp[CPT][8];
 #pragma unroll

@@ -212,14 +212,14 @@ PROX_API int prox_layer_blocks(const prox_layer* layer);
  * stamps[b * PROX_PHASE_STAMPS + i] (uint64, device, prox_layer_blocks()
  * rows, zeroed first; a phase the kernel does not have stays 0):
  *   0 start; 1 input selection done; 2 proxy partials written;
- *   3 past the first grid barrier; 4 scores, histogram and local ranks
- *   published; 5 exact channel mask known (this CTA's item list final,
- *   Stage 2 starts); 6 first gate|up row landed; 7 gate|up dot products
- *   done; 8 W_down^T accumulation done; 9 end; 10 input-magnitude
+ *   3 past the first grid barrier; 4 scores, histogram counts and score
+ *   keys published; 5 exact channel mask known (this CTA's item list
+ *   final, Stage 2 starts); 6 first gate|up row landed; 7 gate|up dot
+ *   products done; 8 W_down^T accumulation done; 9 end; 10 input-magnitude
  *   histogram built; 11 first proxy row landed (thread 0); 12 proxy loop
- *   done (thread 0); 13 scores formed (before the local ranking); 14 past
- *   the second grid barrier, score histogram staged; 15 exact k-th score
- *   found.
+ *   done (thread 0); 13 scores formed; 14 past the second grid barrier,
+ *   first 11-bit digit of the k-th score key known; 15 exact k-th score
+ *   key found (digits 2 and 3).
  * The dense step stamps 0 and 6..9 only.  Same results as prox_ffn /
  * prox_dense_ffn.
  */
