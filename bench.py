@@ -643,6 +643,42 @@ def run_gpu(args):
             "tokens_per_s": round(Bt * 1e6 / us, 1),
             "note": "one persistent launch per token; the weights cycle through the layer copies"}
 
+        # ------------------------------------------------ batches over the union of the masks
+        union = {}
+        for Bt in (8, 16):
+            xu = torch.stack([wl.xs[i % N_X] for i in range(Bt)])
+            yu = torch.empty(Bt, d, dtype=torch.float32, device=dev)
+            G = prox.prox_batch_union_group(wl.layers[0])
+            nu = 0  # channels in the union, summed over the passes
+            for g0 in range(0, Bt, G):
+                r = prox.prox_ffn_batch_union_debug(wl.layers[0], xu[g0:g0 + G], rho)
+                nu += int((r["member"] != 0).sum())
+            torch.cuda.synchronize()
+
+            def union_step(i, xu=xu, yu=yu):
+                prox.prox_ffn_batch_union(wl.slot(i)[0], xu, rho, y=yu)
+
+            n = CHUNK // 4
+            gs = graphs_for(union_step, n, stream)
+            with torch.cuda.stream(stream):
+                gs[0].replay()
+            torch.cuda.synchronize()
+            m, _, _ = timed_replays(gs, stream)
+            us = m * 1e3 / n
+            G_ = d // 128
+            abu = Bt * (F * kx + 4 * F * G_) + nu * 6 * d + Bt * 6 * d
+            union[str(Bt)] = {
+                "us_per_call": round(us, 3), "us_per_token": round(us / Bt, 3),
+                "tokens_per_s": round(Bt * 1e6 / us, 1), "tokens_per_pass": G,
+                "union_channels_per_pass": round(nu / ((Bt + G - 1) // G), 1),
+                "alg_bytes": abu, "gbs": round(abu / (us * 1e-6) / 1e9, 1),
+                "frac_of_peak": round(abu / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+        union["note"] = ("prox_ffn_batch_union: each token's exact mask (one mask-only step per "
+                         "token), then one gate|up pass and one W_down^T pass over the union of "
+                         "the pass's masks; distinct hidden states, weights cycling through the "
+                         "layer copies")
+        extras["batch_union_masks"] = union
+
         # ------------------------------------------------ 32-layer stack
         if not args.no_stack:
             extras["stack32"] = stack_extra(prox, synth, dev, stream, rho, hbm_peak)

@@ -7,6 +7,8 @@
 
 #include <new>
 
+#include <algorithm>
+
 #include "prox_internal.cuh"
 
 namespace prox {
@@ -169,6 +171,7 @@ prox_status prepare(int d_model, int d_ff, const void* w_gate, const void* w_up,
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = prox::fused_configure();
+    if (e == cudaSuccess) e = prox::union_configure();
     if (e == cudaSuccess)
         e = cudaMemsetAsync(workspace, 0, prox::workspace_bytes(d_model, d_ff), s);
     if (e == cudaSuccess)
@@ -412,6 +415,89 @@ prox_status prox_ffn_batch(const prox_layer* layer, const void* x, int batch,
         if (st != PROX_OK) return st;
     }
     return PROX_OK;
+}
+
+int prox_batch_union_group(const prox_layer* layer) {
+    if (!layer || layer->q8) return 0;
+    return prox::union_geometry(layer->d_model, layer->d_ff, layer->num_blocks).G;
+}
+
+namespace {
+
+// A batch over the union of its tokens' masks, in passes of up to G tokens:
+// clear the token bits, each token's mask-only step (its exact mask, its
+// bit ORed into member[c]; y[t] zeroed), then Stage 2 over the union.
+// member_out (debug, batch <= G): the token bits after the pass.
+prox_status run_union(const prox_layer* L, const void* x, int batch, float keep_fraction,
+                      float* y, uint32_t* member_out, cudaStream_t stream) {
+    prox_status st = check_call(L, x, y);
+    if (st != PROX_OK) return st;
+    if (batch < 1 || !frac_ok(keep_fraction)) return PROX_ERR_INVALID_ARG;
+    if (L->q8) return PROX_ERR_UNSUPPORTED_SHAPE;  // bf16 Stage-2 rows only
+    const int G = prox_batch_union_group(L);
+    if (G < 1) return PROX_ERR_UNSUPPORTED_SHAPE;
+    if (member_out && (batch > G || !aligned16(member_out))) return PROX_ERR_INVALID_ARG;
+    const size_t d = (size_t)L->d_model;
+    if (overlap(x, 2 * d * batch, y, 4 * d * batch)) return PROX_ERR_INVALID_ARG;
+    const uint16_t* xs = static_cast<const uint16_t*>(x);
+    uint32_t* member = reinterpret_cast<uint32_t*>(L->ws.hch);  // debug h area, unused here
+    float* H = reinterpret_cast<float*>(L->ws.part);            // proxy partials, free after Stage 1
+    for (int g0 = 0; g0 < batch; g0 += G) {
+        const int gb = std::min(G, batch - g0);
+        cudaError_t e = cudaMemsetAsync(member, 0, (size_t)L->d_ff * 4, stream);
+        if (e != cudaSuccess) return cuda_status(e);
+        for (int t = 0; t < gb; ++t) {
+            prox::FusedLaunch f;
+            f.codes = L->codes;
+            f.scales = L->scales;
+            f.gateup = L->gateup;
+            f.down_t = L->down_t;
+            f.q8 = 0;
+            f.d = L->d_model;
+            f.F = L->d_ff;
+            f.x = xs + (g0 + t) * d;
+            f.y = y + (g0 + t) * d;
+            f.kx = prox_keep_count(L->d_model, 0.5f);
+            f.k = prox_keep_count(L->d_ff, keep_fraction);
+            f.member = member;
+            f.token = t;
+            f.ws = &L->ws;
+            f.kept_out = nullptr;
+            f.scores_out = nullptr;
+            f.idx_out = nullptr;
+            f.h_out = nullptr;
+            f.num_blocks = L->num_blocks;
+            f.limit_ns = prox::kWaitLimitNs;
+            f.inject = 0;
+            f.ts = nullptr;
+            e = prox::launch_fused(f, stream);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        e = prox::launch_union(L->gateup, L->down_t, xs + g0 * d, member, H, y + g0 * d,
+                               L->d_model, L->d_ff, gb, L->num_blocks, L->ws.status,
+                               prox::kWaitLimitNs, stream);
+        if (e == cudaSuccess && member_out)
+            e = cudaMemcpyAsync(member_out, member, (size_t)L->d_ff * 4, cudaMemcpyDeviceToDevice,
+                                stream);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return PROX_OK;
+}
+
+}  // namespace
+
+prox_status prox_ffn_batch_union(const prox_layer* layer, const void* x, int batch,
+                                 float keep_fraction, float* y, prox_stream_t stream) {
+    return run_union(layer, x, batch, keep_fraction, y, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+prox_status prox_ffn_batch_union_debug(const prox_layer* layer, const void* x, int batch,
+                                       float keep_fraction, float* y, uint32_t* member_out,
+                                       prox_stream_t stream) {
+    if (!member_out) return PROX_ERR_INVALID_ARG;
+    return run_union(layer, x, batch, keep_fraction, y, member_out,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 prox_status prox_ffn_blocks(const prox_layer* layer, const void* x, int block_width,

@@ -119,6 +119,8 @@ struct FusedParams {
     long long limit_ns;
     int inject;          // 1: the last CTA withholds its grid-barrier arrival (test hook)
     uint64_t* ts;        // [gridDim][kPhaseStamps] %globaltimer stamps, or null
+    uint32_t* member;    // mask only: per channel the bits of the tokens whose mask holds it
+    int token;
 };
 
 struct Ctl {
@@ -821,7 +823,7 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
     if (sure) {
         int rank = __popc(sb & ((1u << (tid & 31)) - 1u));
         for (int w = 0; w < (tid >> 5); ++w) rank += (int)ctl.warp_tot[w];  // nch <= 256: <= 7 warps
-        if (rank < kPrefetchItems) {
+        if (rank < kPrefetchItems && !p.member) {  // mask only: the rows are read later
             const int c = cb0 + tid;
             const size_t gb = gu_row_bytes(p.d, p.q8), db = down_row_bytes(p.d, p.q8);
             prefetch_l2(p.gateup + (size_t)c * gb, (uint32_t)gb);
@@ -1325,6 +1327,11 @@ __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8
     // ------------------------------------------------ P3: selection, then stage 2
     if (!select_items(p, ctl, area, nb, b, cb0, nch)) return false;
     const int m = ctl.n_items;  // every item is known before Stage 2 starts
+    if (p.member) {  // a batch's union mask: record this token's share, no Stage 2
+        for (int i = tid; i < m; i += kNT) atomicOr(p.member + ctl.item[i], 1u << p.token);
+        stamp(p.ts, 5);
+        return true;
+    }
     if (tid == 0) {
         mbar_arrive(&ctl.sel_bar);
         stamp_here(p.ts, 5);
@@ -1618,6 +1625,8 @@ FusedParams make_params(const FusedLaunch& L) {
     p.limit_ns = L.limit_ns;
     p.inject = L.inject;
     p.ts = L.ts;
+    p.member = L.member;
+    p.token = L.token;
     return p;
 }
 

@@ -205,6 +205,10 @@ struct FusedLaunch {
     const float* y_prev = nullptr;
     uint16_t* x_out = nullptr;
     float eps = 0.0f;
+    // mask only (batch with a union mask): each CTA ORs bit `token` into
+    // member[c] for its share of the mask and skips Stage 2 (y is only zeroed)
+    uint32_t* member = nullptr;
+    int token = 0;
     const Workspace* ws;
     int32_t* kept_out;   // debug outputs, may be null
     float* scores_out;
@@ -243,6 +247,22 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream);
 // The stack launch: layers[l] of the same shape (L.q8 for all), first
 // layer on x0, layer l > 0 on x_l = bf16(RMSNorm(x_{l-1} + y_{l-1}) / eps).
 cudaError_t launch_stack(const FusedLaunch& L, const StackLayers& sl, cudaStream_t stream);
+
+// Stage 2 of a batch over the union of its tokens' masks (prox_union.cu):
+// G tokens per pass at most (their x staged in shared memory), S gate|up
+// ring stages; the W_down^T pass tiles 512-output slices x channel ranges.
+constexpr int kUnionMaxG = 8;
+struct UnionGeom {
+    int G, S, gu_blocks, nslice, nrange, max_items;
+    size_t gu_smem, down_smem;
+};
+UnionGeom union_geometry(int d, int F, int num_blocks);
+cudaError_t union_configure();
+// H: [G][padded_ff(F)] fp32 scratch; y: [G][d] fp32, zeroed before (each
+// token's mask-only step zeroes its row); member: [F] token bits
+cudaError_t launch_union(const void* gateup, const void* down_t, const uint16_t* x,
+                         const uint32_t* member, float* H, float* y, int d, int F, int G,
+                         int num_blocks, int* status, long long limit_ns, cudaStream_t stream);
 cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const uint16_t* x, int d,
                          int F, float* y, int* status, int num_blocks, long long limit_ns,
                          uint64_t* ts, cudaStream_t stream);

@@ -70,6 +70,9 @@ def _load():
             "prox_ffn_debug": (i32, [vp, vp, f32, f32, vp, vp, vp, vp, vp, vp]),
             "prox_ffn_blocks": (i32, [vp, vp, i32, f32, vp, vp]),
             "prox_ffn_batch": (i32, [vp, vp, i32, f32, vp, vp]),
+            "prox_ffn_batch_union": (i32, [vp, vp, i32, f32, vp, vp]),
+            "prox_ffn_batch_union_debug": (i32, [vp, vp, i32, f32, vp, vp, vp]),
+            "prox_batch_union_group": (i32, [vp]),
             "prox_ffn_blocks_debug": (i32, [vp, vp, i32, f32, vp, vp, vp, vp, vp]),
             "prox_ffn_contrib": (i32, [vp, vp, f32, vp, vp]),
             "prox_stack_ffn": (i32, [ctypes.POINTER(vp), i32, vp, f32, f32, vp, vp, vp]),
@@ -365,6 +368,49 @@ def prox_ffn_batch(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, y=No
         _check(_load().prox_ffn_batch(layer.handle, _ptr(x), int(B), float(keep_fraction),
                                       _ptr(y), _stream(stream)), "prox_ffn_batch")
     return y
+
+
+def _batch_x_y(layer, x, y):
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError("x must be a [batch, d_model] tensor")
+    B = x.shape[0]
+    _need(x, torch.bfloat16, (B, layer.d_model), "x")
+    if y is None:
+        y = torch.empty(B, layer.d_model, dtype=torch.float32, device=x.device)
+    _need(y, torch.float32, (B, layer.d_model), "y")
+    return B, y
+
+
+def prox_batch_union_group(layer: ProxLayer) -> int:
+    """Tokens per pass of prox_ffn_batch_union on this layer (0: unsupported)."""
+    return int(_load().prox_batch_union_group(layer.handle))
+
+
+def prox_ffn_batch_union(layer: ProxLayer, x: torch.Tensor, keep_fraction: float, y=None,
+                         stream=None):
+    """Per-token masks, Stage 2 over their union: x bf16 [B, d_model] -> y fp32
+    [B, d_model]; each row in the union is read once for the whole pass."""
+    B, y = _batch_x_y(layer, x, y)
+    with torch.cuda.device(layer.device):
+        _check(_load().prox_ffn_batch_union(layer.handle, _ptr(x), int(B), float(keep_fraction),
+                                            _ptr(y), _stream(stream)), "prox_ffn_batch_union")
+    return y
+
+
+def prox_ffn_batch_union_debug(layer: ProxLayer, x: torch.Tensor, keep_fraction: float,
+                               stream=None) -> dict:
+    """prox_ffn_batch_union plus the per-channel token bits (batch <= one pass):
+    {"y": [B, d_model] fp32, "member": [d_ff] int64 bit words, "masks": list
+    of each token's selected channels (ascending int64 tensors)}."""
+    B, y = _batch_x_y(layer, x, None)
+    member = torch.zeros(layer.d_ff + 4, dtype=torch.int32, device=x.device)
+    with torch.cuda.device(layer.device):
+        _check(_load().prox_ffn_batch_union_debug(layer.handle, _ptr(x), int(B),
+                                                  float(keep_fraction), _ptr(y), _ptr(member),
+                                                  _stream(stream)), "prox_ffn_batch_union_debug")
+    m = member[: layer.d_ff].to(torch.int64) & 0xFFFFFFFF
+    masks = [torch.nonzero((m >> t) & 1).flatten() for t in range(B)]
+    return {"y": y, "member": m, "masks": masks}
 
 
 def prox_ffn_blocks(layer: ProxLayer, x: torch.Tensor, block_width: int, keep_fraction: float,

@@ -239,6 +239,36 @@ PROX_API prox_status prox_ffn_batch(const prox_layer* layer, const void* x, int 
                            float keep_fraction, float* y, prox_stream_t stream);
 
 /*
+ * Batch > 1 decode over the union of the tokens' masks.  Every token keeps
+ * its own exact mask and output, as in prox_ffn_batch ("Prox", Abstract: one
+ * channel mask per token from its proxy ranking; y[t] = the SwiGLU block of
+ * "PrunePath", Sec. 2.1 Eq. (1), over token t's selected channels only), but
+ * Stage 2 reads each row in the union of the masks once for all the tokens
+ * whose mask holds it.  The batch runs in passes of prox_batch_union_group()
+ * tokens: one mask-only step per token (Stage 1, its bit ORed into a
+ * per-channel word), then one gate|up pass and one W_down^T pass over the
+ * union.  x bf16 [batch][d_model], y fp32 [batch][d_model] (device, 16-byte
+ * aligned, not overlapping); keep fraction as in prox_ffn.  The same masks
+ * as prox_ffn per token; y[t] equals prox_ffn's up to the order of the fp32
+ * additions.  Layers prepared with int8 Stage-2 rows (prox_prepare_q8) are
+ * not supported (PROX_ERR_UNSUPPORTED_SHAPE).  Uses the layer's workspace.
+ */
+PROX_API prox_status prox_ffn_batch_union(const prox_layer* layer, const void* x, int batch,
+                                 float keep_fraction, float* y, prox_stream_t stream);
+
+/* Tokens per pass of prox_ffn_batch_union on this layer (their x fit in a
+ * CTA's shared memory next to the gate|up ring): 8 up to d_model 4096,
+ * fewer above; 0 for a null or int8 layer. */
+PROX_API int prox_batch_union_group(const prox_layer* layer);
+
+/* prox_ffn_batch_union plus, for batch <= prox_batch_union_group(),
+ * member_out (uint32 [d_ff], device): bit t of word c is set when token t's
+ * mask holds channel c (parity checks). */
+PROX_API prox_status prox_ffn_batch_union_debug(const prox_layer* layer, const void* x,
+                                       int batch, float keep_fraction, float* y,
+                                       uint32_t* member_out, prox_stream_t stream);
+
+/*
  * The decode step with a block-granular mask ("PrunePath", Sec. 2.2 Eq. (2):
  * after a channel permutation, d_ff splits into E = d_ff / block_width
  * contiguous experts; Sec. 3.1 runs a subset of them).  The weights given to
