@@ -441,7 +441,9 @@ prox_status run_union(const prox_layer* L, const void* x, int batch, float keep_
     if (overlap(x, 2 * d * batch, y, 4 * d * batch)) return PROX_ERR_INVALID_ARG;
     const uint16_t* xs = static_cast<const uint16_t*>(x);
     uint32_t* member = reinterpret_cast<uint32_t*>(L->ws.hch);  // debug h area, unused here
-    float* H = reinterpret_cast<float*>(L->ws.part);            // proxy partials, free after Stage 1
+    // the proxy partials ([16][Fp] float2) are free after Stage 1: they hold
+    // the union pass's partial g and u sums ([4][G][Fp] float, G <= 8)
+    float* GU = reinterpret_cast<float*>(L->ws.part);
     for (int g0 = 0; g0 < batch; g0 += G) {
         const int gb = std::min(G, batch - g0);
         cudaError_t e = cudaMemsetAsync(member, 0, (size_t)L->d_ff * 4, stream);
@@ -473,7 +475,7 @@ prox_status run_union(const prox_layer* L, const void* x, int batch, float keep_
             e = prox::launch_fused(f, stream);
             if (e != cudaSuccess) return cuda_status(e);
         }
-        e = prox::launch_union(L->gateup, L->down_t, xs + g0 * d, member, H, y + g0 * d,
+        e = prox::launch_union(L->gateup, L->down_t, xs + g0 * d, member, GU, y + g0 * d,
                                L->d_model, L->d_ff, gb, L->num_blocks, L->ws.status,
                                prox::kWaitLimitNs, stream);
         if (e == cudaSuccess && member_out)

@@ -258,10 +258,11 @@ struct UnionGeom {
 };
 UnionGeom union_geometry(int d, int F, int num_blocks);
 cudaError_t union_configure();
-// H: [G][padded_ff(F)] fp32 scratch; y: [G][d] fp32, zeroed before (each
-// token's mask-only step zeroes its row); member: [F] token bits
+// GU: [4][G][padded_ff(F)] fp32 scratch (two partial sums each of g and
+// u); y: [G][d] fp32, zeroed before (each token's mask-only step zeroes its
+// row); member: [F] token bits
 cudaError_t launch_union(const void* gateup, const void* down_t, const uint16_t* x,
-                         const uint32_t* member, float* H, float* y, int d, int F, int G,
+                         const uint32_t* member, float* GU, float* y, int d, int F, int G,
                          int num_blocks, int* status, long long limit_ns, cudaStream_t stream);
 cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const uint16_t* x, int d,
                          int F, float* y, int* status, int num_blocks, long long limit_ns,
