@@ -673,10 +673,10 @@ def run_gpu(args):
                 "union_channels_per_pass": round(nu / ((Bt + G - 1) // G), 1),
                 "alg_bytes": abu, "gbs": round(abu / (us * 1e-6) / 1e9, 1),
                 "frac_of_peak": round(abu / (us * 1e-6) / 1e9 / hbm_peak, 4)}
-        union["note"] = ("prox_ffn_batch_union: each token's exact mask (one mask-only step per "
-                         "token), then one gate|up pass and one W_down^T pass over the union of "
-                         "the pass's masks; distinct hidden states, weights cycling through the "
-                         "layer copies")
+        union["note"] = ("prox_ffn_batch_union: every token's exact mask (Stage 1 of the pass's "
+                         "tokens in one launch, a group of CTAs per token), then one gate|up pass "
+                         "and one W_down^T pass over the union of the pass's masks; distinct hidden "
+                         "states, weights cycling through the layer copies")
         extras["batch_union_masks"] = union
 
         # ------------------------------------------------ 32-layer stack

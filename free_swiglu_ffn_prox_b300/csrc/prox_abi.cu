@@ -444,11 +444,21 @@ prox_status run_union(const prox_layer* L, const void* x, int batch, float keep_
     // the proxy partials ([16][Fp] float2) are free after Stage 1: they hold
     // the union pass's partial g and u sums ([4][G][Fp] float, G <= 8)
     float* GU = reinterpret_cast<float*>(L->ws.part);
+    const int k = prox_keep_count(L->d_ff, keep_fraction);
+    const size_t part_bytes = (size_t)prox::kMaxSlices * prox::padded_ff(L->d_ff) * 8;
+    // the grouped Stage-1 launch's barrier words, in the control block
+    unsigned* gbar = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(L->ws.status) + 1024);
     for (int g0 = 0; g0 < batch; g0 += G) {
         const int gb = std::min(G, batch - g0);
         cudaError_t e = cudaMemsetAsync(member, 0, (size_t)L->d_ff * 4, stream);
         if (e != cudaSuccess) return cuda_status(e);
-        for (int t = 0; t < gb; ++t) {
+        // Stage 1 of the pass's tokens: one launch with a group of CTAs per
+        // token when their scratch fits in the proxy-partial area (which the
+        // union pass reuses afterwards), else one mask-only step per token
+        const prox::MaskGroupGeom mgeo =
+            prox::mask_group_geometry(L->d_model, L->d_ff, k, gb, L->num_blocks);
+        const bool grouped = mgeo.gsize > 0 && (size_t)gb * mgeo.stride <= part_bytes;
+        for (int t = 0; t < (grouped ? 1 : gb); ++t) {
             prox::FusedLaunch f;
             f.codes = L->codes;
             f.scales = L->scales;
@@ -460,7 +470,7 @@ prox_status run_union(const prox_layer* L, const void* x, int batch, float keep_
             f.x = xs + (g0 + t) * d;
             f.y = y + (g0 + t) * d;
             f.kx = prox_keep_count(L->d_model, 0.5f);
-            f.k = prox_keep_count(L->d_ff, keep_fraction);
+            f.k = k;
             f.member = member;
             f.token = t;
             f.ws = &L->ws;
@@ -472,7 +482,13 @@ prox_status run_union(const prox_layer* L, const void* x, int batch, float keep_
             f.limit_ns = prox::kWaitLimitNs;
             f.inject = 0;
             f.ts = nullptr;
-            e = prox::launch_fused(f, stream);
+            if (grouped) {
+                e = cudaMemsetAsync(gbar, 0, (size_t)gb * 4, stream);
+                if (e == cudaSuccess)
+                    e = prox::launch_masks(f, gb, reinterpret_cast<uint8_t*>(L->ws.part), gbar, stream);
+            } else {
+                e = prox::launch_fused(f, stream);
+            }
             if (e != cudaSuccess) return cuda_status(e);
         }
         e = prox::launch_union(L->gateup, L->down_t, xs + g0 * d, member, GU, y + g0 * d,

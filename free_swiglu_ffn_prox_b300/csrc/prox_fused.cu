@@ -121,6 +121,7 @@ struct FusedParams {
     uint64_t* ts;        // [gridDim][kPhaseStamps] %globaltimer stamps, or null
     uint32_t* member;    // mask only: per channel the bits of the tokens whose mask holds it
     int token;
+    int gsize;           // > 0: the grid is split into groups of gsize CTAs, one token each
 };
 
 struct Ctl {
@@ -816,7 +817,7 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
     // own thread, while the rest of the selection runs; the CTA whose share
     // holds them finds them in L2 (shares follow channel order, so mostly
     // this CTA or a neighbour)
-    const bool sure = tid < nch && (__float_as_uint(ctl.lsc[tid]) >> 20) > b1;
+    const bool sure = tid < min(nch, kMaxChunk) && (__float_as_uint(ctl.lsc[tid]) >> 20) > b1;
     const unsigned sb = __ballot_sync(0xffffffffu, sure);
     if ((tid & 31) == 0) ctl.warp_tot[tid >> 5] = __popc(sb);
     if (!landed(&ctl.key_ld)) return false;
@@ -920,7 +921,9 @@ template <int CPT, bool Q8>
 __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8_t* area,
                                            unsigned gen, unsigned bi, bool last) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int nb = gridDim.x, b = blockIdx.x;
+    // the CTAs that share this step: the whole grid, or this CTA's group
+    const int nb = p.gsize > 0 ? p.gsize : (int)gridDim.x;
+    const int b = p.gsize > 0 ? (int)blockIdx.x % p.gsize : (int)blockIdx.x;
     const int d = p.d, F = p.F, Fp = p.Fp;
     stamp(p.ts, 0);
     // a later step of a stacked launch finds the barriers of the step before
@@ -1253,12 +1256,16 @@ __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8
     // ------------------------------------------------ P2: scores + histogram
     const int cb0 = chunk_lo(F, b, nb, chunk_align(p.bw));
     const int cb1 = chunk_lo(F, b + 1, nb, chunk_align(p.bw));
-    const int nch = cb1 - cb0;  // <= kMaxChunk (checked by the host)
-    {
-        const bool act = tid < nch;
+    const int nch = cb1 - cb0;  // <= kMaxChunk, except in a group launch (block masks: always)
+    // a group launch's chunk can be wider than the CTA: pieces of kNT channels
+    // (the per-chunk scores in ctl.lsc cover the first kMaxChunk; they serve
+    // the block mask and the L2 prefetch, neither of which a group launch uses)
+    for (int base = 0; base < nch; base += kNT) {
+        const int ci = base + tid;
+        const bool act = ci < nch;
         uint32_t key = 0;
         if (act) {
-            const int c = cb0 + tid;
+            const int c = cb0 + ci;
             float2 v[kMaxSlices];
 #pragma unroll
             for (int sl = 0; sl < kMaxSlices; ++sl)
@@ -1275,7 +1282,7 @@ __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8
             float sc = fabsf(g / (1.0f + expf(-g)) * u);
             if (p.dnorm) sc *= __ldg(p.dnorm + c);
             if (p.scores_out) p.scores_out[c] = sc;
-            ctl.lsc[tid] = sc;
+            if (ci < kMaxChunk) ctl.lsc[ci] = sc;
             key = __float_as_uint(sc);
         }
         if (p.bw > 0) {
@@ -1305,7 +1312,7 @@ __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8
         }
         // the key, in channel order, for the selection; one histogram
         // reduction per distinct bin in the warp
-        if (act) p.skey[cb0 + tid] = key;
+        if (act) p.skey[cb0 + ci] = key;
         const unsigned am = __ballot_sync(0xffffffffu, act);
         if (act) {
             const unsigned peers = __match_any_sync(am, key >> 20);
@@ -1415,6 +1422,33 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_stack(const FusedParams base, c
         __syncthreads();
         if (!fused_step<CPT, Q8>(ctl.sp, ctl, area, gen, bi, l + 1 == sl.n)) return;
     }
+}
+
+// Stage 1 of several tokens at once (a batch's masks): the grid splits into
+// groups of mg.gsize CTAs, group t runs token t's step in mask-only mode on
+// its own x, y row, histogram, proxy partials, score keys and barrier word
+// (mg.scratch + t mg.stride, mg.gbar[t], the latter zero at launch).
+template <int CPT, bool Q8>
+__global__ void __launch_bounds__(kNT, 1) k_prox_masks(const FusedParams base, const MaskGroups mg) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
+    uint8_t* area = smem_raw + ctl_bytes();
+    const int tk = (int)blockIdx.x / base.gsize;
+    if (threadIdx.x == 0) {
+        ctl.abort = 0;
+        FusedParams q = base;
+        uint8_t* sc = mg.scratch + (size_t)tk * mg.stride;
+        q.x = base.x + (size_t)tk * base.d;
+        q.y = base.y + (size_t)tk * base.d;
+        q.hist = reinterpret_cast<uint32_t*>(sc);
+        q.part = reinterpret_cast<float2*>(sc + mg.part_off);
+        q.skey = reinterpret_cast<uint32_t*>(sc + mg.skey_off);
+        q.bar = mg.gbar + tk;
+        q.token = tk;
+        ctl.sp = q;
+    }
+    __syncthreads();
+    fused_step<CPT, Q8>(ctl.sp, ctl, area, 0u, 0u, false);
 }
 
 // Dense baseline: Stage 2 over every channel, CTA i taking [F i/n, F (i+1)/n)
@@ -1534,6 +1568,10 @@ cudaError_t fused_configure() {
     if (e == cudaSuccess) e = set_smem(k_prox_fused<2, true>);
     if (e == cudaSuccess) e = set_smem(k_prox_fused<4, true>);
     if (e == cudaSuccess) e = set_smem(k_prox_fused<8, true>);
+    if (e == cudaSuccess) e = set_smem(k_prox_masks<1, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_masks<2, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_masks<4, false>);
+    if (e == cudaSuccess) e = set_smem(k_prox_masks<8, false>);
     if (e == cudaSuccess) e = set_smem(k_prox_stack<1, false>);
     if (e == cudaSuccess) e = set_smem(k_prox_stack<2, false>);
     if (e == cudaSuccess) e = set_smem(k_prox_stack<4, false>);
@@ -1627,6 +1665,7 @@ FusedParams make_params(const FusedLaunch& L) {
     p.ts = L.ts;
     p.member = L.member;
     p.token = L.token;
+    p.gsize = 0;
     return p;
 }
 
@@ -1684,6 +1723,54 @@ cudaError_t launch_stack(const FusedLaunch& L, const StackLayers& sl, cudaStream
     if (nchunk <= 2 * kPassB) return launch_stack_t<2>(cfg, p, sl);
     if (nchunk <= 4 * kPassB) return launch_stack_t<4>(cfg, p, sl);
     return launch_stack_t<8>(cfg, p, sl);
+}
+
+MaskGroupGeom mask_group_geometry(int d, int F, int k, int ntok, int num_blocks) {
+    MaskGroupGeom g{};
+    if (ntok < 2) return g;
+    const int gsize = num_blocks / ntok;
+    const int kx = (d + 1) / 2;  // the input keep count of a step (keep fraction 0.5)
+    if (gsize < 4 || (k + gsize - 1) / gsize > kMaxItems) return g;
+    const int Fp = padded_ff(F);
+    const ProxyGeom geo = proxy_geometry(F, kx, gsize);
+    auto a256 = [](size_t v) { return (v + 255) / 256 * 256; };
+    g.gsize = gsize;
+    g.part_off = a256((size_t)kHistWords * 4);
+    g.skey_off = g.part_off + a256((size_t)geo.slices * Fp * 8);
+    g.stride = g.skey_off + a256((size_t)Fp * 4);
+    return g;
+}
+
+cudaError_t launch_masks(const FusedLaunch& L, int ntok, uint8_t* scratch, unsigned* gbar,
+                         cudaStream_t stream) {
+    const MaskGroupGeom g = mask_group_geometry(L.d, L.F, L.k, ntok, L.num_blocks);
+    if (g.gsize == 0 || !L.member || L.q8 || L.bw) return cudaErrorInvalidValue;
+    FusedParams p = make_params(L);
+    const ProxyGeom geo = proxy_geometry(L.F, L.kx, g.gsize);
+    p.tiles = geo.tiles;
+    p.slices = geo.slices;
+    p.tile_w = geo.tile_w;
+    p.gsize = g.gsize;
+    p.debug = 0;
+    p.kept_out = nullptr;
+    p.scores_out = nullptr;
+    p.ts = nullptr;
+    MaskGroups mg;
+    mg.scratch = scratch;
+    mg.stride = g.stride;
+    mg.part_off = g.part_off;
+    mg.skey_off = g.skey_off;
+    mg.gbar = gbar;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = coop_config(ntok * g.gsize, stream, attr);
+    const int nchunk = L.d / 8;
+    const int cpt = nchunk <= kPassB ? 1 : nchunk <= 2 * kPassB ? 2 : nchunk <= 4 * kPassB ? 4 : 8;
+    switch (cpt) {
+        case 1: return cudaLaunchKernelEx(&cfg, k_prox_masks<1, false>, p, mg);
+        case 2: return cudaLaunchKernelEx(&cfg, k_prox_masks<2, false>, p, mg);
+        case 4: return cudaLaunchKernelEx(&cfg, k_prox_masks<4, false>, p, mg);
+        default: return cudaLaunchKernelEx(&cfg, k_prox_masks<8, false>, p, mg);
+    }
 }
 
 cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const uint16_t* x, int d,

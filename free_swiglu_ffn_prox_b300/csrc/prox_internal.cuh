@@ -27,7 +27,8 @@ constexpr size_t kControlBytes = 2048;
 
 // Workspace carve-out (offsets in bytes, each 256-aligned).  The first
 // kControlBytes are the control block: status word, then (at +128) the grid
-// barrier count and the call epoch; a fault clears the whole block.
+// barrier count and the call epoch, and (at +1024) the per-token barrier
+// words of a batch's grouped Stage-1 launch; a fault clears the whole block.
 struct Workspace {
     int* status;        // [0] device status word (0 = ok)
     unsigned* bar;      // grid barrier count; bar[1] call epoch
@@ -247,6 +248,25 @@ cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream);
 // The stack launch: layers[l] of the same shape (L.q8 for all), first
 // layer on x0, layer l > 0 on x_l = bf16(RMSNorm(x_{l-1} + y_{l-1}) / eps).
 cudaError_t launch_stack(const FusedLaunch& L, const StackLayers& sl, cudaStream_t stream);
+
+// Stage 1 of several tokens in one launch (mask-only steps in groups of
+// CTAs): each token's histogram, proxy partials and score keys at
+// scratch + t stride (+ part_off, + skey_off); gbar[t] its barrier word
+// (zero at launch).  gsize = 0: not possible for this shape and token count.
+struct MaskGroupGeom {
+    int gsize;
+    size_t stride, part_off, skey_off;
+};
+struct MaskGroups {
+    uint8_t* scratch;
+    size_t stride, part_off, skey_off;
+    unsigned* gbar;
+};
+MaskGroupGeom mask_group_geometry(int d, int F, int k, int ntok, int num_blocks);
+// L: a mask-only step (member set, bf16 rows, channel mask); L.x / L.y the
+// first token's rows, the others follow at d-element strides
+cudaError_t launch_masks(const FusedLaunch& L, int ntok, uint8_t* scratch, unsigned* gbar,
+                         cudaStream_t stream);
 
 // Stage 2 of a batch over the union of its tokens' masks (prox_union.cu):
 // G tokens per pass at most (their x staged in shared memory), S gate|up

@@ -245,9 +245,11 @@ PROX_API prox_status prox_ffn_batch(const prox_layer* layer, const void* x, int 
  * "PrunePath", Sec. 2.1 Eq. (1), over token t's selected channels only), but
  * Stage 2 reads each row in the union of the masks once for all the tokens
  * whose mask holds it.  The batch runs in passes of prox_batch_union_group()
- * tokens: one mask-only step per token (Stage 1, its bit ORed into a
+ * tokens: a mask-only step per token (Stage 1, its bit ORed into a
  * per-channel word), then one gate|up pass and one W_down^T pass over the
- * union.  x bf16 [batch][d_model], y fp32 [batch][d_model] (device, 16-byte
+ * union.  Where the tokens' Stage-1 scratch fits in the layer's workspace
+ * (the Llama shapes), the pass's mask-only steps run as one launch with a
+ * group of CTAs per token.  x bf16 [batch][d_model], y fp32 [batch][d_model] (device, 16-byte
  * aligned, not overlapping); keep fraction as in prox_ffn.  The same masks
  * as prox_ffn per token; y[t] equals prox_ffn's up to the order of the fp32
  * additions.  Layers prepared with int8 Stage-2 rows (prox_prepare_q8) are

@@ -161,3 +161,21 @@ def test_union_batch_argument_errors(prox):
     assert lib.prox_ffn_batch_union(Lq.handle, X.data_ptr(), 4, 0.3, y.data_ptr(), None) == \
         prox.PROX_ERR_UNSUPPORTED_SHAPE
     assert prox.prox_get_status(L) == 0
+
+
+def test_union_batch_grouped_stage1_llama2_7b(prox):
+    """Five tokens of a Llama-2-7B layer: Stage 1 of all five runs in one
+    launch (a group of CTAs per token, chunks wider than a CTA's threads);
+    each token's mask and y as in its own step and against the oracle."""
+    shape = synth.LLAMA2_7B
+    wg, wu, wd = synth.layer(shape, seed=3, device="cuda")
+    L = prox.prox_prepare(wg, wu, wd)
+    torch.cuda.synchronize()
+    w = (host_bits(wg), host_bits(wu), host_bits(wd))
+    del wg, wu, wd
+    px = oracle.Proxy.__new__(oracle.Proxy)
+    px.q_gate, px.s_gate = oracle.quantize(w[0])
+    px.q_up, px.s_up = oracle.quantize(w[1])
+    X = torch.stack([synth.hidden(shape, seed=40 + t) for t in range(5)])
+    for rho in (0.3, 0.1):
+        _check_batch(prox, L, w, X, rho, px=px)
