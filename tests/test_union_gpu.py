@@ -179,3 +179,30 @@ def test_union_batch_grouped_stage1_llama2_7b(prox):
     X = torch.stack([synth.hidden(shape, seed=40 + t) for t in range(5)])
     for rho in (0.3, 0.1):
         _check_batch(prox, L, w, X, rho, px=px)
+
+
+def test_union_batch_with_all_tied_tokens(prox):
+    """Zero tokens among ordinary ones, on the Llama-3-8B layer (grouped
+    Stage 1): a zero token's scores all tie, so its mask is the first k
+    channels and its y is 0; the other tokens are unaffected."""
+    shape = synth.LLAMA3_8B
+    wg, wu, wd = synth.layer(shape, seed=0, device="cuda")
+    L = prox.prox_prepare(wg, wu, wd)
+    torch.cuda.synchronize()
+    del wg, wu, wd
+    X = torch.stack([synth.hidden(shape, seed=60 + t) for t in range(6)])
+    X[1].zero_()
+    X[4].zero_()
+    r = prox.prox_ffn_batch_union_debug(L, X.cuda(), 0.3)
+    torch.cuda.synchronize()
+    assert prox.prox_get_status(L) == 0
+    k = oracle.keep_count(shape.d_ff, 0.3)
+    for t in (1, 4):
+        assert np.array_equal(r["masks"][t].cpu().numpy(), np.arange(k))
+        assert torch.count_nonzero(r["y"][t]) == 0
+    for t in (0, 2, 3, 5):
+        one = prox.prox_ffn_debug(L, X[t].cuda(), 0.3)
+        torch.cuda.synchronize()
+        assert np.array_equal(one["idx"].cpu().numpy(), r["masks"][t].cpu().numpy()), t
+        scale = float(one["y"].abs().max())
+        assert torch.allclose(r["y"][t], one["y"], rtol=0, atol=1e-5 * scale), t
