@@ -917,13 +917,15 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
 // step of a launch publishes gen + bi + 2 for the next launch (every CTA
 // has read gen by then).  Returns false when the CTA must leave (a wait ran
 // out or a check failed; the status word says which).
-template <int CPT, bool Q8>
+// GROUPED: the grid is split into groups of p.gsize CTAs (k_prox_masks);
+// a group's CTA chunks can then be wider than the CTA's threads.
+template <int CPT, bool Q8, bool GROUPED = false>
 __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8_t* area,
                                            unsigned gen, unsigned bi, bool last) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     // the CTAs that share this step: the whole grid, or this CTA's group
-    const int nb = p.gsize > 0 ? p.gsize : (int)gridDim.x;
-    const int b = p.gsize > 0 ? (int)blockIdx.x % p.gsize : (int)blockIdx.x;
+    const int nb = GROUPED ? p.gsize : (int)gridDim.x;
+    const int b = GROUPED ? (int)blockIdx.x % p.gsize : (int)blockIdx.x;
     const int d = p.d, F = p.F, Fp = p.Fp;
     stamp(p.ts, 0);
     // a later step of a stacked launch finds the barriers of the step before
@@ -1260,8 +1262,9 @@ __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8
     // a group launch's chunk can be wider than the CTA: pieces of kNT channels
     // (the per-chunk scores in ctl.lsc cover the first kMaxChunk; they serve
     // the block mask and the L2 prefetch, neither of which a group launch uses)
-    for (int base = 0; base < nch; base += kNT) {
-        const int ci = base + tid;
+    const int npieces = GROUPED ? (nch + kNT - 1) / kNT : 1;
+    for (int piece = 0; piece < npieces; ++piece) {
+        const int ci = piece * kNT + tid;
         const bool act = ci < nch;
         uint32_t key = 0;
         if (act) {
@@ -1448,7 +1451,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_masks(const FusedParams base, c
         ctl.sp = q;
     }
     __syncthreads();
-    fused_step<CPT, Q8>(ctl.sp, ctl, area, 0u, 0u, false);
+    fused_step<CPT, Q8, true>(ctl.sp, ctl, area, 0u, 0u, false);
 }
 
 // Dense baseline: Stage 2 over every channel, CTA i taking [F i/n, F (i+1)/n)
