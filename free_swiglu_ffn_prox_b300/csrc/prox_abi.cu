@@ -452,13 +452,19 @@ prox_status run_union(const prox_layer* L, const void* x, int batch, float keep_
         const int gb = std::min(G, batch - g0);
         cudaError_t e = cudaMemsetAsync(member, 0, (size_t)L->d_ff * 4, stream);
         if (e != cudaSuccess) return cuda_status(e);
-        // Stage 1 of the pass's tokens: one launch with a group of CTAs per
-        // token when their scratch fits in the proxy-partial area (which the
-        // union pass reuses afterwards), else one mask-only step per token
-        const prox::MaskGroupGeom mgeo =
-            prox::mask_group_geometry(L->d_model, L->d_ff, k, gb, L->num_blocks);
-        const bool grouped = mgeo.gsize > 0 && (size_t)gb * mgeo.stride <= part_bytes;
-        for (int t = 0; t < (grouped ? 1 : gb); ++t) {
+        // Stage 1 of the pass's tokens: launches with a group of CTAs per
+        // token, as many tokens per launch as the grid (a CTA per proxy tile
+        // in every group) and the proxy-partial area (which the union pass
+        // reuses afterwards) allow; a token left alone takes a mask-only step
+        auto group_fits = [&](int nt) {
+            const prox::MaskGroupGeom mg =
+                prox::mask_group_geometry(L->d_model, L->d_ff, k, nt, L->num_blocks);
+            return mg.gsize > 0 && (size_t)nt * mg.stride <= part_bytes;
+        };
+        for (int t = 0, nt = 0; t < gb; t += nt) {
+            nt = gb - t;
+            while (nt >= 2 && !group_fits(nt)) --nt;
+            if (nt < 2) nt = 1;
             prox::FusedLaunch f;
             f.codes = L->codes;
             f.scales = L->scales;
@@ -482,10 +488,11 @@ prox_status run_union(const prox_layer* L, const void* x, int batch, float keep_
             f.limit_ns = prox::kWaitLimitNs;
             f.inject = 0;
             f.ts = nullptr;
-            if (grouped) {
-                e = cudaMemsetAsync(gbar, 0, (size_t)gb * 4, stream);
+            if (nt >= 2) {
+                e = cudaMemsetAsync(gbar, 0, (size_t)nt * 4, stream);
                 if (e == cudaSuccess)
-                    e = prox::launch_masks(f, gb, reinterpret_cast<uint8_t*>(L->ws.part), gbar, stream);
+                    e = prox::launch_masks(f, nt, t, reinterpret_cast<uint8_t*>(L->ws.part), gbar,
+                                           stream);
             } else {
                 e = prox::launch_fused(f, stream);
             }

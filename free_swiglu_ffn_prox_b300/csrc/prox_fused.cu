@@ -1447,7 +1447,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_masks(const FusedParams base, c
         q.part = reinterpret_cast<float2*>(sc + mg.part_off);
         q.skey = reinterpret_cast<uint32_t*>(sc + mg.skey_off);
         q.bar = mg.gbar + tk;
-        q.token = tk;
+        q.token = mg.token0 + tk;
         ctl.sp = q;
     }
     __syncthreads();
@@ -1735,6 +1735,8 @@ MaskGroupGeom mask_group_geometry(int d, int F, int k, int ntok, int num_blocks)
     const int kx = (d + 1) / 2;  // the input keep count of a step (keep fraction 0.5)
     if (gsize < 4 || (k + gsize - 1) / gsize > kMaxItems) return g;
     const int Fp = padded_ff(F);
+    // the proxy needs a CTA per tile of up to 1024 channels
+    if ((Fp + 1023) / 1024 > gsize) return g;
     const ProxyGeom geo = proxy_geometry(F, kx, gsize);
     auto a256 = [](size_t v) { return (v + 255) / 256 * 256; };
     g.gsize = gsize;
@@ -1744,8 +1746,8 @@ MaskGroupGeom mask_group_geometry(int d, int F, int k, int ntok, int num_blocks)
     return g;
 }
 
-cudaError_t launch_masks(const FusedLaunch& L, int ntok, uint8_t* scratch, unsigned* gbar,
-                         cudaStream_t stream) {
+cudaError_t launch_masks(const FusedLaunch& L, int ntok, int token0, uint8_t* scratch,
+                         unsigned* gbar, cudaStream_t stream) {
     const MaskGroupGeom g = mask_group_geometry(L.d, L.F, L.k, ntok, L.num_blocks);
     if (g.gsize == 0 || !L.member || L.q8 || L.bw) return cudaErrorInvalidValue;
     FusedParams p = make_params(L);
@@ -1764,6 +1766,7 @@ cudaError_t launch_masks(const FusedLaunch& L, int ntok, uint8_t* scratch, unsig
     mg.part_off = g.part_off;
     mg.skey_off = g.skey_off;
     mg.gbar = gbar;
+    mg.token0 = token0;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = coop_config(ntok * g.gsize, stream, attr);
     const int nchunk = L.d / 8;

@@ -261,12 +261,14 @@ struct MaskGroups {
     uint8_t* scratch;
     size_t stride, part_off, skey_off;
     unsigned* gbar;
+    int token0;  // group t records token bit token0 + t
 };
 MaskGroupGeom mask_group_geometry(int d, int F, int k, int ntok, int num_blocks);
 // L: a mask-only step (member set, bf16 rows, channel mask); L.x / L.y the
-// first token's rows, the others follow at d-element strides
-cudaError_t launch_masks(const FusedLaunch& L, int ntok, uint8_t* scratch, unsigned* gbar,
-                         cudaStream_t stream);
+// first token's rows, the others follow at d-element strides; their bits
+// are token0, token0 + 1, ...
+cudaError_t launch_masks(const FusedLaunch& L, int ntok, int token0, uint8_t* scratch,
+                         unsigned* gbar, cudaStream_t stream);
 
 // Stage 2 of a batch over the union of its tokens' masks (prox_union.cu):
 // G tokens per pass at most (their x staged in shared memory), S gate|up

@@ -206,3 +206,34 @@ def test_union_batch_with_all_tied_tokens(prox):
         assert np.array_equal(one["idx"].cpu().numpy(), r["masks"][t].cpu().numpy()), t
         scale = float(one["y"].abs().max())
         assert torch.allclose(r["y"][t], one["y"], rtol=0, atol=1e-5 * scale), t
+
+
+def test_union_batch_llama3_70b_layer(prox):
+    """Seven tokens of a Llama-3-70B layer: the proxy needs 28 CTAs per token,
+    so Stage 1 runs as a launch of 5 token groups and one of 2.  Every
+    token's mask equals its own step's and y_t matches it and the oracle's
+    sparse FFN on that mask."""
+    shape = synth.LLAMA3_70B
+    wg, wu, wd = synth.layer(shape, seed=1, device="cuda")
+    L = prox.prox_prepare(wg, wu, wd)
+    torch.cuda.synchronize()
+    w = (host_bits(wg), host_bits(wu), host_bits(wd))
+    del wg, wu, wd
+    G = prox.prox_batch_union_group(L)
+    assert G >= 5
+    X = torch.stack([synth.hidden(shape, seed=80 + t) for t in range(G)])
+    r = prox.prox_ffn_batch_union_debug(L, X.cuda(), 0.3)
+    torch.cuda.synchronize()
+    assert prox.prox_get_status(L) == 0
+    k = oracle.keep_count(shape.d_ff, 0.3)
+    for t in range(G):
+        mask = r["masks"][t].cpu().numpy()
+        assert mask.size == k
+        one = prox.prox_ffn_debug(L, X[t].cuda(), 0.3)
+        torch.cuda.synchronize()
+        assert np.array_equal(one["idx"].cpu().numpy(), mask), t
+        scale = float(one["y"].abs().max())
+        assert torch.allclose(r["y"][t], one["y"], rtol=0, atol=1e-5 * scale), t
+        _, y_or = oracle.sparse_ffn(*w, host_bits(X[t]), mask)
+        mx, rl = y_errors(r["y"][t].cpu().numpy(), y_or)
+        assert mx <= ATOL_Y and rl <= RTOL_L2_Y, (t, mx, rl)
