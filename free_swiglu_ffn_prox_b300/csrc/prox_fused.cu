@@ -1541,9 +1541,9 @@ ProxyGeom proxy_geometry(int F, int kx, int num_blocks) {
     // Tiles of W = 256, 512 or 1024 channels (a half-warp, a warp or two
     // warps per proxy row), T tiles x S slices <= blocks; minimise the
     // bytes of the busiest CTA, then prefer fewer slices (less partial
-    // traffic).
+    // traffic).  No fit (more 1024-channel tiles than blocks): tiles = 0.
     const int Fp = padded_ff(F);
-    ProxyGeom best{1, 1, 1024};
+    ProxyGeom best{0, 1, 1024};
     long long best_cost = -1;
     for (int W : {256, 512, 1024}) {
         const int T = (Fp + W - 1) / W;
@@ -1695,6 +1695,7 @@ cudaError_t launch_stack_t(const cudaLaunchConfig_t& cfg, const FusedParams& p, 
 cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream) {
     if (L.num_blocks < 1 || L.num_blocks > kMaxBlocks) return cudaErrorInvalidValue;
     const FusedParams p = make_params(L);
+    if (p.tiles < 1) return cudaErrorInvalidValue;  // a proxy tile per CTA at most
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = coop_config(L.num_blocks, stream, attr);
     const int nchunk = L.d / 8;
@@ -1715,6 +1716,7 @@ cudaError_t launch_stack(const FusedLaunch& L, const StackLayers& sl, cudaStream
     if (L.num_blocks < 1 || L.num_blocks > kMaxBlocks || sl.n < 1 || sl.n > kMaxStack)
         return cudaErrorInvalidValue;
     FusedParams p = make_params(L);
+    if (p.tiles < 1) return cudaErrorInvalidValue;
     p.debug = 0;
     p.kept_out = nullptr;
     p.scores_out = nullptr;
@@ -1752,6 +1754,7 @@ cudaError_t launch_masks(const FusedLaunch& L, int ntok, int token0, uint8_t* sc
     if (g.gsize == 0 || !L.member || L.q8 || L.bw) return cudaErrorInvalidValue;
     FusedParams p = make_params(L);
     const ProxyGeom geo = proxy_geometry(L.F, L.kx, g.gsize);
+    if (geo.tiles < 1) return cudaErrorInvalidValue;
     p.tiles = geo.tiles;
     p.slices = geo.slices;
     p.tile_w = geo.tile_w;
