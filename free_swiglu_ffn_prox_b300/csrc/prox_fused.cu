@@ -1182,9 +1182,11 @@ __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8
             // kRing rows in flight per thread through a cp.async ring in
             // shared memory (slot s of thread t at ring[s * kNT + t]); each
             // thread reads only its own slots, so no block synchronisation.
-            // With tpr a multiple of 16 the row, and kept[q], is uniform
-            // across each half-warp.  One row per iteration keeps the loop
-            // body (and its instruction footprint) small.
+            // With tpr a multiple of 16 (the whole-grid step) the row, and
+            // kept[q], is uniform across each half-warp; other widths (group
+            // launches) only split some warps over two rows.  One row per
+            // iteration keeps the loop body (and its instruction footprint)
+            // small.
             const uint64_t pol = policy_evict_first();
             const uint8_t* colbase = p.codes + c0 + cu * 16;
             uint4* my = ring + tid;
@@ -1540,22 +1542,32 @@ cudaError_t set_smem(K kern) {
 
 }  // namespace
 
-ProxyGeom proxy_geometry(int F, int kx, int num_blocks) {
-    // Tiles of W = 256, 512 or 1024 channels (a half-warp, a warp or two
-    // warps per proxy row), T tiles x S slices <= blocks; minimise the
-    // bytes of the busiest CTA, then prefer fewer slices (less partial
-    // traffic).  No fit (more 1024-channel tiles than blocks): tiles = 0.
+ProxyGeom proxy_geometry(int F, int kx, int num_blocks, bool any_width) {
+    // Tiles of W = 16 tpr channels (tpr threads per proxy row), T tiles x S
+    // slices <= blocks.  No fit (more 1024-channel tiles than blocks):
+    // tiles = 0.
+    //  * a whole-grid step: W = 256, 512 or 1024 (a row is whole half-warps);
+    //    minimise the bytes of the busiest CTA, then prefer fewer slices
+    //    (less partial traffic);
+    //  * any_width (a group of a few CTAs per token): any tpr in 8..64;
+    //    minimise the kept rows per thread of the busiest CTA (its slice's
+    //    rows over its kNT / tpr row-lanes), then fewer slices.  On the
+    //    whole grid this measured slower (a step of the Llama-3-8B layer:
+    //    688-channel tiles, 48.6 against 47.0 us); in groups of 18 CTAs it
+    //    keeps every CTA busy (800-channel tiles: 18 instead of 14 CTAs).
     const int Fp = padded_ff(F);
     ProxyGeom best{0, 1, 1024};
     long long best_cost = -1;
-    for (int W : {256, 512, 1024}) {
+    for (int tpr = any_width ? 8 : 16; tpr <= 64; tpr += any_width ? 1 : tpr) {
+        const int W = 16 * tpr;
         const int T = (Fp + W - 1) / W;
         if (T > num_blocks) continue;
         int S = num_blocks / T;
         if (S > kMaxSlices) S = kMaxSlices;
         if (S > kx) S = kx;
         if (S < 1) S = 1;
-        const long long cost = (long long)min(W, Fp) * ((kx + S - 1) / S);
+        const long long rows = (kx + S - 1) / S;
+        const long long cost = any_width ? (rows + kNT / tpr - 1) / (kNT / tpr) : (long long)min(W, Fp) * rows;
         if (best_cost < 0 || cost < best_cost || (cost == best_cost && S < best.slices)) {
             best_cost = cost;
             best = {T, S, W};
@@ -1647,7 +1659,7 @@ FusedParams make_params(const FusedLaunch& L) {
     p.y_prev = L.y_prev;
     p.x_out = L.x_out;
     p.eps = L.eps;
-    const ProxyGeom geo = proxy_geometry(L.F, L.kx, L.num_blocks);
+    const ProxyGeom geo = proxy_geometry(L.F, L.kx, L.num_blocks, false);
     p.tiles = geo.tiles;
     p.slices = geo.slices;
     p.tile_w = geo.tile_w;
@@ -1742,7 +1754,7 @@ MaskGroupGeom mask_group_geometry(int d, int F, int k, int ntok, int num_blocks)
     const int Fp = padded_ff(F);
     // the proxy needs a CTA per tile of up to 1024 channels
     if ((Fp + 1023) / 1024 > gsize) return g;
-    const ProxyGeom geo = proxy_geometry(F, kx, gsize);
+    const ProxyGeom geo = proxy_geometry(F, kx, gsize, true);
     auto a256 = [](size_t v) { return (v + 255) / 256 * 256; };
     g.gsize = gsize;
     g.part_off = a256((size_t)kHistWords * 4);
@@ -1756,7 +1768,7 @@ cudaError_t launch_masks(const FusedLaunch& L, int ntok, int token0, uint8_t* sc
     const MaskGroupGeom g = mask_group_geometry(L.d, L.F, L.k, ntok, L.num_blocks);
     if (g.gsize == 0 || !L.member || L.q8 || L.bw) return cudaErrorInvalidValue;
     FusedParams p = make_params(L);
-    const ProxyGeom geo = proxy_geometry(L.F, L.kx, g.gsize);
+    const ProxyGeom geo = proxy_geometry(L.F, L.kx, g.gsize, true);
     if (geo.tiles < 1) return cudaErrorInvalidValue;
     p.tiles = geo.tiles;
     p.slices = geo.slices;

@@ -184,7 +184,7 @@ constexpr size_t down_row_bytes(int d, int q8) { return q8 ? (size_t)d : (size_t
 struct ProxyGeom {
     int tiles, slices, tile_w;
 };
-ProxyGeom proxy_geometry(int F, int kx, int num_blocks);
+ProxyGeom proxy_geometry(int F, int kx, int num_blocks, bool any_width = false);
 
 struct FusedLaunch {
     const uint8_t* codes;
