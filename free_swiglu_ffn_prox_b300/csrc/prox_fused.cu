@@ -334,23 +334,23 @@ __device__ __forceinline__ float dot8_bf16(const uint4 a, const uint4 b, float a
 // int8 weights: a word of four two's-complement codes, flipped to offset
 // binary (w ^ 0x80808080), gives code e as the exact float 2^23 + (q + 128)
 // by placing its byte under the exponent of 2^23 (one PRMT); subtracting
-// 2^23 + 128 leaves q exactly.
-__device__ __forceinline__ float q8_value(uint32_t wo, int e) {
-    return __uint_as_float(__byte_perm(wo, 0x4Bu, 0x4550u | (unsigned)e)) - 8388736.0f;
+// 2^23 + 128 leaves q exactly.  Codes e and e + 1 come as a pair, with one
+// packed subtraction.
+__device__ __forceinline__ float2 q8_pair(uint32_t wo, int e) {
+    const float2 b = make_float2(__uint_as_float(__byte_perm(wo, 0x4Bu, 0x4550u | (unsigned)e)),
+                                 __uint_as_float(__byte_perm(wo, 0x4Bu, 0x4550u | (unsigned)(e + 1))));
+    return __fadd2_rn(b, make_float2(-8388736.0f, -8388736.0f));
 }
 
 // acc += sum over 8 elements of q_e * x_e (int8 codes w, bf16 x; every
-// product is exact in fp32)
-__device__ __forceinline__ float dot8_q8(const uint2 w, const uint4 x, float acc) {
+// product is exact in fp32), as two partial sums (even, odd elements) with
+// packed FMAs
+__device__ __forceinline__ float2 dot8_q8x2(const uint2 w, const uint4 x, float2 acc) {
     const uint32_t w0 = w.x ^ 0x80808080u, w1 = w.y ^ 0x80808080u;
-    acc = fmaf(q8_value(w0, 0), __uint_as_float(x.x << 16), acc);
-    acc = fmaf(q8_value(w0, 1), __uint_as_float(x.x & 0xffff0000u), acc);
-    acc = fmaf(q8_value(w0, 2), __uint_as_float(x.y << 16), acc);
-    acc = fmaf(q8_value(w0, 3), __uint_as_float(x.y & 0xffff0000u), acc);
-    acc = fmaf(q8_value(w1, 0), __uint_as_float(x.z << 16), acc);
-    acc = fmaf(q8_value(w1, 1), __uint_as_float(x.z & 0xffff0000u), acc);
-    acc = fmaf(q8_value(w1, 2), __uint_as_float(x.w << 16), acc);
-    acc = fmaf(q8_value(w1, 3), __uint_as_float(x.w & 0xffff0000u), acc);
+    acc = __ffma2_rn(q8_pair(w0, 0), make_float2(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u)), acc);
+    acc = __ffma2_rn(q8_pair(w0, 2), make_float2(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u)), acc);
+    acc = __ffma2_rn(q8_pair(w1, 0), make_float2(__uint_as_float(x.z << 16), __uint_as_float(x.z & 0xffff0000u)), acc);
+    acc = __ffma2_rn(q8_pair(w1, 2), make_float2(__uint_as_float(x.w << 16), __uint_as_float(x.w & 0xffff0000u)), acc);
     return acc;
 }
 
@@ -493,11 +493,14 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
             if constexpr (Q8) {
                 const uint2* gr = reinterpret_cast<const uint2*>(st);
                 const uint2* ur = gr + nchunk;
+                float2 g2 = make_float2(0.0f, 0.0f), u2 = g2;
                 for (int ch = lane; ch < nchunk; ch += 32) {
                     const uint4 xw = xv[ch];
-                    g = dot8_q8(gr[ch], xw, g);
-                    u = dot8_q8(ur[ch], xw, u);
+                    g2 = dot8_q8x2(gr[ch], xw, g2);
+                    u2 = dot8_q8x2(ur[ch], xw, u2);
                 }
+                g = g2.x + g2.y;
+                u = u2.x + u2.y;
             } else {
                 const uint4* gr = reinterpret_cast<const uint4*>(st);
                 const uint4* ur = gr + nchunk;
@@ -555,10 +558,15 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
                     const uint2* r8 = reinterpret_cast<const uint2*>(row);
                     const uint2 dw = global ? __ldg(r8 + ch) : r8[ch];
                     const uint32_t w0 = dw.x ^ 0x80808080u, w1 = dw.y ^ 0x80808080u;
+                    const float2 h2 = make_float2(hv, hv);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        yp[q][e] = fmaf(hv, q8_value(w0, e), yp[q][e]);
-                        yp[q][4 + e] = fmaf(hv, q8_value(w1, e), yp[q][4 + e]);
+                    for (int e = 0; e < 4; e += 2) {
+                        float2 a = __ffma2_rn(h2, q8_pair(w0, e), make_float2(yp[q][e], yp[q][e + 1]));
+                        yp[q][e] = a.x;
+                        yp[q][e + 1] = a.y;
+                        a = __ffma2_rn(h2, q8_pair(w1, e), make_float2(yp[q][4 + e], yp[q][5 + e]));
+                        yp[q][4 + e] = a.x;
+                        yp[q][5 + e] = a.y;
                     }
                 } else {
                     const uint4* r16 = reinterpret_cast<const uint4*>(row);
