@@ -320,16 +320,6 @@ __device__ __forceinline__ void cp_async_wait_group() {
 }
 
 // ---------------------------------------------------------------- stage 2
-// acc += sum over 8 bf16 pairs of a_e * b_e in fp32 (bf16 -> fp32 is exact)
-__device__ __forceinline__ float dot8_bf16(const uint4 a, const uint4 b, float acc) {
-    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        acc = fmaf(__uint_as_float(av[t] << 16), __uint_as_float(bv[t] << 16), acc);
-        acc = fmaf(__uint_as_float(av[t] & 0xffff0000u), __uint_as_float(bv[t] & 0xffff0000u), acc);
-    }
-    return acc;
-}
 
 // int8 weights: a word of four two's-complement codes, flipped to offset
 // binary (w ^ 0x80808080), gives code e as the exact float 2^23 + (q + 128)
@@ -504,11 +494,22 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
             } else {
                 const uint4* gr = reinterpret_cast<const uint4*>(st);
                 const uint4* ur = gr + nchunk;
+                // bf16 -> fp32 is exact; two partial sums (even, odd
+                // elements) with packed FMAs
+                float2 g2 = make_float2(0.0f, 0.0f), u2 = g2;
                 for (int ch = lane; ch < nchunk; ch += 32) {
-                    const uint4 xw = xv[ch];
-                    g = dot8_bf16(gr[ch], xw, g);
-                    u = dot8_bf16(ur[ch], xw, u);
+                    const uint4 xw = xv[ch], gw = gr[ch], uw = ur[ch];
+                    const uint32_t xa[4] = {xw.x, xw.y, xw.z, xw.w}, ga[4] = {gw.x, gw.y, gw.z, gw.w},
+                                   ua[4] = {uw.x, uw.y, uw.z, uw.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 xf = make_float2(__uint_as_float(xa[e] << 16), __uint_as_float(xa[e] & 0xffff0000u));
+                        g2 = __ffma2_rn(make_float2(__uint_as_float(ga[e] << 16), __uint_as_float(ga[e] & 0xffff0000u)), xf, g2);
+                        u2 = __ffma2_rn(make_float2(__uint_as_float(ua[e] << 16), __uint_as_float(ua[e] & 0xffff0000u)), xf, u2);
+                    }
                 }
+                g = g2.x + g2.y;
+                u = u2.x + u2.y;
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -572,11 +573,13 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
                     const uint4* r16 = reinterpret_cast<const uint4*>(row);
                     const uint4 dw = global ? __ldg(r16 + ch) : r16[ch];
                     const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
+                    const float2 h2 = make_float2(hv, hv);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        yp[q][2 * e] = fmaf(hv, __uint_as_float(dv[e] << 16), yp[q][2 * e]);
-                        yp[q][2 * e + 1] =
-                            fmaf(hv, __uint_as_float(dv[e] & 0xffff0000u), yp[q][2 * e + 1]);
+                        const float2 a = __ffma2_rn(h2, make_float2(__uint_as_float(dv[e] << 16), __uint_as_float(dv[e] & 0xffff0000u)),
+                                                    make_float2(yp[q][2 * e], yp[q][2 * e + 1]));
+                        yp[q][2 * e] = a.x;
+                        yp[q][2 * e + 1] = a.y;
                     }
                 }
             }
