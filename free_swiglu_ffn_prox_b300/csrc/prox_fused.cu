@@ -6,23 +6,25 @@
 //       (ties -> lower index) itself from x (a few KB, L2 resident), so no
 //       launch or barrier precedes the proxy stream.
 //   P1  proxy GEMV (Stage 1): CTA (tile, slice) streams the int4 proxy rows
-//       of its slice of the kept inputs, restricted to its channel tile, with
-//       128-bit loads, and writes per-slice partial (g~, u~) sums.
+//       of its slice of the kept inputs, restricted to its channel tile,
+//       through a per-thread cp.async ring, and writes per-slice partial
+//       (g~, u~) sums.
 //   --- grid barrier 1
 //   P2  CTA b owns the channel chunk [cb0, cb1) (chunk starts on multiples of
 //       4 channels, ~F/n wide): sums the slices in a fixed order
-//       (deterministic scores), forms |silu(g~) u~|, adds the chunk to a
-//       global histogram of the scores' top 11 bits, ranks the chunk and
-//       publishes it sorted (score keys and chunk-local channel bytes).
+//       (deterministic scores), forms |silu(g~) u~| (times ||W_down[:, c]||
+//       for the contribution signal; block sums for a block mask), publishes
+//       every channel's score key (the fp32 bits) in channel order and adds
+//       the chunk to a global histogram of the keys' top 11 bits.
 //   --- grid barrier 2
-//   P3a every CTA finds the exact k-th score itself (HBM is idle, so staging
-//       the histogram and every sorted chunk from L2 is fast): the digit-1
-//       bin from the histogram, that bin's candidates by a binary search per
-//       chunk, two more radix digits over the candidates, ties to the lower
-//       channel; the selected channels of each chunk are a prefix of its
-//       sorted list, and CTA b takes the positions [k b / n, k (b+1) / n) of
-//       the selected channels in chunk order as its Stage-2 items (an even
-//       split: every CTA moves the same bytes).
+//   P3a every CTA finds the exact k-th key itself: it stages all keys from L2
+//       into shared memory while it selects the digit-1 bin from the global
+//       histogram, then resolves digits 2 (bits 19..9) and 3 (bits 8..0)
+//       over that bin's candidates with loads-only passes that build
+//       per-thread bit masks; ties go to the lower channel.  A block scan
+//       gives every selected channel its position in channel order, and CTA
+//       b takes the positions [k b / n, k (b+1) / n) as its Stage-2 items
+//       (an even split: every CTA moves the same bytes).
 //   P3b Stage 2 (Eq. (1) of the PrunePath page restricted to the mask):
 //       gate|up rows and W_down^T rows arrive by bulk copies (TMA) into two
 //       shared-memory rings (bytes in flight capped); pass-A warps form
@@ -33,6 +35,12 @@
 //   Q8 instances): the codes are decoded exactly to fp32 and the scales are
 //   applied to g, u and h.
 //
+// The same step also runs
+//   * in a layer stack, several steps in one launch (k_prox_stack), each
+//     later layer forming its x from the previous layer's x and y in P0;
+//   * mask-only, for a batch over the union of its tokens' masks: after P3a
+//     each CTA records its share of the token's mask and skips Stage 2, with
+//     one token per launch or a group of CTAs per token (k_prox_masks).
 // The same Stage-2 code over all channels is the dense baseline (k_dense).
 // Every wait is bounded: a wait that runs out records PROX_ERR_TIMEOUT in
 // the layer's status word, lets copies in flight land and leaves the kernel.
@@ -101,10 +109,10 @@ struct FusedParams {
     int tiles, slices, tile_w;
     // workspace
     int* status;
-    unsigned* bar;       // [0] barrier count, [1] call epoch, [2] result flag,
-                         // [3] T, [4] split, [5] list length (control block)
-    unsigned* epoch;     // number of completed calls on this workspace
-    uint32_t* hist;      // [kHistWords]: digit-1, digit-2, digit-3 histograms
+    unsigned* bar;       // [0] grid-barrier arrival count, [1] grid barriers completed
+                         // on this workspace (control block; a group launch: its word)
+    unsigned* epoch;     // grid barriers completed on this workspace (bar + 1)
+    uint32_t* hist;      // [kHistWords]: histogram of the score keys' top 11 bits
     float2* part;        // [slices][Fp]
     uint32_t* skey;      // [Fp] every channel's score key (the fp32 score's bits), channel order
     int* idx_list;       // [Fp] debug: the selected channels, ascending
@@ -179,11 +187,12 @@ __device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
 }
 
 // Grid-wide barrier for co-resident CTAs.  The barrier word counts arrivals
-// and is never reset between calls: in call number `epoch` (read by every
-// CTA at its start) barrier i (1 or 2) completes when the word reaches
-// n * (2 epoch + i).  Arrivals are fire-and-forget release reductions; CTA
-// thread 0 polls with acquire loads.  Returns false (and records
-// PROX_ERR_TIMEOUT) if the count does not arrive within limit_ns.
+// and is never reset between calls: `target` is n times the number of the
+// barrier (the callers count the barriers completed on the workspace before
+// the launch, read by every CTA at its start).  Arrivals are fire-and-forget
+// release reductions; CTA thread 0 polls with acquire loads.  Returns false
+// (and records PROX_ERR_TIMEOUT) if the count does not arrive within
+// limit_ns.
 __device__ bool grid_barrier(unsigned* bar, unsigned target, int* status, long long limit_ns,
                              Ctl& ctl, bool skip_arrive) {
     __syncthreads();
