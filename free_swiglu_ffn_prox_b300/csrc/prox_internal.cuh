@@ -27,16 +27,18 @@ constexpr size_t kControlBytes = 2048;
 
 // Workspace carve-out (offsets in bytes, each 256-aligned).  The first
 // kControlBytes are the control block: status word, then (at +128) the grid
-// barrier count and the call epoch, and (at +1024) the per-token barrier
-// words of a batch's grouped Stage-1 launch; a fault clears the whole block.
+// barrier arrival count and the number of grid barriers completed, and (at
+// +1024) the per-token barrier words of a batch's grouped Stage-1 launch; a
+// fault clears the whole block.
 struct Workspace {
     int* status;        // [0] device status word (0 = ok)
-    unsigned* bar;      // grid barrier count; bar[1] call epoch
+    unsigned* bar;      // grid-barrier arrival count; bar[1] grid barriers completed
     uint32_t* hist;     // [kHistWords] score histogram, zeroed by each call
-    float2* part;       // [kMaxSlices][Fp] per-slice proxy partials (g~, u~)
+    float2* part;       // [kMaxSlices][Fp] per-slice proxy partials (g~, u~); a union
+                        // batch: its grouped Stage-1 scratch, then its g and u sums
     uint32_t* skey;     // [Fp] every channel's score key (fp32 score bits)
     int* idx_list;      // [Fp] debug: selected channels, ascending
-    float* hch;         // [Fp] debug: h per channel
+    float* hch;         // [Fp] debug: h per channel (a union batch: the token bits)
     float* dnorm;       // [Fp] ||W_down[:, c]||_2 per channel, written by prepare (persistent)
     uint16_t* x_stage;  // [d] bf16 input staged from host memory (prox_ffn_host)
     float* y_stage;     // [d] fp32 output staged for host memory (prox_ffn_host)

@@ -393,9 +393,8 @@ PROX_API prox_status prox_ffn_resnorm(const prox_layer* layer, const void* x_pre
  * allocate device memory when they run a step -- a host framework or server
  * that reserved the device up front and refuses further allocations, plugins
  * and latency-critical loops where an allocation would synchronise the
- * device -- the step's scratch (proxy partials, score histogram, per-chunk
- * sorted scores, selection results, grid-barrier words) lives in a fixed
- * 4 MiB array compiled into the
+ * device -- the step's scratch (proxy partials, score histogram, score
+ * keys, grid-barrier words) lives in a fixed 4 MiB array compiled into the
  * library, which every device that loads the library holds until the process
  * exits.  Nothing is allocated: no cudaMalloc, cudaFree or allocating
  * library routine is called.
