@@ -59,6 +59,7 @@ KERNELS_PER_STEP = 1       # the decode step is one persistent kernel
 KERNEL_NAMES = ("k_prox_fused",)
 SOURCE_OF = {              # kernel -> source file whose hash guards ncu traffic numbers
     "k_prox_fused": "prox_fused.cu",
+    "k_dense": "prox_fused.cu",
 }
 N_X = 16                   # distinct hidden states cycled through
 CHUNK = 64                 # steps per captured graph
@@ -571,7 +572,8 @@ def run_gpu(args):
         extras["dense"] = {"us_per_token": round(dus, 3),
                            "gbs": round(ab["dense"] / (dus * 1e-6) / 1e9, 1),
                            "frac_of_peak": round(ab["dense"] / (dus * 1e-6) / 1e9 / hbm_peak, 4),
-                           "speedup_prox_over_dense": round(dus / (ms_per_step * 1e3), 3)}
+                           "speedup_prox_over_dense": round(dus / (ms_per_step * 1e3), 3),
+                           "traffic": traffic_from_profiles("k_dense")}
 
         # ------------------------------------------------ int8 Stage-2 rows
         if not args.no_q8:
