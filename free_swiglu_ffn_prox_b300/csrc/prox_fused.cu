@@ -792,15 +792,19 @@ __device__ __forceinline__ void block_select(const uint32_t* h, uint32_t krem, C
 __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int nb, int b,
                              int cb0, int nch) {
     const int tid = threadIdx.x;
-    const int F = p.F, Fp = p.Fp;
+    // the ranked keys: one per channel, or one per block of bw channels (a
+    // block mask: its K = k / bw largest blocks, every channel of each)
+    const int bw = p.bw > 0 ? p.bw : 1;
+    const int F = p.F / bw, kk_sel = p.k / bw;
+    const uint32_t kbytes = (uint32_t)((F * 4 + 15) / 16 * 16);
     uint32_t* h2 = reinterpret_cast<uint32_t*>(area + (size_t)2 * p.d);
     uint32_t* h3 = h2 + kHistBins;
-    uint32_t* sk = h3 + 512;  // [Fp] score keys, channel order
+    uint32_t* sk = h3 + 512;  // [F] score keys, channel (block) order
     if (tid == 0) {
         asm volatile("fence.proxy.async.global;" ::: "memory");
         const uint64_t pol = policy_evict_first();
-        mbar_arrive_expect_tx(&ctl.key_ld, (uint32_t)(Fp * 4));
-        bulk_g2s(sk, p.skey, (uint32_t)(Fp * 4), &ctl.key_ld, pol);
+        mbar_arrive_expect_tx(&ctl.key_ld, kbytes);
+        bulk_g2s(sk, p.skey, kbytes, &ctl.key_ld, pol);
     }
     for (int i = tid; i < kHistBins + 512; i += kNT) h2[i] = 0u;
     // waits for one of the staging copies; after a timeout lets both land
@@ -829,7 +833,7 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
     };
     // digit 1 from the histogram of every chunk, read from L2 straight into
     // the selecting threads (the keys still landing)
-    block_select<2048>(nullptr, (uint32_t)p.k, ctl, p.hist);
+    block_select<2048>(nullptr, (uint32_t)kk_sel, ctl, p.hist);
     stamp(p.ts, 14);
     if (ctl.sel[0] == 0xffffffffu) return broken();
     const uint32_t b1 = ctl.sel[0], k1 = ctl.sel[1];
@@ -905,24 +909,31 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
     const uint32_t ex = block_excl_scan<kNT>(gt | (eq << 16), ctl, tot);
     const uint32_t ties = ex >> 16;
     const uint32_t pos = (ex & 0xffffu) + min(ties, r);  // selected channels before this thread's
-    if ((tot & 0xffffu) + min(tot >> 16, r) != (uint32_t)p.k) return broken();
+    if ((tot & 0xffffu) + min(tot >> 16, r) != (uint32_t)kk_sel) return broken();
     const int q0 = chunk_begin(p.k, b, nb), q1 = chunk_begin(p.k, b + 1, nb);
     if (q1 - q0 > kMaxItems) return broken();
     // the ties this thread keeps: its lowest min(eq, r - ties) tie bits
     uint32_t keep = ties < r ? min(eq, r - ties) : 0u;
     uint64_t sel = gtm;
     for (uint64_t m = eqm; m && keep; m &= m - 1, --keep) sel |= m & (~m + 1);
-    // a thread whose selected channels meet [q0, q1) writes those items; in
-    // debug mode CTA 0 writes the whole mask
+    // a thread whose selected keys meet the channel positions [q0, q1) writes
+    // those items (a selected block at position j holds the channel
+    // positions [j bw, (j + 1) bw)); in debug mode CTA 0 writes the whole mask
     const int nsel = __popcll(sel);
-    if ((int)pos < q1 && (int)pos + nsel > q0) {
-        int at = (int)pos;
-        for (uint64_t m = sel; m && at < q1; m &= m - 1, ++at)
-            if (at >= q0) ctl.item[at - q0] = i0 + __ffsll((long long)m) - 1;
+    if ((int)pos * bw < q1 && ((int)pos + nsel) * bw > q0) {
+        int at = (int)pos * bw;
+        for (uint64_t m = sel; m && at < q1; m &= m - 1) {
+            const int c = (i0 + __ffsll((long long)m) - 1) * bw;
+            for (int j = 0; j < bw; ++j, ++at)
+                if (at >= q0 && at < q1) ctl.item[at - q0] = c + j;
+        }
     }
     if (p.debug && b == 0) {
-        int at = (int)pos;
-        for (uint64_t m = sel; m; m &= m - 1, ++at) p.idx_list[at] = i0 + __ffsll((long long)m) - 1;
+        int at = (int)pos * bw;
+        for (uint64_t m = sel; m; m &= m - 1) {
+            const int c = (i0 + __ffsll((long long)m) - 1) * bw;
+            for (int j = 0; j < bw; ++j, ++at) p.idx_list[at] = c + j;
+        }
     }
     for (int i = tid; i < q1 - q0; i += kNT) ctl.conf[i] = 1;
     if (tid == 0) ctl.n_items = q1 - q0;
@@ -1339,10 +1350,13 @@ __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8
             }
         }
         // the key, in channel order, for the selection; one histogram
-        // reduction per distinct bin in the warp
-        if (act) p.skey[cb0 + ci] = key;
-        const unsigned am = __ballot_sync(0xffffffffu, act);
-        if (act) {
+        // reduction per distinct bin in the warp.  A block mask ranks blocks:
+        // one key and one count per block, from its first channel (chunks
+        // start on block boundaries)
+        const bool pub = act && (p.bw == 0 || ((cb0 + ci) & (p.bw - 1)) == 0);
+        if (pub) p.skey[p.bw ? (cb0 + ci) / p.bw : cb0 + ci] = key;
+        const unsigned am = __ballot_sync(0xffffffffu, pub);
+        if (pub) {
             const unsigned peers = __match_any_sync(am, key >> 20);
             if (lane == __ffs(peers) - 1)
                 asm volatile("red.global.add.u32 [%0], %1;" ::"l"(p.hist + (key >> 20)),
