@@ -18,16 +18,15 @@
 //                  (packed pairs of FMAs) and writes the two partial sums to
 //                  GU[part][t][c] (no synchronisation between the warps).
 //   k_union_down   CTA (s, r) takes the 512-output slice s of the W_down^T
-//                  rows of the union channels in range r.  Each thread owns 8
+//                  rows of the union channels in range r.  When it stages the
+//                  range's items it forms h = silu(g) u from the two parts'
+//                  sums (0 where a token's mask lacks c).  Each thread owns 8
 //                  outputs of the slice in one of 8 row groups, streams its
 //                  16-byte pieces of the rows through a cp.async ring and
 //                  accumulates y_t += h_t,c W_down^T[c, slice] for all 8
-//                  token slots, h = silu(g) u from the two parts' sums when
-//                  the range's items are staged (0 where a token's mask lacks
-//                  c), two
-//                  outputs per packed FMA.  The row groups are summed in
-//                  shared memory and added to y with one vector reduction per
-//                  4 outputs and token.
+//                  token slots, two outputs per packed FMA.  The row groups
+//                  are summed in shared memory and added to y with one vector
+//                  reduction per 4 outputs and token.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -227,7 +226,7 @@ __global__ void __launch_bounds__(kDownThreads, 1) k_union_down(const UnionDownA
     extern __shared__ __align__(128) uint8_t smem[];
     // ring [kDownRing][kDownThreads] uint4, later the row-group sums
     // [4][kUnionMaxG][kDownSlice] float (64 KB of its 96 KB); then the items,
-    // their member bits and their H values [max_items][kUnionMaxG]
+    // their member bits and their h values [max_items][kUnionMaxG]
     uint4* ring = reinterpret_cast<uint4*>(smem);
     float* red = reinterpret_cast<float*>(smem);
     int* item = reinterpret_cast<int*>(smem + (size_t)kDownRing * kDownThreads * 16);
@@ -382,7 +381,7 @@ UnionGeom union_geometry(int d, int F, int num_blocks) {
     g.gu_blocks = std::max(num_blocks, (F + kUItems - 1) / kUItems);
     g.gu_smem = fixed + (size_t)g.G * 2 * d + (size_t)g.S * 4 * d;
     // down: slices of 512 outputs x channel ranges, about one CTA per SM;
-    // a range's items, bits and H values fit next to the 96 KB ring
+    // a range's items, bits and h values fit next to the 96 KB ring
     g.nslice = (d + kDownSlice - 1) / kDownSlice;
     const size_t ring = (size_t)kDownRing * kDownThreads * 16;
     const size_t per_item = 8 + (size_t)4 * kUnionMaxG;
