@@ -76,12 +76,14 @@ def _load():
             lib.oracle_residual_rmsnorm.argtypes = [_i32, _ptr, _ptr, ctypes.c_double, _ptr]
             lib.oracle_quantize_rows_q8.argtypes = [_i32, _i32, _ptr, _ptr, _ptr]
             lib.oracle_sparse_ffn_q8.argtypes = [_i32, _i32] + [_ptr] * 7 + [_i32, _ptr, _ptr, _ptr]
+            lib.oracle_quantize_rows_q4.argtypes = [_i32, _i32, _ptr, _ptr, _ptr]
             lib.oracle_block_topk.argtypes = [_i32, _ptr, _i32, _i32, _ptr, _ptr]
             lib.oracle_contrib_scores.argtypes = [_i32, _i32, _ptr, _ptr, _ptr]
             for name in ("oracle_quantize", "oracle_input_topk", "oracle_proxy_scores",
                          "oracle_channel_topk", "oracle_sparse_ffn", "oracle_dense_ffn",
                          "oracle_prox_ffn", "oracle_residual_rmsnorm", "oracle_quantize_rows_q8",
-                         "oracle_sparse_ffn_q8", "oracle_block_topk", "oracle_contrib_scores"):
+                         "oracle_sparse_ffn_q8", "oracle_block_topk", "oracle_contrib_scores",
+                         "oracle_quantize_rows_q4"):
                 getattr(lib, name).restype = _i32
             _lib = lib
     return _lib
@@ -301,6 +303,28 @@ def stage2_q8(w_gate, w_up, w_down):
     qg, sg = quantize_rows_q8(w_gate)
     qu, su = quantize_rows_q8(w_up)
     qd, sd = quantize_rows_q8(np.ascontiguousarray(np.asarray(w_down).T))
+    return {"q_gate": qg, "s_gate": sg, "q_up": qu, "s_up": su, "q_down": qd, "s_down": sd}
+
+
+def quantize_rows_q4(w_bits):
+    """Per-row symmetric int4 of a [rows][n] bf16 matrix (the int4 reading of
+    "compatible with quantization", Prox Abstract): returns (q int8 [rows][n]
+    with values in [-8, 7], s float32 [rows])."""
+    lib = _load()
+    w = _c(w_bits, np.uint16)
+    rows, n = w.shape
+    q = np.empty((rows, n), dtype=np.int8)
+    s = np.empty(rows, dtype=np.float32)
+    _check(lib.oracle_quantize_rows_q4(rows, n, _p(w), _p(q), _p(s)), "quantize_rows_q4")
+    return q, s
+
+
+def stage2_q4(w_gate, w_up, w_down):
+    """int4 Stage-2 weights: rows of W_gate and W_up, rows of W_down^T; the
+    same dictionary as stage2_q8, so sparse_ffn_q8 evaluates Stage 2 on them."""
+    qg, sg = quantize_rows_q4(w_gate)
+    qu, su = quantize_rows_q4(w_up)
+    qd, sd = quantize_rows_q4(np.ascontiguousarray(np.asarray(w_down).T))
     return {"q_gate": qg, "s_gate": sg, "q_up": qu, "s_up": su, "q_down": qd, "s_down": sd}
 
 

@@ -379,10 +379,41 @@ int oracle_quantize_rows_q8(int rows, int n, const uint16_t* W, int8_t* q, float
     return ORACLE_OK;
 }
 
+/* Symmetric int4, one fp32 scale per row (the int4 reading of the same
+ * sentence): amax as above, s = fl32(amax / 7),
+ *   q_j = clamp(rne(fl32(W[r][j] / s)), -8, 7), or 0 when s == 0
+ * (|w / s| <= 7, so -8 is never reached from a symmetric scale; the clamp
+ * is the int4 range).  The codes are returned as int8 values in [-8, 7]. */
+int oracle_quantize_rows_q4(int rows, int n, const uint16_t* W, int8_t* q, float* s) {
+    if (rows <= 0 || n <= 0 || !W || !q || !s) return ORACLE_BAD_ARG;
+    for (int r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int j = 0; j < n; ++j) {
+            float aw = fabsf((float)oracle_bf16_to_double(W[(size_t)r * n + j]));
+            if (aw > amax) amax = aw;
+        }
+        float sr = amax / 7.0f;                      /* binary32 division */
+        s[r] = sr;
+        for (int j = 0; j < n; ++j) {
+            int code = 0;
+            if (sr != 0.0f) {
+                float w = (float)oracle_bf16_to_double(W[(size_t)r * n + j]);
+                float t = rintf(w / sr);             /* binary32 division, ties to even */
+                if (t < -8.0f) t = -8.0f;
+                if (t > 7.0f) t = 7.0f;
+                code = (int)t;
+            }
+            q[(size_t)r * n + j] = (int8_t)code;
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* Stage 2 on int8 weights ([PP] Eq. (1) with the dequantized rows): for c in
  * idx, g_c = s_gate[c] sum_j q_gate[c][j] x_j, u_c likewise,
  * h_c = silu(g_c) u_c, y_i = sum_c h_c s_down[c] q_down[c][i], where
- * q_down / s_down quantize the rows of W_down^T.  fp64, full bf16 x. */
+ * q_down / s_down quantize the rows of W_down^T.  fp64, full bf16 x.  The
+ * same sums serve int4 codes (values in [-8, 7] held as int8). */
 int oracle_sparse_ffn_q8(int F, int d, const int8_t* q_gate, const float* s_gate,
                          const int8_t* q_up, const float* s_up, const int8_t* q_down,
                          const float* s_down, const uint16_t* x, int k, const int32_t* idx,

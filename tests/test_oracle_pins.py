@@ -642,3 +642,71 @@ def test_block_topk_rejects_ragged_widths(oracle_mod):
         oracle_mod.block_topk(np.ones(10), 4, 1)  # 10 channels do not split into blocks of 4
     with pytest.raises(Exception):
         oracle_mod.block_topk(np.ones(8), 2, 5)   # only 4 blocks
+
+
+def test_q4_quantizer_invariants(oracle_mod):
+    """Per-row symmetric int4: -8 <= q <= 7 (|q| <= 7 from a symmetric scale);
+    the row's largest magnitude maps to +-7; |w - s q| <= s/2 (plus the
+    binary32 rounding of w/s); zero rows give q = 0, s = 0; each row's scale is
+    amax / 7 of that row alone."""
+    rng = np.random.default_rng(15)
+    w = (rng.standard_normal((29, 256)) * rng.uniform(0.001, 3.0, size=(29, 1))).astype(np.float32)
+    w[6] = 0.0
+    bits = oracle_mod.double_to_bf16(w)
+    q, s = oracle_mod.quantize_rows_q4(bits)
+    wf = oracle_mod.bf16_bits_to_f64(bits)
+    assert np.all(q >= -7) and np.all(q <= 7)
+    assert np.all(q[6] == 0) and s[6] == 0.0
+    amax = np.abs(wf).max(axis=1)
+    for r in range(29):
+        if r == 6:
+            continue
+        assert s[r] == np.float32(np.float32(amax[r]) / np.float32(7.0))
+        j = int(np.argmax(np.abs(wf[r])))
+        assert abs(int(q[r, j])) == 7 and np.sign(q[r, j]) == np.sign(wf[r, j])
+        err = np.abs(wf[r] - float(s[r]) * q[r].astype(np.float64))
+        assert np.all(err <= float(s[r]) * (0.5 + 7 * 2.0 ** -24))
+
+
+def test_q4_quantizer_hand_worked_row(oracle_mod):
+    """A row whose largest magnitude is 7 * 2^-3: the scale is exactly 2^-3,
+    every quotient w / s is exact, and the codes are worked out by hand.
+    Half-way quotients go to the even integer (2.5 -> 2, 3.5 -> 4, -0.5 -> 0,
+    6.5 -> 6, -5.5 -> -6), whole ones stay."""
+    u = 2.0 ** -3
+    row = np.array([7, 2.5, 3.5, -0.5, 6.5, -5.5, -7, 0, 1, -3]) * u
+    want = np.array([7, 2, 4, 0, 6, -6, -7, 0, 1, -3], dtype=np.int8)
+    bits = oracle_mod.double_to_bf16(row.reshape(1, -1))
+    assert np.array_equal(oracle_mod.bf16_bits_to_f64(bits).ravel(), row)  # exact in bf16
+    q, s = oracle_mod.quantize_rows_q4(bits)
+    assert s[0] == np.float32(u)
+    assert np.array_equal(q[0], want)
+
+
+def test_q4_stage2_reduces_to_bf16_stage2_on_exact_weights(oracle_mod):
+    """Weights w = 2^-3 q_true with integer |q_true| <= 7 and every row (and
+    W_down column) reaching 7 are exact in bf16 and quantize exactly (s =
+    2^-3), so the int4 Stage 2 equals the bf16 Stage 2 (an independent
+    function of the oracle) on any channel set."""
+    rng = np.random.default_rng(16)
+    F, d = 80, 128
+    def exact(rows, cols, col_major=False):
+        qt = rng.integers(-7, 8, size=(rows, cols))
+        if col_major:
+            qt[rng.integers(0, rows, size=cols), np.arange(cols)] = 7
+        else:
+            qt[np.arange(rows), rng.integers(0, cols, size=rows)] = -7
+        return qt, _exact_bf16_bits(qt.astype(np.float32) * np.float32(2.0 ** -3))
+    qg_t, wg = exact(F, d)
+    qu_t, wu = exact(F, d)
+    qd_t, wd = exact(d, F, col_major=True)
+    x = synth.bits(synth.make_x(d, 3, 20.0, 19))
+    q4 = oracle_mod.stage2_q4(wg, wu, wd)
+    assert np.array_equal(q4["q_gate"], qg_t) and np.array_equal(q4["q_up"], qu_t)
+    assert np.array_equal(q4["q_down"], qd_t.T)
+    assert np.all(q4["s_gate"] == np.float32(2.0 ** -3)) and np.all(q4["s_down"] == np.float32(2.0 ** -3))
+    idx = np.sort(rng.choice(F, 23, replace=False)).astype(np.int32)
+    h4, y4 = oracle_mod.sparse_ffn_q8(q4, x, idx)
+    h, y = oracle_mod.sparse_ffn(wg, wu, wd, x, idx)
+    assert np.allclose(h4, h, rtol=1e-12, atol=1e-12)
+    assert np.allclose(y4, y, rtol=1e-12, atol=1e-12 * max(1.0, np.abs(y).max()))
