@@ -23,7 +23,8 @@ same way) and the roofline of the dominant kernel; the end-to-end number
 through the host-buffer entry point prox_ffn_host (x copied in and y copied
 out every step, inside the timed region); latency and GB/s at keep fractions
 0.5 / 0.3 / 0.1; the in-library dense GEMV and the speedup over it; the
-same step and dense GEMV on layers with int8 Stage-2 rows (prox_prepare_q8);
+same step and dense GEMV on layers with int8 and with int4 Stage-2 rows
+(prox_prepare_q8, prox_prepare_q4);
 the step with block-granular masks of 16 and 64 channels (prox_ffn_blocks);
 a batch of 8 tokens with per-token masks (prox_ffn_batch);
 the 32-layer stack; and the CPU oracle timed on this host's cores (a
@@ -89,6 +90,16 @@ def algorithmic_bytes_q8(d: int, F: int, k: int, kx: int) -> dict:
     G = d // 128
     step = F * kx + 4 * F * G + k * (3 * d + 16) + 2 * d + 4 * d + 4 * k
     return {"step": step, "dense": F * (3 * d + 16) + 2 * d + 4 * d}
+
+
+def algorithmic_bytes_q4(d: int, F: int, k: int, kx: int) -> dict:
+    """As algorithmic_bytes with int4 Stage-2 rows: per selected channel the
+    gate|up codes d bytes plus 16 bytes of row scales, and d/2 bytes of
+    W_down^T codes."""
+    G = d // 128
+    row = d + 16 + d // 2
+    step = F * kx + 4 * F * G + k * row + 2 * d + 4 * d + 4 * k
+    return {"step": step, "dense": F * row + 2 * d + 4 * d}
 
 
 def keep_count(n: int, frac: float) -> int:
@@ -577,8 +588,11 @@ def run_gpu(args):
 
         # ------------------------------------------------ int8 Stage-2 rows
         if not args.no_q8:
-            extras["int8_stage2"] = q8_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak,
-                                             l2, ms_per_step, dus)
+            extras["int8_stage2"] = qrows_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak,
+                                                l2, ms_per_step, dus, wq=1)
+        if not args.no_q4:
+            extras["int4_stage2"] = qrows_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak,
+                                                l2, ms_per_step, dus, wq=2)
 
         # ------------------------------------------------ block-granular masks
         blocks = {}
@@ -835,22 +849,24 @@ def shape_sweep(prox, synth, shape, dev, stream, hbm_peak, l2):
     return out
 
 
-def q8_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak, l2, bf16_us_per_step,
-             bf16_dense_us):
-    """The same step and the dense GEMV on layers prepared with int8 Stage-2
-    rows (prox_prepare_q8), enough copies to exceed the L2 between reuses."""
+def qrows_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak, l2, bf16_us_per_step,
+                bf16_dense_us, wq):
+    """The same step and the dense GEMV on layers prepared with int8 (wq 1,
+    prox_prepare_q8) or int4 (wq 2, prox_prepare_q4) Stage-2 rows, enough
+    copies to exceed the L2 between reuses."""
     import torch
 
     d, F = shape.d_model, shape.d_ff
     k = keep_count(F, rho)
-    ab = algorithmic_bytes_q8(d, F, k, kx)
+    ab = (algorithmic_bytes_q8 if wq == 1 else algorithmic_bytes_q4)(d, F, k, kx)
+    prepare = prox.prox_prepare_q8 if wq == 1 else prox.prox_prepare_q4
     R = 4
     while R < 16 and R * ab["step"] < 4 * l2:
         R *= 2
     layers = []
     for r in range(R):
         wg, wu, wd = synth.layer(shape, seed=r, device=dev)
-        layers.append(prox.prox_prepare_q8(wg, wu, wd))
+        layers.append(prepare(wg, wu, wd))
         del wg, wu, wd
     xs = [synth.hidden(shape, seed=1 + i, device="cpu").to(dev) for i in range(N_X)]
     ys = [torch.empty(d, dtype=torch.float32, device=dev) for _ in range(N_X)]
@@ -880,7 +896,7 @@ def q8_extra(prox, synth, shape, dev, stream, rho, kx, hbm_peak, l2, bf16_us_per
                      "frac_of_peak": round(gbs / hbm_peak, 4)}
     for L in layers:
         if prox.prox_get_status(L) != 0:
-            raise SystemExit("device status set in the int8 Stage-2 measurement")
+            raise SystemExit(f"device status set in the int{8 if wq == 1 else 4} Stage-2 measurement")
     out["step"]["speedup_over_bf16_step"] = round(bf16_us_per_step * 1e3 / out["step"]["us_per_token"], 3)
     out["dense"]["speedup_over_bf16_dense"] = round(bf16_dense_us / out["dense"]["us_per_token"], 3)
     del layers
@@ -1103,6 +1119,8 @@ def main():
                     help="skip the 32-layer stack measurement in the extras")
     ap.add_argument("--no-q8", action="store_true",
                     help="skip the int8 Stage-2 measurement in the extras")
+    ap.add_argument("--no-q4", action="store_true",
+                    help="skip the int4 Stage-2 measurement in the extras")
     ap.add_argument("--no-shapes", action="store_true",
                     help="skip the Llama-2-7B and Llama-3-70B sweeps in the extras")
     ap.add_argument("--phases", action="store_true",

@@ -89,7 +89,7 @@ prox_status run_prox(const prox_layer* L, const void* x, float keep_fraction, fl
     f.scales = L->scales;
     f.gateup = L->gateup;
     f.down_t = L->down_t;
-    f.q8 = L->q8;
+    f.wq = L->wq;
     f.d = L->d_model;
     f.F = L->d_ff;
     f.x = static_cast<const uint16_t*>(x);
@@ -142,21 +142,21 @@ prox_status check_call(const prox_layer* L, const void* x, const float* y) {
     return PROX_OK;
 }
 
-prox_status query_sizes(int d_model, int d_ff, int q8, prox_sizes* out) {
+prox_status query_sizes(int d_model, int d_ff, int wq, prox_sizes* out) {
     if (!out) return PROX_ERR_INVALID_ARG;
     if (!shape_ok(d_model, d_ff)) return PROX_ERR_UNSUPPORTED_SHAPE;
     const size_t Fp = (size_t)prox::padded_ff(d_ff);
     out->proxy_codes = (size_t)d_model * Fp;
     out->proxy_scales = (size_t)(d_model / prox::kGroup) * Fp * 4;
-    out->gateup = (size_t)d_ff * prox::gu_row_bytes(d_model, q8);
-    out->down_t = (size_t)d_ff * prox::down_row_bytes(d_model, q8);
+    out->gateup = (size_t)d_ff * prox::gu_row_bytes(d_model, wq);
+    out->down_t = (size_t)d_ff * prox::down_row_bytes(d_model, wq);
     out->workspace = prox::workspace_bytes(d_model, d_ff);
     return PROX_OK;
 }
 
 prox_status prepare(int d_model, int d_ff, const void* w_gate, const void* w_up,
                     const void* w_down, void* proxy_codes, void* proxy_scales, void* gateup,
-                    void* down_t, void* workspace, prox_stream_t stream, int q8,
+                    void* down_t, void* workspace, prox_stream_t stream, int wq,
                     prox_layer** out) {
     if (!out) return PROX_ERR_INVALID_ARG;
     *out = nullptr;
@@ -180,7 +180,7 @@ prox_status prepare(int d_model, int d_ff, const void* w_gate, const void* w_up,
                                  static_cast<const __nv_bfloat16*>(w_down),
                                  static_cast<uint8_t*>(proxy_codes),
                                  static_cast<__half2*>(proxy_scales),
-                                 gateup, down_t, q8,
+                                 gateup, down_t, wq,
                                  prox::carve_workspace(workspace, d_model, d_ff).dnorm, s);
     if (e != cudaSuccess) return PROX_ERR_CUDA;
     // one persistent CTA per SM; every CTA holds its chunk of the channels
@@ -200,7 +200,7 @@ prox_status prepare(int d_model, int d_ff, const void* w_gate, const void* w_up,
     L->scales = static_cast<const __half2*>(proxy_scales);
     L->gateup = gateup;
     L->down_t = down_t;
-    L->q8 = q8;
+    L->wq = wq;
     L->ws = prox::carve_workspace(workspace, d_model, d_ff);
     *out = L;
     return PROX_OK;
@@ -239,6 +239,10 @@ prox_status prox_query_sizes_q8(int d_model, int d_ff, prox_sizes* out) {
     return query_sizes(d_model, d_ff, 1, out);
 }
 
+prox_status prox_query_sizes_q4(int d_model, int d_ff, prox_sizes* out) {
+    return query_sizes(d_model, d_ff, 2, out);
+}
+
 prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, const void* w_up,
                          const void* w_down, void* proxy_codes, void* proxy_scales,
                          void* gateup, void* down_t, void* workspace, prox_stream_t stream,
@@ -253,6 +257,14 @@ prox_status prox_prepare_q8(int d_model, int d_ff, const void* w_gate, const voi
                             prox_layer** out) {
     return prepare(d_model, d_ff, w_gate, w_up, w_down, proxy_codes, proxy_scales, gateup_q8,
                    down_q8, workspace, stream, 1, out);
+}
+
+prox_status prox_prepare_q4(int d_model, int d_ff, const void* w_gate, const void* w_up,
+                            const void* w_down, void* proxy_codes, void* proxy_scales,
+                            void* gateup_q4, void* down_q4, void* workspace, prox_stream_t stream,
+                            prox_layer** out) {
+    return prepare(d_model, d_ff, w_gate, w_up, w_down, proxy_codes, proxy_scales, gateup_q4,
+                   down_q4, workspace, stream, 2, out);
 }
 
 prox_status prox_ffn_ex(const prox_layer* layer, const void* x, float keep_fraction,
@@ -338,7 +350,7 @@ prox_status prox_stack_ffn(const prox_layer* const* layers, int n_layers, const 
     for (int l = 0; l < n_layers; ++l) {
         const prox_layer* L = layers[l];
         if (!L) return PROX_ERR_INVALID_ARG;
-        if (L->d_model != L0->d_model || L->d_ff != L0->d_ff || L->q8 != L0->q8 ||
+        if (L->d_model != L0->d_model || L->d_ff != L0->d_ff || L->wq != L0->wq ||
             L->device != L0->device || L->num_blocks != L0->num_blocks)
             return PROX_ERR_INVALID_ARG;
         sl.layer[l].codes = L->codes;
@@ -351,7 +363,7 @@ prox_status prox_stack_ffn(const prox_layer* const* layers, int n_layers, const 
     f.scales = L0->scales;
     f.gateup = L0->gateup;
     f.down_t = L0->down_t;
-    f.q8 = L0->q8;
+    f.wq = L0->wq;
     f.d = L0->d_model;
     f.F = L0->d_ff;
     f.x = sl.x0;
@@ -378,7 +390,7 @@ prox_status prox_dense_ffn(const prox_layer* layer, const void* x, float* y,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(y, 0, (size_t)layer->d_model * sizeof(float), s);
     if (e == cudaSuccess)
-        e = prox::launch_dense(layer->gateup, layer->down_t, layer->q8,
+        e = prox::launch_dense(layer->gateup, layer->down_t, layer->wq,
                                static_cast<const uint16_t*>(x), layer->d_model, layer->d_ff, y,
                                layer->ws.status, layer->num_blocks, prox::kWaitLimitNs, nullptr,
                                s);
@@ -418,7 +430,7 @@ prox_status prox_ffn_batch(const prox_layer* layer, const void* x, int batch,
 }
 
 int prox_batch_union_group(const prox_layer* layer) {
-    if (!layer || layer->q8) return 0;
+    if (!layer || layer->wq) return 0;
     return prox::union_geometry(layer->d_model, layer->d_ff, layer->num_blocks).G;
 }
 
@@ -433,7 +445,7 @@ prox_status run_union(const prox_layer* L, const void* x, int batch, float keep_
     prox_status st = check_call(L, x, y);
     if (st != PROX_OK) return st;
     if (batch < 1 || !frac_ok(keep_fraction)) return PROX_ERR_INVALID_ARG;
-    if (L->q8) return PROX_ERR_UNSUPPORTED_SHAPE;  // bf16 Stage-2 rows only
+    if (L->wq) return PROX_ERR_UNSUPPORTED_SHAPE;  // bf16 Stage-2 rows only
     const int G = prox_batch_union_group(L);
     if (G < 1) return PROX_ERR_UNSUPPORTED_SHAPE;
     if (member_out && (batch > G || !aligned16(member_out))) return PROX_ERR_INVALID_ARG;
@@ -470,7 +482,7 @@ prox_status run_union(const prox_layer* L, const void* x, int batch, float keep_
             f.scales = L->scales;
             f.gateup = L->gateup;
             f.down_t = L->down_t;
-            f.q8 = 0;
+            f.wq = 0;
             f.d = L->d_model;
             f.F = L->d_ff;
             f.x = xs + (g0 + t) * d;
@@ -618,7 +630,7 @@ prox_status prox_ffn_phase_times(const prox_layer* layer, const void* x, float k
     if (dense) {
         e = cudaMemsetAsync(y, 0, (size_t)layer->d_model * sizeof(float), s);
         if (e == cudaSuccess)
-            e = prox::launch_dense(layer->gateup, layer->down_t, layer->q8,
+            e = prox::launch_dense(layer->gateup, layer->down_t, layer->wq,
                                    static_cast<const uint16_t*>(x), layer->d_model, layer->d_ff,
                                    y, layer->ws.status, layer->num_blocks, prox::kWaitLimitNs,
                                    stamps, s);

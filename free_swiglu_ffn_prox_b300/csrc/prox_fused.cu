@@ -31,9 +31,9 @@
 //       h = silu(W_gate x) (W_up x) per item (one warp per row), pass-B
 //       warps own slices of d_model and accumulate h * W_down^T; one vector
 //       atomic per element adds the CTA's part of y at the end.
-//   Stage-2 rows are bf16, or int8 with one fp32 scale per row (the kernels'
-//   Q8 instances): the codes are decoded exactly to fp32 and the scales are
-//   applied to g, u and h.
+//   Stage-2 rows are bf16 (WQ = 0), or int8 (1) or int4 (2) codes with one
+//   fp32 scale per row: the codes are decoded exactly to fp32 and the scales
+//   are applied to g, u and h.
 //
 // The same step also runs
 //   * in a layer stack, several steps in one launch (k_prox_stack), each
@@ -59,7 +59,7 @@ constexpr int kDProducerWarp = 17;
 constexpr int kSelectorWarp = 18;
 constexpr int kMaxStages = 16;
 constexpr size_t kGuRingBytes = 112 * 1024;   // gate|up bytes in flight per SM (bf16)
-constexpr size_t kGuRingBytesQ8 = 136 * 1024; // ... (int8 rows: 16 stages at d = 4096)
+constexpr size_t kGuRingBytesQ = 136 * 1024;  // ... (int8 rows: 16 stages at d = 4096; int4)
 constexpr size_t kDRingBytes = 48 * 1024;     // W_down^T bytes in flight per SM
 constexpr int kMaxItems = 512;            // Stage-2 items per CTA
 constexpr int kMaxChunk = 256;            // channels per CTA chunk
@@ -87,9 +87,9 @@ struct FusedParams {
     // layer
     const uint8_t* codes;
     const __half2* scales;
-    const uint8_t* gateup;  // Stage-2 rows, bf16 or (q8) int8 with scales
+    const uint8_t* gateup;  // Stage-2 rows: bf16, or int8 / int4 codes with scales
     const uint8_t* down_t;
-    int q8;
+    int wq;                 // Stage-2 row format: 0 bf16, 1 int8, 2 int4
     int d, F, Fp;
     // call
     const uint16_t* x;
@@ -341,21 +341,48 @@ __device__ __forceinline__ float2 q8_pair(uint32_t wo, int e) {
     return __fadd2_rn(b, make_float2(-8388736.0f, -8388736.0f));
 }
 
-// acc += sum over 8 elements of q_e * x_e (int8 codes w, bf16 x; every
-// product is exact in fp32), as two partial sums (even, odd elements) with
-// packed FMAs
-__device__ __forceinline__ float2 dot8_q8x2(const uint2 w, const uint4 x, float2 acc) {
+// acc += sum over 8 elements of q_e * x_e (int8 codes w; x as fp32, elements
+// 0..3 in xa and 4..7 in xb; every product is exact in fp32), as two
+// partial sums (even, odd elements) with packed FMAs
+__device__ __forceinline__ float2 dot8_q8x2(const uint2 w, const float4 xa, const float4 xb, float2 acc) {
     const uint32_t w0 = w.x ^ 0x80808080u, w1 = w.y ^ 0x80808080u;
-    acc = __ffma2_rn(q8_pair(w0, 0), make_float2(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u)), acc);
-    acc = __ffma2_rn(q8_pair(w0, 2), make_float2(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u)), acc);
-    acc = __ffma2_rn(q8_pair(w1, 0), make_float2(__uint_as_float(x.z << 16), __uint_as_float(x.z & 0xffff0000u)), acc);
-    acc = __ffma2_rn(q8_pair(w1, 2), make_float2(__uint_as_float(x.w << 16), __uint_as_float(x.w & 0xffff0000u)), acc);
+    acc = __ffma2_rn(q8_pair(w0, 0), make_float2(xa.x, xa.y), acc);
+    acc = __ffma2_rn(q8_pair(w0, 2), make_float2(xa.z, xa.w), acc);
+    acc = __ffma2_rn(q8_pair(w1, 0), make_float2(xb.x, xb.y), acc);
+    acc = __ffma2_rn(q8_pair(w1, 2), make_float2(xb.z, xb.w), acc);
+    return acc;
+}
+
+// int4 weights: a word holds the offset-binary codes n = q + 8 of 8
+// consecutive elements, element 2 j + h in bits 16 h + 4 j.  Masking nibble
+// j of the low and of the high half-word and OR-ing in the exponent of 2^23
+// gives the exact floats 2^23 + n 2^(4 j) (one LOP3 each); one packed FMA by
+// 2^(-4 j) with addend -(2^(23 - 4 j) + 8) leaves q = n - 8 exactly (every
+// intermediate value is an integer below 2^24).  The pair is elements
+// (2 j, 2 j + 1), the two halves of bf16 word j of the same 8 elements.
+template <int J>
+__device__ __forceinline__ float2 q4_pair(uint32_t lo, uint32_t hi) {
+    constexpr uint32_t m = 0xFu << (4 * J);
+    constexpr float sc = 1.0f / (float)(1u << (4 * J));
+    constexpr float off = -(float)(1u << (23 - 4 * J)) - 8.0f;
+    const float2 b = make_float2(__uint_as_float((lo & m) | 0x4B000000u),
+                                 __uint_as_float((hi & m) | 0x4B000000u));
+    return __ffma2_rn(b, make_float2(sc, sc), make_float2(off, off));
+}
+
+// acc += sum over 8 elements of q_e * x_e (int4 codes w; x as in dot8_q8x2)
+__device__ __forceinline__ float2 dot8_q4x2(const uint32_t w, const float4 xa, const float4 xb, float2 acc) {
+    const uint32_t hi = w >> 16;
+    acc = __ffma2_rn(q4_pair<0>(w, hi), make_float2(xa.x, xa.y), acc);
+    acc = __ffma2_rn(q4_pair<1>(w, hi), make_float2(xa.z, xa.w), acc);
+    acc = __ffma2_rn(q4_pair<2>(w, hi), make_float2(xb.x, xb.y), acc);
+    acc = __ffma2_rn(q4_pair<3>(w, hi), make_float2(xb.z, xb.w), acc);
     return acc;
 }
 
 struct Stage2Args {
-    const uint8_t* gateup;  // [F] rows of gu_row_bytes(d, Q8)
-    const uint8_t* down_t;  // [F] rows of down_row_bytes(d, Q8)
+    const uint8_t* gateup;  // [F] rows of gu_row_bytes(d, WQ)
+    const uint8_t* down_t;  // [F] rows of down_row_bytes(d, WQ)
     float* y;
     float* hch;     // [F] h per channel (debug, may be null)
     int* status;
@@ -376,12 +403,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, long l
     return __all_sync(0xffffffffu, got);
 }
 
-// Waits (every lane polls) until the shared-memory flag is set.
+// Waits (every lane polls) until the shared-memory flag is set.  After two
+// polls the warp sleeps between polls: a spinning warp takes issue slots
+// from the warps on its scheduler that compute what it waits for (pass B
+// waiting on pass A's h).
 __device__ __forceinline__ bool warp_wait_flag(const uint8_t* flag, long long limit_ns, Ctl& ctl,
                                                int* status) {
     bool got = true;
     uint64_t t0 = 0;
     for (uint32_t it = 1; !*reinterpret_cast<const volatile uint8_t*>(flag); ++it) {
+        if (it > 2) __nanosleep(32);
         if ((it & 63u) == 0) {
             if (*reinterpret_cast<volatile int*>(&ctl.abort)) {
                 got = false;
@@ -405,27 +436,29 @@ __device__ __forceinline__ bool warp_wait_flag(const uint8_t* flag, long long li
 // Items [0, m) are known when the roles start; the rest (ctl.n_items, their
 // channels and ctl.conf of every item) only once ctl.sel_bar completes.
 // Shared area: x as bf16 (2 d bytes), then n_gu gate|up stages and n_d
-// W_down^T stages, one row each (bf16: 4 d and 2 d bytes; Q8: the int8 codes
-// 2 d + 16 bytes with the row's scales s_gate, s_up, s_down, and d bytes).
+// W_down^T stages, one row each (bf16: 4 d and 2 d bytes; int8: the codes
+// 2 d + 16 bytes with the row's scales s_gate, s_up, s_down, and d bytes;
+// int4: d + 16 and d / 2 bytes); for codes, x once more as fp32 after the
+// rings (4 d bytes).
 //   GU producer (warp 16) / D producer (warp 17): lane 0 issues one bulk copy
 //       per item into the next stage of its ring;
 //   pass A (warp w < n_a, n_a dividing n_gu): the items i = w (mod n_a); item
 //       i sits in gate|up stage i mod n_gu, whose items are all = w (mod
 //       n_a), so one warp consumes each stage's uses in order (a parity wait
 //       is never taken two uses ahead): g, u over the whole row,
-//       h = silu(g) u, then ctl.hready[i] (Q8: g and u times the row scales,
-//       and ctl.h[i] = h s_down, the factor of the int8 W_down^T row);
+//       h = silu(g) u, then ctl.hready[i] (codes: g and u times the row
+//       scales, and ctl.h[i] = h s_down, the factor of the W_down^T codes);
 //   pass B (warps 8..15): every thread owns 8-element slices of d and, for
 //       each confirmed item in order, adds h * W_down^T[c, slice].
-template <int CPT, bool Q8>
+template <int CPT, int WQ>
 __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = a.d, n_gu = a.n_gu, n_d = a.n_d, n_a = a.n_a;
-    const size_t gu_bytes = gu_row_bytes(d, Q8), d_bytes = down_row_bytes(d, Q8);
+    const size_t gu_bytes = gu_row_bytes(d, WQ), d_bytes = down_row_bytes(d, WQ);
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(area);
     uint8_t* gu_ring = area + (size_t)2 * d;
     uint8_t* d_ring = gu_ring + (size_t)n_gu * gu_bytes;
-    const int nchunk = d / 8;  // 8-element chunks per row (16 bytes bf16, 8 bytes int8)
+    const int nchunk = d / 8;  // 8-element chunks per row (16 bytes bf16, 8 int8, 4 int4)
 
     if (warp == kGuProducerWarp || warp == kDProducerWarp) {
         if (lane != 0) return;
@@ -475,6 +508,21 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
         // ------------------------------------------------ pass A: h per item
         if (warp >= n_a) return;
         const uint4* xv = reinterpret_cast<const uint4*>(xs);
+        // codes: the pass-A warps first write x as fp32 in two planes
+        // (elements 0..3 and 4..7 of every 8-element chunk), so that a lane's
+        // x loads are consecutive and no row converts x again
+        float4* xfa = reinterpret_cast<float4*>(d_ring + (size_t)n_d * d_bytes);
+        float4* xfb = xfa + nchunk;
+        if constexpr (WQ != 0) {
+            for (int ch = threadIdx.x; ch < nchunk; ch += n_a * 32) {
+                const uint4 w = xv[ch];
+                xfa[ch] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                                      __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+                xfb[ch] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                                      __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+            }
+            named_barrier_sync(2, n_a * 32);  // warps 0 .. n_a - 1, each once
+        }
         bool known = false;
         for (int i = warp;; i += n_a) {
             const int s = i % n_gu;
@@ -489,14 +537,25 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
             if (i == 0 && lane == 0) stamp_here(a.ts, 6);
             const uint8_t* st = gu_ring + (size_t)s * gu_bytes;
             float g = 0.0f, u = 0.0f;
-            if constexpr (Q8) {
+            if constexpr (WQ == 2) {
+                const uint32_t* gr = reinterpret_cast<const uint32_t*>(st);
+                const uint32_t* ur = gr + nchunk;
+                float2 g2 = make_float2(0.0f, 0.0f), u2 = g2;
+                for (int ch = lane; ch < nchunk; ch += 32) {
+                    const float4 xa = xfa[ch], xb = xfb[ch];
+                    g2 = dot8_q4x2(gr[ch], xa, xb, g2);
+                    u2 = dot8_q4x2(ur[ch], xa, xb, u2);
+                }
+                g = g2.x + g2.y;
+                u = u2.x + u2.y;
+            } else if constexpr (WQ == 1) {
                 const uint2* gr = reinterpret_cast<const uint2*>(st);
                 const uint2* ur = gr + nchunk;
                 float2 g2 = make_float2(0.0f, 0.0f), u2 = g2;
                 for (int ch = lane; ch < nchunk; ch += 32) {
-                    const uint4 xw = xv[ch];
-                    g2 = dot8_q8x2(gr[ch], xw, g2);
-                    u2 = dot8_q8x2(ur[ch], xw, u2);
+                    const float4 xa = xfa[ch], xb = xfb[ch];
+                    g2 = dot8_q8x2(gr[ch], xa, xb, g2);
+                    u2 = dot8_q8x2(ur[ch], xa, xb, u2);
                 }
                 g = g2.x + g2.y;
                 u = u2.x + u2.y;
@@ -527,15 +586,15 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
             }
             if (lane == 0) {
                 float hs = 1.0f;  // factor of the W_down^T row
-                if constexpr (Q8) {
-                    const float4 sc = *reinterpret_cast<const float4*>(st + (size_t)2 * d);
+                if constexpr (WQ != 0) {  // the scales end the row
+                    const float4 sc = *reinterpret_cast<const float4*>(st + gu_bytes - 16);
                     g *= sc.x;
                     u *= sc.y;
                     hs = sc.z;
                 }
                 mbar_arrive(&ctl.gu_empty[s]);
                 const float h = g / (1.0f + expf(-g)) * u;  // silu(g) * u
-                ctl.h[i] = Q8 ? h * hs : h;
+                ctl.h[i] = WQ ? h * hs : h;
                 if (a.hch) a.hch[ctl.item[i]] = h;
                 __threadfence_block();
                 *reinterpret_cast<volatile uint8_t*>(&ctl.hready[i]) = 1;
@@ -564,7 +623,24 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
         for (int q = 0; q < CPT; ++q) {
             const int ch = t + q * kPassB;
             if (ch < nchunk) {
-                if constexpr (Q8) {
+                if constexpr (WQ == 2) {
+                    const uint32_t* r4 = reinterpret_cast<const uint32_t*>(row);
+                    const uint32_t dw = global ? __ldg(r4 + ch) : r4[ch];
+                    const uint32_t hi = dw >> 16;
+                    const float2 h2 = make_float2(hv, hv);
+                    float2 a = __ffma2_rn(h2, q4_pair<0>(dw, hi), make_float2(yp[q][0], yp[q][1]));
+                    yp[q][0] = a.x;
+                    yp[q][1] = a.y;
+                    a = __ffma2_rn(h2, q4_pair<1>(dw, hi), make_float2(yp[q][2], yp[q][3]));
+                    yp[q][2] = a.x;
+                    yp[q][3] = a.y;
+                    a = __ffma2_rn(h2, q4_pair<2>(dw, hi), make_float2(yp[q][4], yp[q][5]));
+                    yp[q][4] = a.x;
+                    yp[q][5] = a.y;
+                    a = __ffma2_rn(h2, q4_pair<3>(dw, hi), make_float2(yp[q][6], yp[q][7]));
+                    yp[q][6] = a.x;
+                    yp[q][7] = a.y;
+                } else if constexpr (WQ == 1) {
                     const uint2* r8 = reinterpret_cast<const uint2*>(row);
                     const uint2 dw = global ? __ldg(r8 + ch) : r8[ch];
                     const uint32_t w0 = dw.x ^ 0x80808080u, w1 = dw.y ^ 0x80808080u;
@@ -853,7 +929,7 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
         for (int w = 0; w < (tid >> 5); ++w) rank += (int)ctl.warp_tot[w];  // nch <= 256: <= 7 warps
         if (rank < kPrefetchItems && !p.member) {  // mask only: the rows are read later
             const int c = cb0 + tid;
-            const size_t gb = gu_row_bytes(p.d, p.q8), db = down_row_bytes(p.d, p.q8);
+            const size_t gb = gu_row_bytes(p.d, p.wq), db = down_row_bytes(p.d, p.wq);
             prefetch_l2(p.gateup + (size_t)c * gb, (uint32_t)gb);
             prefetch_l2(p.down_t + (size_t)c * db, (uint32_t)db);
         }
@@ -953,7 +1029,7 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
 // out or a check failed; the status word says which).
 // GROUPED: the grid is split into groups of p.gsize CTAs (k_prox_masks);
 // a group's CTA chunks can then be wider than the CTA's threads.
-template <int CPT, bool Q8, bool GROUPED = false>
+template <int CPT, int WQ, bool GROUPED = false>
 __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8_t* area,
                                            unsigned gen, unsigned bi, bool last) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -1399,13 +1475,13 @@ __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8
     a.n_a = p.n_a;
     a.limit_ns = p.limit_ns;
     a.ts = p.ts;
-    if (wid != kSelectorWarp) stage2_roles<CPT, Q8>(a, ctl, area, m);
+    if (wid != kSelectorWarp) stage2_roles<CPT, WQ>(a, ctl, area, m);
     stage2_join(a, ctl);
     return !*reinterpret_cast<volatile int*>(&ctl.abort);
 }
 
 // The decode step: one layer per launch.
-template <int CPT, bool Q8>
+template <int CPT, int WQ>
 __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
@@ -1415,7 +1491,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
         ctl.epoch = *reinterpret_cast<volatile unsigned*>(p.epoch);
     }
     __syncthreads();
-    fused_step<CPT, Q8>(p, ctl, area, ctl.epoch, 0u, true);
+    fused_step<CPT, WQ>(p, ctl, area, ctl.epoch, 0u, true);
 }
 
 // A stack of layers in one launch: layer l takes x_l = bf16(RMSNorm(x_{l-1}
@@ -1425,7 +1501,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_fused(const FusedParams p) {
 // weights and buffers, copied into shared memory for its step.  Layer l's
 // step barriers are number gen + 3l + 1 and + 2; the barrier in front of
 // layer l > 0 is number gen + 3l.
-template <int CPT, bool Q8>
+template <int CPT, int WQ>
 __global__ void __launch_bounds__(kNT, 1) k_prox_stack(const FusedParams base, const StackLayers sl) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
@@ -1462,7 +1538,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_stack(const FusedParams base, c
             ctl.sp = q;
         }
         __syncthreads();
-        if (!fused_step<CPT, Q8>(ctl.sp, ctl, area, gen, bi, l + 1 == sl.n)) return;
+        if (!fused_step<CPT, WQ>(ctl.sp, ctl, area, gen, bi, l + 1 == sl.n)) return;
     }
 }
 
@@ -1470,7 +1546,7 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_stack(const FusedParams base, c
 // groups of mg.gsize CTAs, group t runs token t's step in mask-only mode on
 // its own x, y row, histogram, proxy partials, score keys and barrier word
 // (mg.scratch + t mg.stride, mg.gbar[t], the latter zero at launch).
-template <int CPT, bool Q8>
+template <int CPT, int WQ>
 __global__ void __launch_bounds__(kNT, 1) k_prox_masks(const FusedParams base, const MaskGroups mg) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
@@ -1490,12 +1566,12 @@ __global__ void __launch_bounds__(kNT, 1) k_prox_masks(const FusedParams base, c
         ctl.sp = q;
     }
     __syncthreads();
-    fused_step<CPT, Q8, true>(ctl.sp, ctl, area, 0u, 0u, false);
+    fused_step<CPT, WQ, true>(ctl.sp, ctl, area, 0u, 0u, false);
 }
 
 // Dense baseline: Stage 2 over every channel, CTA i taking [F i/n, F (i+1)/n)
 // (all items known and confirmed from the start).
-template <int CPT, bool Q8>
+template <int CPT, int WQ>
 __global__ void __launch_bounds__(kNT, 1) k_dense(const Stage2Args a, const uint16_t* x) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem_raw);
@@ -1519,7 +1595,7 @@ __global__ void __launch_bounds__(kNT, 1) k_dense(const Stage2Args a, const uint
         fence_mbar_init();
     }
     __syncthreads();
-    if ((tid >> 5) != kSelectorWarp) stage2_roles<CPT, Q8>(a, ctl, area, n);
+    if ((tid >> 5) != kSelectorWarp) stage2_roles<CPT, WQ>(a, ctl, area, n);
     stage2_join(a, ctl);
 }
 
@@ -1540,19 +1616,23 @@ struct Ring {
 
 size_t area_budget() { return kSmemLimit - ctl_bytes(); }
 
-// Stage-2 rings after x (2 d bytes): gate|up stages (one row each) up to
-// kGuRingBytes (bf16) or kGuRingBytesQ8 (int8) and kMaxStages, consumed by
+// Stage-2 rings after x (stage2_x_bytes): gate|up stages (one row each) up to
+// kGuRingBytes (bf16) or kGuRingBytesQ (int8, int4) and kMaxStages, consumed by
 // n_a = min(stages, kPassAWarps) pass-A warps (the stage count rounded down
 // to a multiple of n_a), then W_down^T stages up to kDRingBytes, both within
 // the shared memory left.  The bf16 caps keep ~160 KB in flight per SM:
 // enough to saturate HBM, and every extra byte in flight only lengthens the
 // queues that the channel selection's loads wait in.  Rows of int8 are half
-// as long, so their ring holds more of them.
-Ring ring_for(int d, int q8) {
-    const size_t budget = area_budget() - (size_t)2 * d;
-    const size_t gu = gu_row_bytes(d, q8), dd = down_row_bytes(d, q8);
+// as long, so their ring holds more of them; int4 rows a quarter, so theirs
+// is kMaxStages deep (~66 KB at d = 4096).
+// x in the Stage-2 area: bf16 (2 d bytes), and for codes also fp32 (4 d).
+size_t stage2_x_bytes(int d, int wq) { return (size_t)(wq ? 6 : 2) * d; }
+
+Ring ring_for(int d, int wq) {
+    const size_t budget = area_budget() - stage2_x_bytes(d, wq);
+    const size_t gu = gu_row_bytes(d, wq), dd = down_row_bytes(d, wq);
     Ring r{0, 0, 0};
-    r.n_gu = (int)(min(budget * 2 / 3, q8 ? kGuRingBytesQ8 : kGuRingBytes) / gu);
+    r.n_gu = (int)(min(budget * 2 / 3, wq ? kGuRingBytesQ : kGuRingBytes) / gu);
     if (r.n_gu > kMaxStages) r.n_gu = kMaxStages;
     if (r.n_gu < 1) r.n_gu = 1;
     r.n_a = r.n_gu < kPassAWarps ? r.n_gu : kPassAWarps;
@@ -1564,9 +1644,9 @@ Ring ring_for(int d, int q8) {
     return r;
 }
 
-size_t ring_bytes(int d, int q8, const Ring& r) {
-    return (size_t)2 * d + (size_t)r.n_gu * gu_row_bytes(d, q8) +
-           (size_t)r.n_d * down_row_bytes(d, q8);
+size_t ring_bytes(int d, int wq, const Ring& r) {
+    return stage2_x_bytes(d, wq) + (size_t)r.n_gu * gu_row_bytes(d, wq) +
+           (size_t)r.n_d * down_row_bytes(d, wq);
 }
 
 template <typename K>
@@ -1612,34 +1692,22 @@ ProxyGeom proxy_geometry(int F, int kx, int num_blocks, bool any_width) {
 
 cudaError_t fused_configure() {
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<1, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<2, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<4, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<8, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<1, true>);
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<2, true>);
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<4, true>);
-    if (e == cudaSuccess) e = set_smem(k_prox_fused<8, true>);
-    if (e == cudaSuccess) e = set_smem(k_prox_masks<1, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_masks<2, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_masks<4, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_masks<8, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_stack<1, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_stack<2, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_stack<4, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_stack<8, false>);
-    if (e == cudaSuccess) e = set_smem(k_prox_stack<1, true>);
-    if (e == cudaSuccess) e = set_smem(k_prox_stack<2, true>);
-    if (e == cudaSuccess) e = set_smem(k_prox_stack<4, true>);
-    if (e == cudaSuccess) e = set_smem(k_prox_stack<8, true>);
-    if (e == cudaSuccess) e = set_smem(k_dense<1, false>);
-    if (e == cudaSuccess) e = set_smem(k_dense<2, false>);
-    if (e == cudaSuccess) e = set_smem(k_dense<4, false>);
-    if (e == cudaSuccess) e = set_smem(k_dense<8, false>);
-    if (e == cudaSuccess) e = set_smem(k_dense<1, true>);
-    if (e == cudaSuccess) e = set_smem(k_dense<2, true>);
-    if (e == cudaSuccess) e = set_smem(k_dense<4, true>);
-    if (e == cudaSuccess) e = set_smem(k_dense<8, true>);
+    auto all = [&](auto k1, auto k2, auto k4, auto k8) {
+        if (e == cudaSuccess) e = set_smem(k1);
+        if (e == cudaSuccess) e = set_smem(k2);
+        if (e == cudaSuccess) e = set_smem(k4);
+        if (e == cudaSuccess) e = set_smem(k8);
+    };
+    all(k_prox_fused<1, 0>, k_prox_fused<2, 0>, k_prox_fused<4, 0>, k_prox_fused<8, 0>);
+    all(k_prox_fused<1, 1>, k_prox_fused<2, 1>, k_prox_fused<4, 1>, k_prox_fused<8, 1>);
+    all(k_prox_fused<1, 2>, k_prox_fused<2, 2>, k_prox_fused<4, 2>, k_prox_fused<8, 2>);
+    all(k_prox_masks<1, 0>, k_prox_masks<2, 0>, k_prox_masks<4, 0>, k_prox_masks<8, 0>);
+    all(k_prox_stack<1, 0>, k_prox_stack<2, 0>, k_prox_stack<4, 0>, k_prox_stack<8, 0>);
+    all(k_prox_stack<1, 1>, k_prox_stack<2, 1>, k_prox_stack<4, 1>, k_prox_stack<8, 1>);
+    all(k_prox_stack<1, 2>, k_prox_stack<2, 2>, k_prox_stack<4, 2>, k_prox_stack<8, 2>);
+    all(k_dense<1, 0>, k_dense<2, 0>, k_dense<4, 0>, k_dense<8, 0>);
+    all(k_dense<1, 1>, k_dense<2, 1>, k_dense<4, 1>, k_dense<8, 1>);
+    all(k_dense<1, 2>, k_dense<2, 2>, k_dense<4, 2>, k_dense<8, 2>);
     return e;
 }
 
@@ -1660,15 +1728,20 @@ bool fused_fits(int d, int F) {
     // every channel's score key
     const size_t sel = (size_t)2 * d + (size_t)4 * (kHistBins + 512) + (size_t)4 * padded_ff(F);
     return p01 <= area_budget() && ring_bytes(d, 0, r) <= area_budget() &&
-           ring_bytes(d, 1, ring_for(d, 1)) <= area_budget() && sel <= area_budget() &&
+           ring_bytes(d, 1, ring_for(d, 1)) <= area_budget() &&
+           ring_bytes(d, 2, ring_for(d, 2)) <= area_budget() && sel <= area_budget() &&
            r.n_gu >= 1 && r.n_d >= 1 && d / 8 <= kXGroups * kNT;
 }
 
 namespace {
 template <int CPT>
 cudaError_t launch_fused_t(const cudaLaunchConfig_t& cfg, const FusedParams& p) {
-    return p.q8 ? cudaLaunchKernelEx(&cfg, k_prox_fused<CPT, true>, p)
-                : cudaLaunchKernelEx(&cfg, k_prox_fused<CPT, false>, p);
+    switch (p.wq) {
+        case 0: return cudaLaunchKernelEx(&cfg, k_prox_fused<CPT, 0>, p);
+        case 1: return cudaLaunchKernelEx(&cfg, k_prox_fused<CPT, 1>, p);
+        case 2: return cudaLaunchKernelEx(&cfg, k_prox_fused<CPT, 2>, p);
+        default: return cudaErrorInvalidValue;
+    }
 }
 }  // namespace
 
@@ -1679,7 +1752,7 @@ FusedParams make_params(const FusedLaunch& L) {
     p.scales = L.scales;
     p.gateup = static_cast<const uint8_t*>(L.gateup);
     p.down_t = static_cast<const uint8_t*>(L.down_t);
-    p.q8 = L.q8;
+    p.wq = L.wq;
     p.d = L.d;
     p.F = L.F;
     p.Fp = padded_ff(L.F);
@@ -1708,7 +1781,7 @@ FusedParams make_params(const FusedLaunch& L) {
     p.kept_out = L.kept_out;
     p.scores_out = L.scores_out;
     p.debug = (L.idx_out || L.h_out) ? 1 : 0;
-    const Ring r = ring_for(L.d, L.q8);
+    const Ring r = ring_for(L.d, L.wq);
     p.n_gu = r.n_gu;
     p.n_d = r.n_d;
     p.n_a = r.n_a;
@@ -1736,8 +1809,12 @@ cudaLaunchConfig_t coop_config(int blocks, cudaStream_t stream, cudaLaunchAttrib
 
 template <int CPT>
 cudaError_t launch_stack_t(const cudaLaunchConfig_t& cfg, const FusedParams& p, const StackLayers& sl) {
-    return p.q8 ? cudaLaunchKernelEx(&cfg, k_prox_stack<CPT, true>, p, sl)
-                : cudaLaunchKernelEx(&cfg, k_prox_stack<CPT, false>, p, sl);
+    switch (p.wq) {
+        case 0: return cudaLaunchKernelEx(&cfg, k_prox_stack<CPT, 0>, p, sl);
+        case 1: return cudaLaunchKernelEx(&cfg, k_prox_stack<CPT, 1>, p, sl);
+        case 2: return cudaLaunchKernelEx(&cfg, k_prox_stack<CPT, 2>, p, sl);
+        default: return cudaErrorInvalidValue;
+    }
 }
 }  // namespace
 
@@ -1800,7 +1877,7 @@ MaskGroupGeom mask_group_geometry(int d, int F, int k, int ntok, int num_blocks)
 cudaError_t launch_masks(const FusedLaunch& L, int ntok, int token0, uint8_t* scratch,
                          unsigned* gbar, cudaStream_t stream) {
     const MaskGroupGeom g = mask_group_geometry(L.d, L.F, L.k, ntok, L.num_blocks);
-    if (g.gsize == 0 || !L.member || L.q8 || L.bw) return cudaErrorInvalidValue;
+    if (g.gsize == 0 || !L.member || L.wq || L.bw) return cudaErrorInvalidValue;
     FusedParams p = make_params(L);
     const ProxyGeom geo = proxy_geometry(L.F, L.kx, g.gsize, true);
     if (geo.tiles < 1) return cudaErrorInvalidValue;
@@ -1824,14 +1901,14 @@ cudaError_t launch_masks(const FusedLaunch& L, int ntok, int token0, uint8_t* sc
     const int nchunk = L.d / 8;
     const int cpt = nchunk <= kPassB ? 1 : nchunk <= 2 * kPassB ? 2 : nchunk <= 4 * kPassB ? 4 : 8;
     switch (cpt) {
-        case 1: return cudaLaunchKernelEx(&cfg, k_prox_masks<1, false>, p, mg);
-        case 2: return cudaLaunchKernelEx(&cfg, k_prox_masks<2, false>, p, mg);
-        case 4: return cudaLaunchKernelEx(&cfg, k_prox_masks<4, false>, p, mg);
-        default: return cudaLaunchKernelEx(&cfg, k_prox_masks<8, false>, p, mg);
+        case 1: return cudaLaunchKernelEx(&cfg, k_prox_masks<1, 0>, p, mg);
+        case 2: return cudaLaunchKernelEx(&cfg, k_prox_masks<2, 0>, p, mg);
+        case 4: return cudaLaunchKernelEx(&cfg, k_prox_masks<4, 0>, p, mg);
+        default: return cudaLaunchKernelEx(&cfg, k_prox_masks<8, 0>, p, mg);
     }
 }
 
-cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const uint16_t* x, int d,
+cudaError_t launch_dense(const void* gateup, const void* down_t, int wq, const uint16_t* x, int d,
                          int F, float* y, int* status, int num_blocks, long long limit_ns,
                          uint64_t* ts, cudaStream_t stream) {
     if (num_blocks < 1 || num_blocks > kMaxBlocks) return cudaErrorInvalidValue;
@@ -1843,7 +1920,7 @@ cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const u
     a.status = status;
     a.d = d;
     a.F = F;
-    const Ring r = ring_for(d, q8);
+    const Ring r = ring_for(d, wq);
     a.n_gu = r.n_gu;
     a.n_d = r.n_d;
     a.n_a = r.n_a;
@@ -1855,11 +1932,20 @@ cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const u
         kern<<<num_blocks, kNT, kSmemLimit, stream>>>(a, x);
         return cudaGetLastError();
     };
-    switch (cpt) {
-        case 1: return q8 ? go(k_dense<1, true>) : go(k_dense<1, false>);
-        case 2: return q8 ? go(k_dense<2, true>) : go(k_dense<2, false>);
-        case 4: return q8 ? go(k_dense<4, true>) : go(k_dense<4, false>);
-        default: return q8 ? go(k_dense<8, true>) : go(k_dense<8, false>);
+    if (wq < 0 || wq > 2) return cudaErrorInvalidValue;
+    switch (cpt * 4 + wq) {
+        case 4: return go(k_dense<1, 0>);
+        case 5: return go(k_dense<1, 1>);
+        case 6: return go(k_dense<1, 2>);
+        case 8: return go(k_dense<2, 0>);
+        case 9: return go(k_dense<2, 1>);
+        case 10: return go(k_dense<2, 2>);
+        case 16: return go(k_dense<4, 0>);
+        case 17: return go(k_dense<4, 1>);
+        case 18: return go(k_dense<4, 2>);
+        case 32: return go(k_dense<8, 0>);
+        case 33: return go(k_dense<8, 1>);
+        default: return go(k_dense<8, 2>);
     }
 }
 

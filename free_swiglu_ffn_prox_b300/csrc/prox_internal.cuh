@@ -169,17 +169,23 @@ __device__ __forceinline__ void record_status(int* status, int code) {
 
 // ----------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  All run on `stream`.
-// q8 = 0: gateup/down_t receive the bf16 Stage-2 layouts; q8 = 1: the int8
+// wq = 0: gateup/down_t receive the bf16 Stage-2 layouts; wq = 1: the int8
 // ones (gate|up rows of 2 d + 16 bytes with their scales, W_down^T rows of d
-// bytes), see prox_prepare_q8.
+// bytes), see prox_prepare_q8; wq = 2: the int4 ones (d + 16 and d / 2
+// bytes), see prox_prepare_q4.
 cudaError_t launch_prepare(int d, int F, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
                            const __nv_bfloat16* w_down, uint8_t* codes, __half2* scales,
-                           void* gateup, void* down_t, int q8, float* down_norms,
+                           void* gateup, void* down_t, int wq, float* down_norms,
                            cudaStream_t stream);
 
 // Bytes of one Stage-2 gate|up row and one W_down^T row in device memory.
-constexpr size_t gu_row_bytes(int d, int q8) { return q8 ? (size_t)2 * d + 16 : (size_t)4 * d; }
-constexpr size_t down_row_bytes(int d, int q8) { return q8 ? (size_t)d : (size_t)2 * d; }
+// wq: 0 bf16, 1 int8, 2 int4 (codes, then 16 bytes of row scales).
+constexpr size_t gu_row_bytes(int d, int wq) {
+    return wq == 2 ? (size_t)d + 16 : wq ? (size_t)2 * d + 16 : (size_t)4 * d;
+}
+constexpr size_t down_row_bytes(int d, int wq) {
+    return wq == 2 ? (size_t)d / 2 : wq ? (size_t)d : (size_t)2 * d;
+}
 
 // Proxy work split: `tiles` channel tiles of `tile_w` channels (a multiple
 // of 16) times `slices` slices of the kept inputs, tiles * slices <= blocks.
@@ -191,9 +197,9 @@ ProxyGeom proxy_geometry(int F, int kx, int num_blocks, bool any_width = false);
 struct FusedLaunch {
     const uint8_t* codes;
     const __half2* scales;
-    const void* gateup;  // Stage-2 rows, bf16 or int8 (q8)
+    const void* gateup;  // Stage-2 rows: bf16, int8 or int4 (wq)
     const void* down_t;
-    int q8 = 0;
+    int wq = 0;
     int d, F;
     const uint16_t* x;
     float* y;
@@ -247,7 +253,7 @@ int fused_max_chunk();
 int fused_max_blocks();
 size_t fused_smem_bytes();
 cudaError_t launch_fused(const FusedLaunch& L, cudaStream_t stream);
-// The stack launch: layers[l] of the same shape (L.q8 for all), first
+// The stack launch: layers[l] of the same shape (L.wq for all), first
 // layer on x0, layer l > 0 on x_l = bf16(RMSNorm(x_{l-1} + y_{l-1}) / eps).
 cudaError_t launch_stack(const FusedLaunch& L, const StackLayers& sl, cudaStream_t stream);
 
@@ -288,7 +294,7 @@ cudaError_t union_configure();
 cudaError_t launch_union(const void* gateup, const void* down_t, const uint16_t* x,
                          const uint32_t* member, float* GU, float* y, int d, int F, int G,
                          int num_blocks, int* status, long long limit_ns, cudaStream_t stream);
-cudaError_t launch_dense(const void* gateup, const void* down_t, int q8, const uint16_t* x, int d,
+cudaError_t launch_dense(const void* gateup, const void* down_t, int wq, const uint16_t* x, int d,
                          int F, float* y, int* status, int num_blocks, long long limit_ns,
                          uint64_t* ts, cudaStream_t stream);
 
@@ -304,8 +310,8 @@ struct prox_layer {
     int device, num_sms, num_blocks;
     const uint8_t* codes;
     const __half2* scales;
-    const void* gateup;  // bf16 layouts, or the int8 ones when q8 is set
+    const void* gateup;  // bf16 layouts, or the int8 / int4 ones (wq 1 / 2)
     const void* down_t;
-    int q8;
+    int wq;
     prox::Workspace ws;
 };

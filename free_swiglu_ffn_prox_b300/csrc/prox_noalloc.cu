@@ -110,7 +110,7 @@ extern "C" PROX_API prox_status prox_ffn_noalloc(const prox_layer* layer, const 
     f.scales = layer->scales;
     f.gateup = layer->gateup;
     f.down_t = layer->down_t;
-    f.q8 = layer->q8;
+    f.wq = layer->wq;
     f.d = layer->d_model;
     f.F = layer->d_ff;
     f.x = static_cast<const uint16_t*>(x);

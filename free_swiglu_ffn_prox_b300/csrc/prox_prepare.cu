@@ -6,9 +6,10 @@
 //   * the int4 group-128 symmetric proxy, packed input-dim-major so that one
 //     kept input dimension is one contiguous row of d_ff bytes;
 //   * the channel-interleaved gate|up rows and the channel-major W_down^T,
-//     either as bf16 copies or quantized to int8 per row (symmetric, one fp32
-//     scale amax / 127 per row; the scales travel at the end of each gate|up
-//     row so that one bulk copy brings a channel's codes and scales).
+//     either as bf16 copies or quantized per row to int8 or int4 (symmetric,
+//     one fp32 scale amax / 127 or amax / 7 per row; the scales travel at the
+//     end of each gate|up row so that one bulk copy brings a channel's codes
+//     and scales).
 #include "prox_internal.cuh"
 
 namespace prox {
@@ -66,19 +67,37 @@ k_transpose(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ d
     }
 }
 
-// int8 code of w on a row with scale s: round-to-nearest-even of the binary32
-// quotient w / s, clamped to [-127, 127]; 0 on an all-zero row.
-__device__ __forceinline__ int8_t q8_code(float w, float s) {
+// Row codes: int8 (WQ = 1) = round-to-nearest-even of the binary32 quotient
+// w / s clamped to [-127, 127] with s = amax / 127; int4 (WQ = 2) the same
+// with s = amax / 7, clamped to [-8, 7].  0 on an all-zero row.
+template <int WQ>
+__device__ __forceinline__ int row_code(float w, float s) {
     if (s == 0.0f) return 0;
-    return (int8_t)min(127, max(-127, __float2int_rn(__fdiv_rn(w, s))));
+    const int q = __float2int_rn(__fdiv_rn(w, s));
+    return WQ == 2 ? min(7, max(-8, q)) : min(127, max(-127, q));
+}
+template <int WQ>
+__device__ __forceinline__ float row_scale(float amax) {
+    return __fdiv_rn(amax, WQ == 2 ? 7.0f : 127.0f);
 }
 
-// One CTA per channel c: the int8 gate and up rows of c and their scales,
-// row c of the output = q_gate[c][0..d) | q_up[c][0..d) | s_gate s_up s_down 0
-// (s_down is written by k_q8_down).
+// int4 word of 8 consecutive codes (offset binary n = q + 8): element
+// 2 j + h in bits 16 h + 4 j.
+__device__ __forceinline__ uint32_t pack_q4(const int* q) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w |= (uint32_t)(q[e] + 8) << (16 * (e & 1) + 4 * (e >> 1));
+    return w;
+}
+
+// One CTA per channel c: the gate and up codes of c and their scales, row c
+// of the output = codes of gate | codes of up | s_gate s_up s_down 0
+// (int8: 2 d bytes of codes, int4: d bytes; s_down is written by
+// k_rowq_down).
+template <int WQ>
 __global__ void __launch_bounds__(256)
-k_q8_gateup(const __nv_bfloat16* __restrict__ w_gate, const __nv_bfloat16* __restrict__ w_up,
-            uint8_t* __restrict__ out, int d) {
+k_rowq_gateup(const __nv_bfloat16* __restrict__ w_gate, const __nv_bfloat16* __restrict__ w_up,
+              uint8_t* __restrict__ out, int d) {
     __shared__ float red[2][8];
     const int c = blockIdx.x, tid = threadIdx.x;
     const __nv_bfloat16* rg = w_gate + (size_t)c * d;
@@ -103,28 +122,45 @@ k_q8_gateup(const __nv_bfloat16* __restrict__ w_gate, const __nv_bfloat16* __res
         mg = fmaxf(mg, red[0][w]);
         mu = fmaxf(mu, red[1][w]);
     }
-    const float sg = __fdiv_rn(mg, 127.0f), su = __fdiv_rn(mu, 127.0f);
-    uint8_t* row = out + (size_t)c * gu_row_bytes(d, 1);
-    int8_t* qg = reinterpret_cast<int8_t*>(row);
-    int8_t* qu = qg + d;
-    for (int j = tid; j < d; j += 256) {
-        qg[j] = q8_code(__bfloat162float(rg[j]), sg);
-        qu[j] = q8_code(__bfloat162float(ru[j]), su);
+    const float sg = row_scale<WQ>(mg), su = row_scale<WQ>(mu);
+    uint8_t* row = out + (size_t)c * gu_row_bytes(d, WQ);
+    if constexpr (WQ == 2) {
+        uint32_t* qg = reinterpret_cast<uint32_t*>(row);
+        uint32_t* qu = qg + d / 8;
+        for (int ch = tid; ch < d / 8; ch += 256) {
+            int cg[8], cu[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                cg[e] = row_code<WQ>(__bfloat162float(rg[8 * ch + e]), sg);
+                cu[e] = row_code<WQ>(__bfloat162float(ru[8 * ch + e]), su);
+            }
+            qg[ch] = pack_q4(cg);
+            qu[ch] = pack_q4(cu);
+        }
+    } else {
+        int8_t* qg = reinterpret_cast<int8_t*>(row);
+        int8_t* qu = qg + d;
+        for (int j = tid; j < d; j += 256) {
+            qg[j] = (int8_t)row_code<WQ>(__bfloat162float(rg[j]), sg);
+            qu[j] = (int8_t)row_code<WQ>(__bfloat162float(ru[j]), su);
+        }
     }
     if (tid == 0) {
-        float* t = reinterpret_cast<float*>(row + (size_t)2 * d);
+        float* t = reinterpret_cast<float*>(row + gu_row_bytes(d, WQ) - 16);
         t[0] = sg;
         t[1] = su;
         t[3] = 0.0f;
     }
 }
 
-// W_down [d][F] -> int8 W_down^T [F][d], one scale per channel (a column of
-// W_down): 32 channels per CTA, the column maxima first, then 32 x 32 tiles
-// through shared memory.  s_down[c] goes to the scale slot of gate|up row c.
+// W_down [d][F] -> W_down^T codes [F][down_row_bytes], one scale per channel
+// (a column of W_down): 32 channels per CTA, the column maxima first, then
+// 32 x 32 tiles through shared memory.  s_down[c] goes to the scale slot of
+// gate|up row c.
+template <int WQ>
 __global__ void __launch_bounds__(256)
-k_q8_down(const __nv_bfloat16* __restrict__ w_down, int8_t* __restrict__ down_q8,
-          uint8_t* __restrict__ gateup_q8, int d, int F) {
+k_rowq_down(const __nv_bfloat16* __restrict__ w_down, uint8_t* __restrict__ down_q,
+            uint8_t* __restrict__ gateup_q, int d, int F) {
     __shared__ float tile[32][33];
     __shared__ float red[8][32];
     __shared__ float sc[32];
@@ -139,20 +175,32 @@ k_q8_down(const __nv_bfloat16* __restrict__ w_down, int8_t* __restrict__ down_q8
     if (ty == 0) {
         float m = red[0][tx];
         for (int j = 1; j < 8; ++j) m = fmaxf(m, red[j][tx]);
-        const float sd = __fdiv_rn(m, 127.0f);
+        const float sd = row_scale<WQ>(m);
         sc[tx] = sd;
         if (c < F)
-            *reinterpret_cast<float*>(gateup_q8 + (size_t)c * gu_row_bytes(d, 1) + (size_t)2 * d +
-                                      8) = sd;
+            *reinterpret_cast<float*>(gateup_q + (size_t)c * gu_row_bytes(d, WQ) +
+                                      gu_row_bytes(d, WQ) - 8) = sd;
     }
     __syncthreads();
     for (int r0 = 0; r0 < d; r0 += 32) {  // d is a multiple of 128
         for (int i = ty; i < 32; i += 8)
             tile[i][tx] = c < F ? __bfloat162float(w_down[(size_t)(r0 + i) * F + c]) : 0.0f;
         __syncthreads();
-        for (int i = ty; i < 32; i += 8) {
-            const int cc = c0 + i;
-            if (cc < F) down_q8[(size_t)cc * d + r0 + tx] = q8_code(tile[tx][i], sc[i]);
+        if constexpr (WQ == 2) {
+            // 32 channels x 4 words of 8 codes: thread t < 128 packs word
+            // t & 3 of channel c0 + (t >> 2)
+            const int t = threadIdx.x, i = t >> 2, wd = t & 3, cc = c0 + i;
+            if (t < 128 && cc < F) {
+                int q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q[e] = row_code<WQ>(tile[8 * wd + e][i], sc[i]);
+                reinterpret_cast<uint32_t*>(down_q + (size_t)cc * (d / 2))[(r0 / 8) + wd] = pack_q4(q);
+            }
+        } else {
+            for (int i = ty; i < 32; i += 8) {
+                const int cc = c0 + i;
+                if (cc < F) down_q[(size_t)cc * d + r0 + tx] = (uint8_t)row_code<WQ>(tile[tx][i], sc[i]);
+            }
         }
         __syncthreads();
     }
@@ -179,7 +227,7 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_prepare(int d, int F, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
                            const __nv_bfloat16* w_down, uint8_t* codes, __half2* scales,
-                           void* gateup, void* down_t, int q8, float* down_norms,
+                           void* gateup, void* down_t, int wq, float* down_norms,
                            cudaStream_t stream) {
     const int Fp = padded_ff(F);
     const int G = d / kGroup;
@@ -188,12 +236,20 @@ cudaError_t launch_prepare(int d, int F, const __nv_bfloat16* w_gate, const __nv
     k_quantize_pack<<<qgrid, 128, 0, stream>>>(w_gate, w_up, codes, scales, d, F, Fp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (q8) {
-        k_q8_gateup<<<F, 256, 0, stream>>>(w_gate, w_up, static_cast<uint8_t*>(gateup), d);
+    if (wq == 1) {
+        k_rowq_gateup<1><<<F, 256, 0, stream>>>(w_gate, w_up, static_cast<uint8_t*>(gateup), d);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        k_q8_down<<<(F + 31) / 32, 256, 0, stream>>>(w_down, static_cast<int8_t*>(down_t),
-                                                     static_cast<uint8_t*>(gateup), d, F);
+        k_rowq_down<1><<<(F + 31) / 32, 256, 0, stream>>>(w_down, static_cast<uint8_t*>(down_t),
+                                                          static_cast<uint8_t*>(gateup), d, F);
+        return cudaGetLastError();
+    }
+    if (wq == 2) {
+        k_rowq_gateup<2><<<F, 256, 0, stream>>>(w_gate, w_up, static_cast<uint8_t*>(gateup), d);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        k_rowq_down<2><<<(F + 31) / 32, 256, 0, stream>>>(w_down, static_cast<uint8_t*>(down_t),
+                                                          static_cast<uint8_t*>(gateup), d, F);
         return cudaGetLastError();
     }
     // gate|up interleave: two strided 2-D copies into the [F][2][d] rows

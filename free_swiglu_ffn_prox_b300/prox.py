@@ -62,6 +62,9 @@ def _load():
             "prox_query_sizes_q8": (i32, [i32, i32, ctypes.POINTER(_Sizes)]),
             "prox_prepare_q8": (i32, [i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.POINTER(vp)]),
+            "prox_query_sizes_q4": (i32, [i32, i32, ctypes.POINTER(_Sizes)]),
+            "prox_prepare_q4": (i32, [i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      ctypes.POINTER(vp)]),
             "prox_ffn": (i32, [vp, vp, f32, vp, vp]),
             "prox_ffn_ex": (i32, [vp, vp, f32, f32, vp, vp]),
             "prox_ffn_host": (i32, [vp, vp, f32, vp, vp]),
@@ -138,10 +141,16 @@ def prox_keep_count(n: int, frac: float) -> int:
     return int(_load().prox_keep_count(int(n), float(frac)))
 
 
-def prox_query_sizes(d_model: int, d_ff: int, q8: bool = False) -> dict:
-    """Buffer sizes for prox_prepare (q8: for prox_prepare_q8)."""
+_PREPARE_SUFFIX = {0: "", 1: "_q8", 2: "_q4"}
+
+
+def prox_query_sizes(d_model: int, d_ff: int, q8: bool = False, q4: bool = False) -> dict:
+    """Buffer sizes for prox_prepare (q8: for prox_prepare_q8, q4: for
+    prox_prepare_q4)."""
+    if q8 and q4:
+        raise ValueError("q8 and q4 are exclusive")
     s = _Sizes()
-    name = "prox_query_sizes_q8" if q8 else "prox_query_sizes"
+    name = "prox_query_sizes" + _PREPARE_SUFFIX[2 if q4 else 1 if q8 else 0]
     _check(getattr(_load(), name)(int(d_model), int(d_ff), ctypes.byref(s)), name)
     return {n: int(getattr(s, n)) for n, _ in _Sizes._fields_}
 
@@ -150,9 +159,11 @@ class ProxLayer:
     """A prepared layer: the device buffers (owned here, as torch tensors)
     and the library's host handle."""
 
-    def __init__(self, d_model, d_ff, bufs, handle, device, q8=False):
+    def __init__(self, d_model, d_ff, bufs, handle, device, wq=0):
         self.d_model, self.d_ff = int(d_model), int(d_ff)
-        self.q8 = bool(q8)
+        self.wq = int(wq)  # Stage-2 rows: 0 bf16, 1 int8, 2 int4
+        self.q8 = self.wq == 1
+        self.q4 = self.wq == 2
         self.bufs = bufs
         self.handle = handle
         self.device = device
@@ -169,7 +180,7 @@ class ProxLayer:
             pass
 
 
-def _prepare(w_gate, w_up, w_down, stream, q8):
+def _prepare(w_gate, w_up, w_down, stream, wq):
     lib = _load()
     if w_gate.dim() != 2:
         raise ValueError("w_gate must be [d_ff, d_model]")
@@ -177,24 +188,24 @@ def _prepare(w_gate, w_up, w_down, stream, q8):
     for t, shp, nm in ((w_gate, (d_ff, d_model), "w_gate"), (w_up, (d_ff, d_model), "w_up"),
                        (w_down, (d_model, d_ff), "w_down")):
         _need(t, torch.bfloat16, shp, nm)
-    sz = prox_query_sizes(d_model, d_ff, q8)
+    sz = prox_query_sizes(d_model, d_ff, q8=wq == 1, q4=wq == 2)
     dev = w_gate.device
     bufs = {n: torch.empty(sz[n], dtype=torch.uint8, device=dev) for n in sz}
     h = ctypes.c_void_p()
-    name = "prox_prepare_q8" if q8 else "prox_prepare"
+    name = "prox_prepare" + _PREPARE_SUFFIX[wq]
     with torch.cuda.device(dev):
         _check(getattr(lib, name)(d_model, d_ff, _ptr(w_gate), _ptr(w_up), _ptr(w_down),
                                   _ptr(bufs["proxy_codes"]), _ptr(bufs["proxy_scales"]),
                                   _ptr(bufs["gateup"]), _ptr(bufs["down_t"]),
                                   _ptr(bufs["workspace"]), _stream(stream), ctypes.byref(h)),
                name)
-    return ProxLayer(d_model, d_ff, bufs, h, dev, q8)
+    return ProxLayer(d_model, d_ff, bufs, h, dev, wq)
 
 
 def prox_prepare(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
                  stream=None) -> ProxLayer:
     """Builds the proxy and Stage-2 layouts of one layer (see prox.h)."""
-    return _prepare(w_gate, w_up, w_down, stream, False)
+    return _prepare(w_gate, w_up, w_down, stream, 0)
 
 
 def prox_prepare_q8(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
@@ -202,7 +213,14 @@ def prox_prepare_q8(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tens
     """As prox_prepare with int8 Stage-2 rows (see prox.h); every step call on
     the returned layer runs Stage 2 on them.  bufs["gateup"] and
     bufs["down_t"] hold the int8 layouts."""
-    return _prepare(w_gate, w_up, w_down, stream, True)
+    return _prepare(w_gate, w_up, w_down, stream, 1)
+
+
+def prox_prepare_q4(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
+                    stream=None) -> ProxLayer:
+    """As prox_prepare with int4 Stage-2 rows (see prox.h); bufs["gateup"]
+    and bufs["down_t"] hold the int4 layouts."""
+    return _prepare(w_gate, w_up, w_down, stream, 2)
 
 
 def _x_y(layer: ProxLayer, x, y):

@@ -1,7 +1,8 @@
 /*
  * prox.h -- C ABI of libprox: two-stage sparse SwiGLU FFN decode (batch 1;
  * prox_ffn_batch runs a batch token by token) on NVIDIA B300 (sm_103a).
- * Variants of the same step: int8 Stage-2 rows (prox_prepare_q8), block-
+ * Variants of the same step: int8 or int4 Stage-2 rows (prox_prepare_q8,
+ * prox_prepare_q4), block-
  * granular channel masks (prox_ffn_blocks), and the residual + RMSNorm glue
  * of a layer stack fused in front of the step (prox_ffn_resnorm).
  *
@@ -109,6 +110,15 @@ typedef struct prox_layer prox_layer;
  *                int8 q_up[c][0..d), then fp32 s_gate[c], s_up[c],
  *                s_down[c] and 4 zero bytes.
  *   down_q8      int8 [F][d]: row c = q_down[c][:], the codes of W_down[:][c].
+ * prox_prepare_q4 writes int4 Stage-2 layouts the same way with
+ * s_r = fl32(max_j |r_j| / 7) and q_r[j] = clamp(rne(fl32(r_j / s_r)), -8, 7),
+ * packed as offset-binary nibbles n = q + 8, eight consecutive elements
+ * 8 i .. 8 i + 7 per little-endian 32-bit word i, element 8 i + 2 m + h in
+ * bits 16 h + 4 m (m = 0..3, h = 0..1):
+ *   gateup_q4    [F] rows of d + 16 bytes: d / 8 words of q_gate[c],
+ *                d / 8 words of q_up[c], then fp32 s_gate[c], s_up[c],
+ *                s_down[c] and 4 zero bytes.
+ *   down_q4      [F] rows of d / 2 bytes: the words of q_down[c][:].
  */
 
 /* Sizes of the buffers above for a layer shape.  Host only; queues nothing.
@@ -118,6 +128,10 @@ PROX_API prox_status prox_query_sizes(int d_model, int d_ff, prox_sizes* out);
 /* As prox_query_sizes for prox_prepare_q8: gateup and down_t hold the sizes
  * of gateup_q8 (d_ff * (2 d_model + 16)) and down_q8 (d_ff * d_model). */
 PROX_API prox_status prox_query_sizes_q8(int d_model, int d_ff, prox_sizes* out);
+
+/* As prox_query_sizes for prox_prepare_q4: gateup and down_t hold the sizes
+ * of gateup_q4 (d_ff * (d_model + 16)) and down_q4 (d_ff * d_model / 2). */
+PROX_API prox_status prox_query_sizes_q4(int d_model, int d_ff, prox_sizes* out);
 
 /*
  * One-off per-layer preparation ("Prox", Abstract: quantized proxy weights
@@ -152,6 +166,18 @@ PROX_API prox_status prox_prepare(int d_model, int d_ff, const void* w_gate, con
 PROX_API prox_status prox_prepare_q8(int d_model, int d_ff, const void* w_gate, const void* w_up,
                             const void* w_down, void* proxy_codes, void* proxy_scales,
                             void* gateup_q8, void* down_q8, void* workspace,
+                            prox_stream_t stream, prox_layer** out);
+
+/*
+ * As prox_prepare_q8 with int4 Stage-2 rows (a quarter of the bf16 bytes per
+ * channel): gateup_q4 and down_q4 (sizes from prox_query_sizes_q4) receive
+ * the int4 layouts above.  The same entry points run on the layer, with the
+ * same sums over the int4 codes; the channel mask is again the bf16 layer's.
+ * Errors as prox_prepare.
+ */
+PROX_API prox_status prox_prepare_q4(int d_model, int d_ff, const void* w_gate, const void* w_up,
+                            const void* w_down, void* proxy_codes, void* proxy_scales,
+                            void* gateup_q4, void* down_q4, void* workspace,
                             prox_stream_t stream, prox_layer** out);
 
 /*
@@ -252,15 +278,15 @@ PROX_API prox_status prox_ffn_batch(const prox_layer* layer, const void* x, int 
  * group of CTAs per token.  x bf16 [batch][d_model], y fp32 [batch][d_model] (device, 16-byte
  * aligned, not overlapping); keep fraction as in prox_ffn.  The same masks
  * as prox_ffn per token; y[t] equals prox_ffn's up to the order of the fp32
- * additions.  Layers prepared with int8 Stage-2 rows (prox_prepare_q8) are
- * not supported (PROX_ERR_UNSUPPORTED_SHAPE).  Uses the layer's workspace.
+ * additions.  Layers prepared with int8 or int4 Stage-2 rows
+ * (prox_prepare_q8, _q4) are not supported (PROX_ERR_UNSUPPORTED_SHAPE).  Uses the layer's workspace.
  */
 PROX_API prox_status prox_ffn_batch_union(const prox_layer* layer, const void* x, int batch,
                                  float keep_fraction, float* y, prox_stream_t stream);
 
 /* Tokens per pass of prox_ffn_batch_union on this layer (their x fit in a
  * CTA's shared memory next to the gate|up ring): 8 up to d_model 4096,
- * fewer above; 0 for a null or int8 layer. */
+ * fewer above; 0 for a null, int8 or int4 layer. */
 PROX_API int prox_batch_union_group(const prox_layer* layer);
 
 /* prox_ffn_batch_union plus, for batch <= prox_batch_union_group(),

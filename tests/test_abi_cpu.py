@@ -59,9 +59,9 @@ def test_query_sizes(lib):
     s = prox.prox_query_sizes(256, 688)  # ragged d_ff: padded to 704 proxy columns
     assert s["proxy_codes"] == 256 * 704 and s["proxy_scales"] == 2 * 704 * 4
     for d, F in ((100, 64), (0, 64), (256, 0), (16384 + 128, 64), (256, 32769)):
-        for q8 in (False, True):
+        for q8, q4 in ((False, False), (True, False), (False, True)):
             with pytest.raises(prox.ProxError) as e:
-                prox.prox_query_sizes(d, F, q8)
+                prox.prox_query_sizes(d, F, q8, q4)
             assert e.value.code == prox.PROX_ERR_UNSUPPORTED_SHAPE
 
 
@@ -97,6 +97,22 @@ def test_status_strings(lib):
     assert prox.prox_status_string(99) == "unknown status"
 
 
+def test_query_sizes_q4(lib):
+    """int4 Stage-2 rows: d / 2 bytes of gate and of up codes plus 16 bytes
+    of scales per channel, d / 2 bytes of W_down^T codes; the proxy and the
+    workspace are those of the bf16 layer."""
+    from free_swiglu_ffn_prox_b300 import prox
+
+    for d, F in ((4096, 14336), (256, 688), (8192, 28672)):
+        s, s4 = prox.prox_query_sizes(d, F), prox.prox_query_sizes(d, F, q4=True)
+        assert s4["gateup"] == F * (d + 16)
+        assert s4["down_t"] == F * d // 2
+        for n in ("proxy_codes", "proxy_scales", "workspace"):
+            assert s4[n] == s[n]
+    with pytest.raises(ValueError):
+        prox.prox_query_sizes(256, 688, q8=True, q4=True)
+
+
 def test_bad_arguments_are_rejected_before_any_device_work(lib):
     vp = ctypes.c_void_p
     h = vp()
@@ -121,6 +137,15 @@ def test_bad_arguments_are_rejected_before_any_device_work(lib):
     args[6] = vp(0x10004)
     assert lib.prox_prepare_q8(256, 64, *args, None, ctypes.byref(h)) == 3
     assert lib.prox_prepare_q8(256, 64, *good, None, None) == 1
+    # and the int4 one
+    assert lib.prox_prepare_q4(100, 64, *good, None, ctypes.byref(h)) == 2
+    args = list(good)
+    args[5] = None
+    assert lib.prox_prepare_q4(256, 64, *args, None, ctypes.byref(h)) == 1
+    args = list(good)
+    args[5] = vp(0x10008)
+    assert lib.prox_prepare_q4(256, 64, *args, None, ctypes.byref(h)) == 3
+    assert lib.prox_prepare_q4(256, 64, *good, None, None) == 1
     # calls on a null layer
     assert lib.prox_ffn(None, good[0], ctypes.c_float(0.3), good[1], None) == 1
     assert lib.prox_ffn_ex(None, good[0], ctypes.c_float(0.3), ctypes.c_float(0.5), good[1], None) == 1

@@ -1,6 +1,6 @@
 """The roofline numerator: bench.py's algorithmic bytes per step must be the
 bytes of the library's own layouts that the step reads (sizes from
-prox_query_sizes / prox_query_sizes_q8), plus x, y and the lists.  Host only."""
+prox_query_sizes / _q8 / _q4), plus x, y and the lists.  Host only."""
 import os
 import sys
 
@@ -25,16 +25,17 @@ def test_step_bytes_are_the_layout_bytes_the_step_reads(prox, d, F, rho):
     import bench
 
     kx, k = prox.prox_keep_count(d, 0.5), prox.prox_keep_count(F, rho)
-    for q8, fn in ((False, bench.algorithmic_bytes), (True, bench.algorithmic_bytes_q8)):
-        sz = prox.prox_query_sizes(d, F, q8=q8)
+    for wq, fn in ((0, bench.algorithmic_bytes), (1, bench.algorithmic_bytes_q8),
+                   (2, bench.algorithmic_bytes_q4)):
+        sz = prox.prox_query_sizes(d, F, q8=wq == 1, q4=wq == 2)
         Fp = sz["proxy_codes"] // d            # proxy row length (padded channels)
         assert Fp == F  # these shapes need no padding, so the kept rows are F bytes
         proxy = kx * Fp + sz["proxy_scales"]   # kept proxy rows + every scale
         stage2 = k * (sz["gateup"] // F + sz["down_t"] // F)  # selected rows
         io = 2 * d + 4 * d + 4 * k             # x bf16, y fp32, channel list int32
-        assert fn(d, F, k, kx)["step"] == proxy + stage2 + io, (q8, d, F, rho)
+        assert fn(d, F, k, kx)["step"] == proxy + stage2 + io, (wq, d, F, rho)
         dense = sz["gateup"] + sz["down_t"] + 2 * d + 4 * d
-        assert fn(d, F, k, kx)["dense"] == dense, (q8, d, F)
+        assert fn(d, F, k, kx)["dense"] == dense, (wq, d, F)
 
 
 def test_headline_bytes(prox):
