@@ -58,6 +58,7 @@ constexpr int kGuProducerWarp = 16;
 constexpr int kDProducerWarp = 17;
 constexpr int kSelectorWarp = 18;
 constexpr int kMaxStages = 16;
+constexpr int kPassBStep = 2;             // pass-B items per step (4 starved the 6-stage bf16 ring)
 constexpr size_t kGuRingBytes = 112 * 1024;   // gate|up bytes in flight per SM (bf16)
 constexpr size_t kGuRingBytesQ = 136 * 1024;  // ... (int8 rows: 16 stages at d = 4096; int4)
 constexpr size_t kDRingBytes = 48 * 1024;     // W_down^T bytes in flight per SM
@@ -432,26 +433,32 @@ __device__ __forceinline__ bool warp_wait_flag(const uint8_t* flag, long long li
     return __all_sync(0xffffffffu, got);
 }
 
-// Stage-2 roles of warps 0..17 over the CTA's items ctl.item[0..n_items).
-// Items [0, m) are known when the roles start; the rest (ctl.n_items, their
-// channels and ctl.conf of every item) only once ctl.sel_bar completes.
+// Stage-2 roles of warps 0..17 over the CTA's items ctl.item[0..n), every
+// item final when the roles start (the decode step resolves the exact mask
+// first; the dense pass takes every channel of its chunk).
 // Shared area: x as bf16 (2 d bytes), then n_gu gate|up stages and n_d
 // W_down^T stages, one row each (bf16: 4 d and 2 d bytes; int8: the codes
 // 2 d + 16 bytes with the row's scales s_gate, s_up, s_down, and d bytes;
 // int4: d + 16 and d / 2 bytes); for codes, x once more as fp32 after the
 // rings (4 d bytes).
-//   GU producer (warp 16) / D producer (warp 17): lane 0 issues one bulk copy
-//       per item into the next stage of its ring;
+//   GU producer (warp 16) / D producer (warp 17): the whole warp issues, in
+//       rounds of W = min(32, stages) items (distinct stages): lane j waits
+//       until the stage of item r W + j is free and issues its bulk copy;
 //   pass A (warp w < n_a, n_a dividing n_gu): the items i = w (mod n_a); item
 //       i sits in gate|up stage i mod n_gu, whose items are all = w (mod
 //       n_a), so one warp consumes each stage's uses in order (a parity wait
 //       is never taken two uses ahead): g, u over the whole row,
 //       h = silu(g) u, then ctl.hready[i] (codes: g and u times the row
 //       scales, and ctl.h[i] = h s_down, the factor of the W_down^T codes);
-//   pass B (warps 8..15): every thread owns 8-element slices of d and, for
-//       each confirmed item in order, adds h * W_down^T[c, slice].
+//   pass B (warps 8..15): every thread owns 8-element slices of d and adds
+//       h * W_down^T[c, slice] for the items in order, kPassBStep per
+//       step: the waits for their stages and flags, then the rows.  With
+//       one item per step the chain of waits and index arithmetic measured
+//       ~0.45 us per item, which set the pace of Stage 2 once the rows were
+//       int8 or int4 (two per step: the int8 dense pass 59.6 -> 48.6 us).
+// Stages and their phase parities advance by counters (no division).
 template <int CPT, int WQ>
-__device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m) {
+__device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int n) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = a.d, n_gu = a.n_gu, n_d = a.n_d, n_a = a.n_a;
     const size_t gu_bytes = gu_row_bytes(d, WQ), d_bytes = down_row_bytes(d, WQ);
@@ -461,9 +468,12 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
     const int nchunk = d / 8;  // 8-element chunks per row (16 bytes bf16, 8 int8, 4 int4)
 
     if (warp == kGuProducerWarp || warp == kDProducerWarp) {
-        if (lane != 0) return;
+        // The whole warp issues: in round r, lane j takes item r W + j
+        // (W = min(32, stages), so a round's items use distinct stages),
+        // waits until its stage is free and issues the bulk copy.
         const bool gu = warp == kGuProducerWarp;
         const int ns = gu ? n_gu : n_d;
+        const int W = ns < 32 ? ns : 32;
         const size_t sb = gu ? gu_bytes : d_bytes;
         uint64_t* full = gu ? ctl.gu_full : ctl.d_full;
         uint64_t* empty = gu ? ctl.gu_empty : ctl.d_empty;
@@ -479,27 +489,26 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
             }
             return false;
         };
-        bool known = false;
-        for (int i = 0;; ++i) {
-            if (i >= m) {
-                if (!known) {
-                    if (!wait(&ctl.sel_bar, 0)) break;
-                    known = true;
+        for (int i0 = 0; i0 < n; i0 += W) {
+            const int i = i0 + lane;
+            bool ok = true;
+            if (lane < W && i < n) {
+                const int s = i % ns;
+                if (i >= ns) ok = wait(&empty[s], ((i / ns) - 1) & 1);
+                if (ok && !*reinterpret_cast<volatile int*>(&ctl.abort)) {
+                    const int c = ctl.item[i];
+                    if (c < 0 || c >= a.F) {  // never expected: the lists hold chunk channels
+                        record_status(a.status, PROX_ERR_DEVICE_CHECK);
+                        ctl.abort = 1;
+                        ok = false;
+                    } else {
+                        last[s] = i;
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)sb);
+                        bulk_g2s(base + (size_t)s * sb, src + (size_t)c * sb, (uint32_t)sb, &full[s], pol);
+                    }
                 }
-                if (i >= ctl.n_items) break;
             }
-            const int s = i % ns;
-            if (i >= ns && !wait(&empty[s], ((i / ns) - 1) & 1)) break;
-            if (ctl.abort) break;
-            const int c = ctl.item[i];
-            if (c < 0 || c >= a.F) {  // never expected: the lists hold chunk channels
-                record_status(a.status, PROX_ERR_DEVICE_CHECK);
-                ctl.abort = 1;
-                break;
-            }
-            last[s] = i;
-            mbar_arrive_expect_tx(&full[s], (uint32_t)sb);
-            bulk_g2s(base + (size_t)s * sb, src + (size_t)c * sb, (uint32_t)sb, &full[s], pol);
+            if (!__all_sync(0xffffffffu, ok) || *reinterpret_cast<volatile int*>(&ctl.abort)) break;
         }
         return;
     }
@@ -523,17 +532,10 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
             }
             named_barrier_sync(2, n_a * 32);  // warps 0 .. n_a - 1, each once
         }
-        bool known = false;
-        for (int i = warp;; i += n_a) {
-            const int s = i % n_gu;
-            if (i >= m) {
-                if (!known) {
-                    if (!warp_wait(&ctl.sel_bar, 0, a.limit_ns, ctl, a.status)) break;
-                    known = true;
-                }
-                if (i >= ctl.n_items) break;
-            }
-            if (!warp_wait(&ctl.gu_full[s], (i / n_gu) & 1, a.limit_ns, ctl, a.status)) break;
+        int s = warp;      // stage of item i
+        uint32_t ph = 0;   // its phase parity
+        for (int i = warp; i < n; i += n_a) {
+            if (!warp_wait(&ctl.gu_full[s], ph, a.limit_ns, ctl, a.status)) break;
             if (i == 0 && lane == 0) stamp_here(a.ts, 6);
             const uint8_t* st = gu_ring + (size_t)s * gu_bytes;
             float g = 0.0f, u = 0.0f;
@@ -599,33 +601,31 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
                 __threadfence_block();
                 *reinterpret_cast<volatile uint8_t*>(&ctl.hready[i]) = 1;
             }
+            s += n_a;
+            if (s >= n_gu) {
+                s -= n_gu;
+                ph ^= 1u;
+            }
         }
         if (warp == 0 && lane == 0) stamp_here(a.ts, 7);
         return;
     }
 
     // ---------------------------------------------------- pass B: y += h W_down^T
-    // Items [0, m) are known when the roles start.  Both callers pass the
-    // whole list (the decode step resolves the exact mask first; the dense
-    // pass takes every channel), so every item is confirmed.  Were m shorter,
-    // a warp would add the first m tentatively until it sees the list final,
-    // then skip the items dropped from it and take out again those it had
-    // already added (their W_down^T rows read once more from global memory),
-    // each warp for its own slices of y.
     const int t = threadIdx.x - kPassBWarp0 * 32;
     float yp[CPT][8];
 #pragma unroll
     for (int q = 0; q < CPT; ++q)
 #pragma unroll
         for (int e = 0; e < 8; ++e) yp[q][e] = 0.0f;
-    auto add_row = [&](const uint8_t* row, float hv, bool global) {
+    auto add_row = [&](const uint8_t* row, float hv) {
 #pragma unroll
         for (int q = 0; q < CPT; ++q) {
             const int ch = t + q * kPassB;
             if (ch < nchunk) {
                 if constexpr (WQ == 2) {
                     const uint32_t* r4 = reinterpret_cast<const uint32_t*>(row);
-                    const uint32_t dw = global ? __ldg(r4 + ch) : r4[ch];
+                    const uint32_t dw = r4[ch];
                     const uint32_t hi = dw >> 16;
                     const float2 h2 = make_float2(hv, hv);
                     float2 a = __ffma2_rn(h2, q4_pair<0>(dw, hi), make_float2(yp[q][0], yp[q][1]));
@@ -642,7 +642,7 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
                     yp[q][7] = a.y;
                 } else if constexpr (WQ == 1) {
                     const uint2* r8 = reinterpret_cast<const uint2*>(row);
-                    const uint2 dw = global ? __ldg(r8 + ch) : r8[ch];
+                    const uint2 dw = r8[ch];
                     const uint32_t w0 = dw.x ^ 0x80808080u, w1 = dw.y ^ 0x80808080u;
                     const float2 h2 = make_float2(hv, hv);
 #pragma unroll
@@ -656,7 +656,7 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
                     }
                 } else {
                     const uint4* r16 = reinterpret_cast<const uint4*>(row);
-                    const uint4 dw = global ? __ldg(r16 + ch) : r16[ch];
+                    const uint4 dw = r16[ch];
                     const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
                     const float2 h2 = make_float2(hv, hv);
 #pragma unroll
@@ -670,39 +670,48 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int m
             }
         }
     };
-    bool ok = true, known = false;
-    int n = m, first_known = 0;  // items [0, first_known) were added tentatively
-    for (int i = 0; ok; ++i) {
-        if (!known) {
-            if (i >= m) {
-                ok = warp_wait(&ctl.sel_bar, 0, a.limit_ns, ctl, a.status);
-                if (!ok) break;
-                known = true;
-            } else {
-                known = __shfl_sync(0xffffffffu, lane == 0 ? mbar_test_wait(&ctl.sel_bar, 0) : false, 0);
-            }
-            if (known) {
-                n = ctl.n_items;
-                first_known = i;
+    // up to kPassBStep items per step, each in its own stage
+    const int step = n_d < kPassBStep ? n_d : kPassBStep;
+    bool ok = true;
+    int s = 0;         // stage of item i
+    uint32_t ph = 0;   // its phase parity
+    for (int i = 0; i < n; i += step) {
+        const int cnt = n - i < step ? n - i : step;
+        int ss[kPassBStep];
+        uint32_t pp[kPassBStep];
+#pragma unroll
+        for (int j = 0; j < kPassBStep; ++j) {
+            ss[j] = j == 0 ? s : ss[j - 1] + 1;
+            pp[j] = j == 0 ? ph : pp[j - 1];
+            if (ss[j] == n_d) {
+                ss[j] = 0;
+                pp[j] ^= 1u;
             }
         }
-        if (i >= n) break;
-        const int s = i % n_d;
-        ok = warp_wait(&ctl.d_full[s], (i / n_d) & 1, a.limit_ns, ctl, a.status);
+#pragma unroll
+        for (int j = 0; j < kPassBStep; ++j)
+            if (j < cnt && ok) ok = warp_wait(&ctl.d_full[ss[j]], pp[j], a.limit_ns, ctl, a.status);
+#pragma unroll
+        for (int j = 0; j < kPassBStep; ++j)
+            if (j < cnt && ok) ok = warp_wait_flag(&ctl.hready[i + j], a.limit_ns, ctl, a.status);
         if (!ok) break;
-        if (!known || ctl.conf[i]) {
-            ok = warp_wait_flag(&ctl.hready[i], a.limit_ns, ctl, a.status);
-            if (!ok) break;
-            add_row(d_ring + (size_t)s * d_bytes, *reinterpret_cast<const volatile float*>(&ctl.h[i]),
-                    false);
-        }
+#pragma unroll
+        for (int j = 0; j < kPassBStep; ++j)
+            if (j < cnt)
+                add_row(d_ring + (size_t)ss[j] * d_bytes,
+                        *reinterpret_cast<const volatile float*>(&ctl.h[i + j]));
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.d_empty[s]);
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < kPassBStep; ++j)
+                if (j < cnt) mbar_arrive(&ctl.d_empty[ss[j]]);
+        }
+        s += cnt;  // cnt <= n_d: at most one wrap
+        if (s >= n_d) {
+            s -= n_d;
+            ph ^= 1u;
+        }
     }
-    if (ok && known)
-        for (int i = 0; i < first_known; ++i)
-            if (!ctl.conf[i])
-                add_row(a.down_t + (size_t)ctl.item[i] * d_bytes, -ctl.h[i], true);
     if (t == 0) stamp_here(a.ts, 8);
     if (ok && !ctl.abort && n > 0) {
 #pragma unroll
