@@ -58,7 +58,15 @@ constexpr int kGuProducerWarp = 16;
 constexpr int kDProducerWarp = 17;
 constexpr int kSelectorWarp = 18;
 constexpr int kMaxStages = 16;
-constexpr int kPassBStep = 2;             // pass-B items per step (4 starved the 6-stage bf16 ring)
+// 8-element chunks of d per pass-B thread (the kernels' CPT)
+__host__ __device__ constexpr int chunks_per_thread(int d) {
+    return d / 8 <= kPassB ? 1 : d / 8 <= 2 * kPassB ? 2 : d / 8 <= 4 * kPassB ? 4 : 8;
+}
+// Codes: bytes of one item's W_down^T slices over all pass-B threads in the
+// self-streamed slots (CPT chunks of 8 (int8) or 4 (int4) bytes each).
+__host__ __device__ constexpr size_t self_item_bytes(int d, int wq) {
+    return (size_t)chunks_per_thread(d) * (wq == 2 ? 4 : 8) * kPassB;
+}
 constexpr size_t kGuRingBytes = 112 * 1024;   // gate|up bytes in flight per SM (bf16)
 constexpr size_t kGuRingBytesQ = 136 * 1024;  // ... (int8 rows: 16 stages at d = 4096; int4)
 constexpr size_t kDRingBytes = 48 * 1024;     // W_down^T bytes in flight per SM
@@ -329,6 +337,14 @@ __device__ __forceinline__ void cp_async_wait_group() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// 4- or 8-byte global -> shared copy (cp.async through L1), L2 policy hint.
+template <int B>
+__device__ __forceinline__ void cp_async_small(void* dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], %2, %3;" ::"r"(smem_u32(dst)),
+                 "l"(src), "n"(B), "l"(pol)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- stage 2
 
 // int8 weights: a word of four two's-complement codes, flipped to offset
@@ -436,14 +452,15 @@ __device__ __forceinline__ bool warp_wait_flag(const uint8_t* flag, long long li
 // Stage-2 roles of warps 0..17 over the CTA's items ctl.item[0..n), every
 // item final when the roles start (the decode step resolves the exact mask
 // first; the dense pass takes every channel of its chunk).
-// Shared area: x as bf16 (2 d bytes), then n_gu gate|up stages and n_d
-// W_down^T stages, one row each (bf16: 4 d and 2 d bytes; int8: the codes
-// 2 d + 16 bytes with the row's scales s_gate, s_up, s_down, and d bytes;
-// int4: d + 16 and d / 2 bytes); for codes, x once more as fp32 after the
-// rings (4 d bytes).
-//   GU producer (warp 16) / D producer (warp 17): the whole warp issues, in
-//       rounds of W = min(32, stages) items (distinct stages): lane j waits
-//       until the stage of item r W + j is free and issues its bulk copy;
+// Shared area: x as bf16 (2 d bytes), then n_gu gate|up stages, one row
+// each (bf16 4 d bytes; int8: the codes 2 d + 16 bytes with the row's
+// scales s_gate, s_up, s_down; int4 d + 16), then for bf16 n_d W_down^T
+// stages of 2 d bytes, for codes the pass-B slots of n_d items
+// (self_item_bytes each) and x once more as fp32 (4 d bytes).
+//   GU producer (warp 16) / D producer (warp 17, bf16 only): the whole warp
+//       issues, in rounds of W = min(32, stages) items (distinct stages):
+//       lane j waits until the stage of item r W + j is free and issues its
+//       bulk copy;
 //   pass A (warp w < n_a, n_a dividing n_gu): the items i = w (mod n_a); item
 //       i sits in gate|up stage i mod n_gu, whose items are all = w (mod
 //       n_a), so one warp consumes each stage's uses in order (a parity wait
@@ -451,11 +468,9 @@ __device__ __forceinline__ bool warp_wait_flag(const uint8_t* flag, long long li
 //       h = silu(g) u, then ctl.hready[i] (codes: g and u times the row
 //       scales, and ctl.h[i] = h s_down, the factor of the W_down^T codes);
 //   pass B (warps 8..15): every thread owns 8-element slices of d and adds
-//       h * W_down^T[c, slice] for the items in order, kPassBStep per
-//       step: the waits for their stages and flags, then the rows.  With
-//       one item per step the chain of waits and index arithmetic measured
-//       ~0.45 us per item, which set the pace of Stage 2 once the rows were
-//       int8 or int4 (two per step: the int8 dense pass 59.6 -> 48.6 us).
+//       h * W_down^T[c, slice] for the items in order; for bf16 rows from
+//       the W_down^T ring, for codes from slots that each thread fills with
+//       its own slices (see there).
 // Stages and their phase parities advance by counters (no division).
 template <int CPT, int WQ>
 __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int n) {
@@ -467,6 +482,7 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int n
     uint8_t* d_ring = gu_ring + (size_t)n_gu * gu_bytes;
     const int nchunk = d / 8;  // 8-element chunks per row (16 bytes bf16, 8 int8, 4 int4)
 
+    if (WQ != 0 && warp == kDProducerWarp) return;  // codes: pass B streams its own slices
     if (warp == kGuProducerWarp || warp == kDProducerWarp) {
         // The whole warp issues: in round r, lane j takes item r W + j
         // (W = min(32, stages), so a round's items use distinct stages),
@@ -520,7 +536,7 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int n
         // codes: the pass-A warps first write x as fp32 in two planes
         // (elements 0..3 and 4..7 of every 8-element chunk), so that a lane's
         // x loads are consecutive and no row converts x again
-        float4* xfa = reinterpret_cast<float4*>(d_ring + (size_t)n_d * d_bytes);
+        float4* xfa = reinterpret_cast<float4*>(d_ring + (size_t)n_d * self_item_bytes(d, WQ));
         float4* xfb = xfa + nchunk;
         if constexpr (WQ != 0) {
             for (int ch = threadIdx.x; ch < nchunk; ch += n_a * 32) {
@@ -618,98 +634,112 @@ __device__ void stage2_roles(const Stage2Args& a, Ctl& ctl, uint8_t* area, int n
     for (int q = 0; q < CPT; ++q)
 #pragma unroll
         for (int e = 0; e < 8; ++e) yp[q][e] = 0.0f;
+    // y slice q += hv * the 8 weights of the chunk at p (q a constant
+    // after unrolling)
+    auto acc_chunk = [&](int q, const uint8_t* p, float hv) {
+        const float2 h2 = make_float2(hv, hv);
+        if constexpr (WQ == 2) {
+            const uint32_t dw = *reinterpret_cast<const uint32_t*>(p);
+            const uint32_t hi = dw >> 16;
+            float2 a = __ffma2_rn(h2, q4_pair<0>(dw, hi), make_float2(yp[q][0], yp[q][1]));
+            yp[q][0] = a.x;
+            yp[q][1] = a.y;
+            a = __ffma2_rn(h2, q4_pair<1>(dw, hi), make_float2(yp[q][2], yp[q][3]));
+            yp[q][2] = a.x;
+            yp[q][3] = a.y;
+            a = __ffma2_rn(h2, q4_pair<2>(dw, hi), make_float2(yp[q][4], yp[q][5]));
+            yp[q][4] = a.x;
+            yp[q][5] = a.y;
+            a = __ffma2_rn(h2, q4_pair<3>(dw, hi), make_float2(yp[q][6], yp[q][7]));
+            yp[q][6] = a.x;
+            yp[q][7] = a.y;
+        } else if constexpr (WQ == 1) {
+            const uint2 dw = *reinterpret_cast<const uint2*>(p);
+            const uint32_t w0 = dw.x ^ 0x80808080u, w1 = dw.y ^ 0x80808080u;
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                float2 a = __ffma2_rn(h2, q8_pair(w0, e), make_float2(yp[q][e], yp[q][e + 1]));
+                yp[q][e] = a.x;
+                yp[q][e + 1] = a.y;
+                a = __ffma2_rn(h2, q8_pair(w1, e), make_float2(yp[q][4 + e], yp[q][5 + e]));
+                yp[q][4 + e] = a.x;
+                yp[q][5 + e] = a.y;
+            }
+        } else {
+            const uint4 dw = *reinterpret_cast<const uint4*>(p);
+            const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 a = __ffma2_rn(h2, make_float2(__uint_as_float(dv[e] << 16), __uint_as_float(dv[e] & 0xffff0000u)),
+                                            make_float2(yp[q][2 * e], yp[q][2 * e + 1]));
+                yp[q][2 * e] = a.x;
+                yp[q][2 * e + 1] = a.y;
+            }
+        }
+    };
+    constexpr size_t chunk_bytes = WQ == 2 ? 4 : WQ == 1 ? 8 : 16;
     auto add_row = [&](const uint8_t* row, float hv) {
 #pragma unroll
         for (int q = 0; q < CPT; ++q) {
             const int ch = t + q * kPassB;
-            if (ch < nchunk) {
-                if constexpr (WQ == 2) {
-                    const uint32_t* r4 = reinterpret_cast<const uint32_t*>(row);
-                    const uint32_t dw = r4[ch];
-                    const uint32_t hi = dw >> 16;
-                    const float2 h2 = make_float2(hv, hv);
-                    float2 a = __ffma2_rn(h2, q4_pair<0>(dw, hi), make_float2(yp[q][0], yp[q][1]));
-                    yp[q][0] = a.x;
-                    yp[q][1] = a.y;
-                    a = __ffma2_rn(h2, q4_pair<1>(dw, hi), make_float2(yp[q][2], yp[q][3]));
-                    yp[q][2] = a.x;
-                    yp[q][3] = a.y;
-                    a = __ffma2_rn(h2, q4_pair<2>(dw, hi), make_float2(yp[q][4], yp[q][5]));
-                    yp[q][4] = a.x;
-                    yp[q][5] = a.y;
-                    a = __ffma2_rn(h2, q4_pair<3>(dw, hi), make_float2(yp[q][6], yp[q][7]));
-                    yp[q][6] = a.x;
-                    yp[q][7] = a.y;
-                } else if constexpr (WQ == 1) {
-                    const uint2* r8 = reinterpret_cast<const uint2*>(row);
-                    const uint2 dw = r8[ch];
-                    const uint32_t w0 = dw.x ^ 0x80808080u, w1 = dw.y ^ 0x80808080u;
-                    const float2 h2 = make_float2(hv, hv);
-#pragma unroll
-                    for (int e = 0; e < 4; e += 2) {
-                        float2 a = __ffma2_rn(h2, q8_pair(w0, e), make_float2(yp[q][e], yp[q][e + 1]));
-                        yp[q][e] = a.x;
-                        yp[q][e + 1] = a.y;
-                        a = __ffma2_rn(h2, q8_pair(w1, e), make_float2(yp[q][4 + e], yp[q][5 + e]));
-                        yp[q][4 + e] = a.x;
-                        yp[q][5 + e] = a.y;
-                    }
-                } else {
-                    const uint4* r16 = reinterpret_cast<const uint4*>(row);
-                    const uint4 dw = r16[ch];
-                    const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
-                    const float2 h2 = make_float2(hv, hv);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 a = __ffma2_rn(h2, make_float2(__uint_as_float(dv[e] << 16), __uint_as_float(dv[e] & 0xffff0000u)),
-                                                    make_float2(yp[q][2 * e], yp[q][2 * e + 1]));
-                        yp[q][2 * e] = a.x;
-                        yp[q][2 * e + 1] = a.y;
-                    }
-                }
-            }
+            if (ch < nchunk) acc_chunk(q, row + (size_t)ch * chunk_bytes, hv);
         }
     };
-    // up to kPassBStep items per step, each in its own stage
-    const int step = n_d < kPassBStep ? n_d : kPassBStep;
     bool ok = true;
-    int s = 0;         // stage of item i
-    uint32_t ph = 0;   // its phase parity
-    for (int i = 0; i < n; i += step) {
-        const int cnt = n - i < step ? n - i : step;
-        int ss[kPassBStep];
-        uint32_t pp[kPassBStep];
+    if constexpr (WQ != 0) {
+        // Codes: thread t copies its own chunks of each item's W_down^T row
+        // (cp.async of 8 or 4 bytes) n_d items ahead into its slots and
+        // waits only for its own copies (one cp.async group per item), so
+        // no stage barriers and no producer warp are involved.  Slot (k, q)
+        // of thread t: d_ring + ((k CPT + q) kPassB + t) cb bytes.
+        constexpr int cb = WQ == 2 ? 4 : 8;
+        const int K = n_d;  // 2, 4 or 8
+        const uint64_t pol = policy_evict_first();
+        auto slot = [&](int k, int q) { return d_ring + ((size_t)(k * CPT + q) * kPassB + t) * cb; };
+        auto issue = [&](int i, int k) {
+            const uint8_t* row = a.down_t + (size_t)ctl.item[i] * d_bytes;
 #pragma unroll
-        for (int j = 0; j < kPassBStep; ++j) {
-            ss[j] = j == 0 ? s : ss[j - 1] + 1;
-            pp[j] = j == 0 ? ph : pp[j - 1];
-            if (ss[j] == n_d) {
-                ss[j] = 0;
-                pp[j] ^= 1u;
+            for (int q = 0; q < CPT; ++q) {
+                const int ch = t + q * kPassB;
+                if (ch < nchunk) cp_async_small<cb>(slot(k, q), row + (size_t)ch * cb, pol);
             }
+        };
+        for (int j = 0; j < K; ++j) {
+            if (j < n) issue(j, j);
+            cp_async_commit();
         }
+        int k = 0;
+        for (int i = 0; i < n; ++i) {
+            if (K == 8) cp_async_wait_group<7>();  // item i's group has landed
+            else if (K == 4) cp_async_wait_group<3>();
+            else cp_async_wait_group<1>();
+            ok = warp_wait_flag(&ctl.hready[i], a.limit_ns, ctl, a.status);
+            if (!ok) break;
+            const float hv = *reinterpret_cast<const volatile float*>(&ctl.h[i]);
 #pragma unroll
-        for (int j = 0; j < kPassBStep; ++j)
-            if (j < cnt && ok) ok = warp_wait(&ctl.d_full[ss[j]], pp[j], a.limit_ns, ctl, a.status);
-#pragma unroll
-        for (int j = 0; j < kPassBStep; ++j)
-            if (j < cnt && ok) ok = warp_wait_flag(&ctl.hready[i + j], a.limit_ns, ctl, a.status);
-        if (!ok) break;
-#pragma unroll
-        for (int j = 0; j < kPassBStep; ++j)
-            if (j < cnt)
-                add_row(d_ring + (size_t)ss[j] * d_bytes,
-                        *reinterpret_cast<const volatile float*>(&ctl.h[i + j]));
-        __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-            for (int j = 0; j < kPassBStep; ++j)
-                if (j < cnt) mbar_arrive(&ctl.d_empty[ss[j]]);
+            for (int q = 0; q < CPT; ++q)
+                if (t + q * kPassB < nchunk) acc_chunk(q, slot(k, q), hv);
+            if (i + K < n) issue(i + K, k);  // into the slot just read
+            cp_async_commit();
+            if (++k == K) k = 0;
         }
-        s += cnt;  // cnt <= n_d: at most one wrap
-        if (s >= n_d) {
-            s -= n_d;
-            ph ^= 1u;
+        cp_async_wait_group<0>();  // nothing in flight when the CTA leaves
+    } else {
+        // bf16: the W_down^T ring, one item per step (two per step, waiting
+        // for two of its 6 stages, measured slower)
+        int s = 0;         // stage of item i
+        uint32_t ph = 0;   // its phase parity
+        for (int i = 0; i < n; ++i) {
+            ok = warp_wait(&ctl.d_full[s], ph, a.limit_ns, ctl, a.status) &&
+                 warp_wait_flag(&ctl.hready[i], a.limit_ns, ctl, a.status);
+            if (!ok) break;
+            add_row(d_ring + (size_t)s * d_bytes, *reinterpret_cast<const volatile float*>(&ctl.h[i]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.d_empty[s]);
+            if (++s == n_d) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
     }
     if (t == 0) stamp_here(a.ts, 8);
@@ -1629,7 +1659,9 @@ size_t area_budget() { return kSmemLimit - ctl_bytes(); }
 // kGuRingBytes (bf16) or kGuRingBytesQ (int8, int4) and kMaxStages, consumed by
 // n_a = min(stages, kPassAWarps) pass-A warps (the stage count rounded down
 // to a multiple of n_a), then W_down^T stages up to kDRingBytes, both within
-// the shared memory left.  The bf16 caps keep ~160 KB in flight per SM:
+// the shared memory left; for codes, the pass-B slots of n_d items (8, 4 or
+// 2, at most a third of the area) come first.  The bf16 caps keep ~160 KB
+// in flight per SM:
 // enough to saturate HBM, and every extra byte in flight only lengthens the
 // queues that the channel selection's loads wait in.  Rows of int8 are half
 // as long, so their ring holds more of them; int4 rows a quarter, so theirs
@@ -1639,23 +1671,36 @@ size_t stage2_x_bytes(int d, int wq) { return (size_t)(wq ? 6 : 2) * d; }
 
 Ring ring_for(int d, int wq) {
     const size_t budget = area_budget() - stage2_x_bytes(d, wq);
-    const size_t gu = gu_row_bytes(d, wq), dd = down_row_bytes(d, wq);
+    const size_t gu = gu_row_bytes(d, wq);
     Ring r{0, 0, 0};
-    r.n_gu = (int)(min(budget * 2 / 3, wq ? kGuRingBytesQ : kGuRingBytes) / gu);
+    size_t dbytes = 0;  // the W_down^T stream
+    if (wq) {
+        // codes: n_d = items each pass-B thread streams ahead (8, 4 or 2),
+        // taking at most a third of the area
+        const size_t per = self_item_bytes(d, wq);
+        r.n_d = 8;
+        while (r.n_d > 2 && (size_t)r.n_d * per > budget / 3) r.n_d /= 2;
+        dbytes = (size_t)r.n_d * per;
+    }
+    const size_t room = budget > dbytes ? budget - dbytes : 0;
+    r.n_gu = (int)(min(wq ? room : budget * 2 / 3, wq ? kGuRingBytesQ : kGuRingBytes) / gu);
     if (r.n_gu > kMaxStages) r.n_gu = kMaxStages;
     if (r.n_gu < 1) r.n_gu = 1;
     r.n_a = r.n_gu < kPassAWarps ? r.n_gu : kPassAWarps;
     r.n_gu -= r.n_gu % r.n_a;
-    const size_t left = budget > (size_t)r.n_gu * gu ? budget - (size_t)r.n_gu * gu : 0;
-    r.n_d = (int)(min(left, kDRingBytes) / dd);
-    if (r.n_d > kMaxStages) r.n_d = kMaxStages;
-    if (r.n_d < 1 && left >= dd) r.n_d = 1;
+    if (!wq) {
+        const size_t dd = down_row_bytes(d, 0);
+        const size_t left = budget > (size_t)r.n_gu * gu ? budget - (size_t)r.n_gu * gu : 0;
+        r.n_d = (int)(min(left, kDRingBytes) / dd);
+        if (r.n_d > kMaxStages) r.n_d = kMaxStages;
+        if (r.n_d < 1 && left >= dd) r.n_d = 1;
+    }
     return r;
 }
 
 size_t ring_bytes(int d, int wq, const Ring& r) {
     return stage2_x_bytes(d, wq) + (size_t)r.n_gu * gu_row_bytes(d, wq) +
-           (size_t)r.n_d * down_row_bytes(d, wq);
+           (size_t)r.n_d * (wq ? self_item_bytes(d, wq) : down_row_bytes(d, wq));
 }
 
 template <typename K>
