@@ -32,11 +32,11 @@ def prox():
     return p
 
 
-@pytest.mark.parametrize("d,F,rho,q8", [(1024, 3000, 0.3, False), (4096, 14336, 0.3, False),
-                                        (1024, 3000, 0.3, True)])
-def test_no_alloc_matches_prox_ffn_twice(prox, d, F, rho, q8):
+@pytest.mark.parametrize("d,F,rho,wq", [(1024, 3000, 0.3, 0), (4096, 14336, 0.3, 0),
+                                        (1024, 3000, 0.3, 1), (1024, 3000, 0.3, 2)])
+def test_no_alloc_matches_prox_ffn_twice(prox, d, F, rho, wq):
     wg, wu, wd = synth.make_weights(d, F, 0.02, 51, device="cuda")
-    L = (prox.prox_prepare_q8 if q8 else prox.prox_prepare)(wg, wu, wd)
+    L = (prox.prox_prepare, prox.prox_prepare_q8, prox.prox_prepare_q4)[wq](wg, wu, wd)
     x = synth.make_x(d, max(1, d // 100), 20.0, 52).cuda()
     y_ref = prox.prox_ffn(L, x, rho).cpu().numpy().astype(np.float64)
     for _ in range(2):
