@@ -26,11 +26,13 @@
 //       b takes the positions [k b / n, k (b+1) / n) as its Stage-2 items
 //       (an even split: every CTA moves the same bytes).
 //   P3b Stage 2 (Eq. (1) of the PrunePath page restricted to the mask):
-//       gate|up rows and W_down^T rows arrive by bulk copies (TMA) into two
-//       shared-memory rings (bytes in flight capped); pass-A warps form
-//       h = silu(W_gate x) (W_up x) per item (one warp per row), pass-B
-//       warps own slices of d_model and accumulate h * W_down^T; one vector
-//       atomic per element adds the CTA's part of y at the end.
+//       gate|up rows arrive by bulk copies (TMA) into a shared-memory ring
+//       (bytes in flight capped), and so do bf16 W_down^T rows; for int8 or
+//       int4 rows every pass-B thread streams its own W_down^T slices with
+//       cp.async.  Pass-A warps form h = silu(W_gate x) (W_up x) per item
+//       (one warp per row), pass-B warps own slices of d_model and
+//       accumulate h * W_down^T; one vector atomic per element adds the
+//       CTA's part of y at the end.
 //   Stage-2 rows are bf16 (WQ = 0), or int8 (1) or int4 (2) codes with one
 //   fp32 scale per row: the codes are decoded exactly to fp32 and the scales
 //   are applied to g, u and h.
@@ -144,14 +146,12 @@ struct FusedParams {
 struct Ctl {
     uint64_t gu_full[kMaxStages], gu_empty[kMaxStages];
     uint64_t d_full[kMaxStages], d_empty[kMaxStages];
-    uint64_t sel_bar;                // completes when the item list is final
     uint64_t done_bar;               // every warp is through its Stage-2 role
     uint64_t ld_bar;                 // bulk load of the proxy scales (P1)
     uint64_t key_ld;                 // bulk load of every channel's score key
     int gu_last[kMaxStages], d_last[kMaxStages];
     float h[kMaxItems];              // h of each item
     int item[kMaxItems];             // channel of each item
-    uint8_t conf[kMaxItems];         // item is in the mask (pass B adds it)
     uint8_t hready[kMaxItems];       // h[i] written by pass A
     float lsc[kMaxChunk];            // scores of this CTA's chunk
     __align__(16) uint32_t warp_tot[(kNT / 32 + 4) / 4 * 4];  // per-warp totals, read as uint4
@@ -769,7 +769,6 @@ __device__ __forceinline__ void stage2_init(Ctl& ctl, int n_gu, int n_d, bool re
             mbar_inval(&ctl.d_full[s]);
             mbar_inval(&ctl.d_empty[s]);
         }
-        mbar_inval(&ctl.sel_bar);
         mbar_inval(&ctl.done_bar);
     }
     for (int s = 0; s < n_gu; ++s) {
@@ -782,7 +781,6 @@ __device__ __forceinline__ void stage2_init(Ctl& ctl, int n_gu, int n_d, bool re
         mbar_init(&ctl.d_empty[s], kPassBWarps);
         ctl.d_last[s] = -1;
     }
-    mbar_init(&ctl.sel_bar, 1);
     mbar_init(&ctl.done_bar, kNT / 32);
 }
 
@@ -1050,7 +1048,6 @@ __device__ bool select_items(const FusedParams& p, Ctl& ctl, uint8_t* area, int 
             for (int j = 0; j < bw; ++j, ++at) p.idx_list[at] = c + j;
         }
     }
-    for (int i = tid; i < q1 - q0; i += kNT) ctl.conf[i] = 1;
     if (tid == 0) ctl.n_items = q1 - q0;
     __syncthreads();
     return true;
@@ -1092,10 +1089,7 @@ __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8
         mbar_init(&ctl.key_ld, 1);
         fence_mbar_init();
     }
-    for (int i = tid; i < kMaxItems; i += kNT) {
-        ctl.conf[i] = 0;
-        ctl.hready[i] = 0;
-    }
+    for (int i = tid; i < kMaxItems; i += kNT) ctl.hready[i] = 0;
 
     // ------------------------------------------------ P0: input sparsity
     // area: x bf16 [d] | kept u32 [d] | histograms u32 [256 + 128] | P1 tables
@@ -1496,10 +1490,7 @@ __device__ __forceinline__ bool fused_step(const FusedParams& p, Ctl& ctl, uint8
         stamp(p.ts, 5);
         return true;
     }
-    if (tid == 0) {
-        mbar_arrive(&ctl.sel_bar);
-        stamp_here(p.ts, 5);
-    }
+    if (tid == 0) stamp_here(p.ts, 5);
     __syncthreads();
     Stage2Args a;
     a.gateup = p.gateup;
@@ -1623,14 +1614,12 @@ __global__ void __launch_bounds__(kNT, 1) k_dense(const Stage2Args a, const uint
         reinterpret_cast<uint4*>(area)[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
     for (int i = tid; i < kMaxItems; i += kNT) {
         ctl.item[i] = c0 + i;
-        ctl.conf[i] = i < n ? 1 : 0;
         ctl.hready[i] = 0;
     }
     if (tid == 0) {
         ctl.abort = 0;
         ctl.n_items = n;
         stage2_init(ctl, a.n_gu, a.n_d);
-        mbar_arrive(&ctl.sel_bar);  // the item list is final at once
         fence_mbar_init();
     }
     __syncthreads();
