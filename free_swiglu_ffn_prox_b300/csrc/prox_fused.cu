@@ -132,8 +132,9 @@ struct FusedParams {
     int32_t* kept_out;
     float* scores_out;
     int debug;           // write idx_list and hch
-    // stage-2 ring geometry: n_gu gate|up stages consumed by n_a pass-A
-    // warps (n_a divides n_gu), n_d W_down^T stages
+    // stage-2 geometry: n_gu gate|up stages consumed by n_a pass-A warps
+    // (n_a divides n_gu); n_d W_down^T stages (bf16), or for codes the items
+    // each pass-B thread streams ahead (8, 4 or 2)
     int n_gu, n_d, n_a;
     long long limit_ns;
     int inject;          // 1: the last CTA withholds its grid-barrier arrival (test hook)
@@ -403,7 +404,7 @@ struct Stage2Args {
     float* y;
     float* hch;     // [F] h per channel (debug, may be null)
     int* status;
-    int d, F, n_gu, n_d, n_a;
+    int d, F, n_gu, n_d, n_a;  // as in FusedParams
     long long limit_ns;
     uint64_t* ts;   // [gridDim][kPhaseStamps] or null
 };
@@ -787,8 +788,9 @@ __device__ __forceinline__ void stage2_init(Ctl& ctl, int n_gu, int n_d, bool re
 // End of the Stage-2 roles: every warp, once its lanes are through, arrives
 // on ctl.done_bar; thread 0 waits for all of them (the roles are warp-
 // specialised, so a block barrier is not used here), stamps the end and,
-// after an abort, lets the copies still in flight into the rings land
-// before the CTA leaves (bounded).
+// after an abort, lets the bulk copies still in flight into the rings land
+// before the CTA leaves (bounded).  Pass-B threads that stream code slices
+// wait for their own cp.async copies before they arrive.
 __device__ __forceinline__ void stage2_join(const Stage2Args& a, Ctl& ctl) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl.done_bar);
