@@ -758,7 +758,8 @@ def run_gpu(args):
                 "d_model": d, "d_ff": F, "keep_fraction": rho, "k": k, "input_keep": kappa,
                 "k_x": kx, "layer_copies": R, "hidden_states": N_X,
                 "l2": f"inputs larger than L2: steps cycle through {R} layer copies "
-                      f"({R} x {ab['step'] / 1e6:.1f} MB selected bytes >= 4 x {l2 / 2**20:.0f} MiB L2)",
+                      f"({R} x {ab['step'] / 1e6:.1f} MB = {R * ab['step'] / 1e6:.0f} MB of selected bytes, "
+                      f">= 4 x the {l2 / 2**20:.0f} MiB L2)",
                 "parallelism": "replicas" if ws > 1 else "single GPU",
                 "timing": "CUDA graphs of prox_ffn calls, events on the replay stream"},
             "roofline": roofline,
